@@ -1,0 +1,313 @@
+// api.cu -- the C ABI (include/attn46.h): argument checks, TMA descriptors, launches, the
+// device error word and its readback.  No computation of the method happens here.
+#include <atomic>
+#include <cmath>
+#include <cstdarg>
+#include <cstdint>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "attn46.h"
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace {
+
+using namespace ea46;
+
+thread_local char g_msg[512] = "";
+
+int fail(int code, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_msg, sizeof(g_msg), fmt, ap);
+  va_end(ap);
+  return code;
+}
+
+int ok() {
+  g_msg[0] = '\0';
+  return ATTN_OK;
+}
+
+std::atomic<long long> g_spin_limit{0};
+constexpr long long kDefaultSpin = 4000000000LL;
+
+long long spin_limit() {
+  const long long v = g_spin_limit.load();
+  return v > 0 ? v : kDefaultSpin;
+}
+
+// Device error word: [0] = first error code of the launches since the last attn_check,
+// [1] = where it happened.  One copy per device (module-scope device variable).
+__device__ int g_err_word[2];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+int* g_err_ptr[kMaxDevices] = {};
+
+int err_words(int** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+  if (dev < 0 || dev >= kMaxDevices) return fail(ATTN_ERR_UNSUPPORTED, "device index %d", dev);
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (g_err_ptr[dev] == nullptr) {
+    void* ptr = nullptr;
+    e = cudaGetSymbolAddress(&ptr, g_err_word);
+    if (e != cudaSuccess)
+      return fail(ATTN_ERR_CUDA, "cudaGetSymbolAddress(error word): %s", cudaGetErrorString(e));
+    g_err_ptr[dev] = static_cast<int*>(ptr);
+  }
+  *out = g_err_ptr[dev];
+  return ATTN_OK;
+}
+
+// ---- TMA descriptor encoding through the driver entry point (no link-time libcuda) ----
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// [B, S, H, D] tensor viewed as the 4-D box grid (D, H, S, B); one box = 128 tokens x one
+// swizzle panel of one head.
+int make_qkv_map(CUtensorMap* m, const void* ptr, int B, int S, int H, int D, bool fp8) {
+  EncodeTiledFn enc = encode_fn();
+  if (enc == nullptr) return fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled entry point unavailable");
+  const int esz = fp8 ? 1 : 2;
+  const int row_bytes = D * esz;
+  const int panel_row = row_bytes >= 128 ? 128 : row_bytes;
+  const cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H),
+                              static_cast<cuuint64_t>(S), static_cast<cuuint64_t>(B)};
+  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(D) * esz,
+                                 static_cast<cuuint64_t>(H) * D * esz,
+                                 static_cast<cuuint64_t>(S) * H * D * esz};
+  const cuuint32_t box[4] = {static_cast<cuuint32_t>(panel_row / esz), 1, 128, 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  const CUresult r = enc(m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                         4, const_cast<void*>(ptr), dims, strides, box, estr,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE,
+                         panel_row == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", int(r));
+  return ATTN_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool overlap(const void* a, size_t na, const void* b, size_t nb) {
+  const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+  return x < y + nb && y < x + na;
+}
+
+// Shape and pointer checks shared by the attention entry points.
+int check_attn_args(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                    int B, int H, int S, int D, int causal, float scale, int esz) {
+  if (q == nullptr || k == nullptr || v == nullptr || o == nullptr)
+    return fail(ATTN_ERR_INVALID_ARG, "q, k, v and o must be non-null device pointers");
+  if (B < 1 || H < 1 || S < 1)
+    return fail(ATTN_ERR_INVALID_ARG, "B, H, S must be >= 1 (got %d, %d, %d)", B, H, S);
+  if (D != 64 && D != 128 && D != 256)
+    return fail(D > 0 ? ATTN_ERR_UNSUPPORTED : ATTN_ERR_INVALID_ARG,
+                "head dimension D = %d not supported (64, 128, 256)", D);
+  if (causal != 0 && causal != 1) return fail(ATTN_ERR_INVALID_ARG, "causal must be 0 or 1");
+  if (!std::isfinite(scale) || scale < 0.f)
+    return fail(ATTN_ERR_INVALID_ARG, "scale must be finite and >= 0 (0 selects 1/sqrt(D))");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o))
+    return fail(ATTN_ERR_INVALID_ARG, "q, k, v and o must be 16-byte aligned");
+  if (lse != nullptr && (reinterpret_cast<uintptr_t>(lse) & 3u) != 0)
+    return fail(ATTN_ERR_INVALID_ARG, "lse must be 4-byte aligned");
+  const unsigned long long n = 1ull * B * S * H * D;
+  if (n > (1ull << 40) / 2)
+    return fail(ATTN_ERR_INVALID_ARG, "tensor too large (%llu elements)", n);
+  const unsigned long long rows_per_cta = 128ull * attn_q_tiles(D);
+  const unsigned long long grid = 1ull * ((S + rows_per_cta - 1) / rows_per_cta) * H * B;
+  if (grid > 0x7fffffffull) return fail(ATTN_ERR_INVALID_ARG, "too many query blocks");
+  const size_t in_bytes = n * esz, out_bytes = n * 2;
+  if (overlap(o, out_bytes, q, in_bytes) || overlap(o, out_bytes, k, in_bytes) ||
+      overlap(o, out_bytes, v, in_bytes))
+    return fail(ATTN_ERR_INVALID_ARG, "o overlaps an input");
+  if (lse != nullptr) {
+    const size_t lse_bytes = 4ull * B * H * S;
+    if (overlap(lse, lse_bytes, o, out_bytes) || overlap(lse, lse_bytes, q, in_bytes) ||
+        overlap(lse, lse_bytes, k, in_bytes) || overlap(lse, lse_bytes, v, in_bytes))
+      return fail(ATTN_ERR_INVALID_ARG, "lse overlaps another tensor");
+  }
+  return ATTN_OK;
+}
+
+template <bool FP8>
+int dispatch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+             const AttnParams& p, int D, int causal, cudaStream_t st) {
+  cudaError_t e = cudaErrorInvalidValue;
+  switch (D * 2 + causal) {
+    case 64 * 2 + 0: e = launch_attn<64, FP8, false>(tq, tk, tv, p, st); break;
+    case 64 * 2 + 1: e = launch_attn<64, FP8, true>(tq, tk, tv, p, st); break;
+    case 128 * 2 + 0: e = launch_attn<128, FP8, false>(tq, tk, tv, p, st); break;
+    case 128 * 2 + 1: e = launch_attn<128, FP8, true>(tq, tk, tv, p, st); break;
+    case 256 * 2 + 0: e = launch_attn<256, FP8, false>(tq, tk, tv, p, st); break;
+    case 256 * 2 + 1: e = launch_attn<256, FP8, true>(tq, tk, tv, p, st); break;
+    default: break;
+  }
+  if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "attention launch failed: %s", cudaGetErrorString(e));
+  return ok();
+}
+
+int run_attn(const void* q, const void* k, const void* v, const float* qs, const float* ks,
+             const float* vs, void* o, float* lse, int B, int H, int S, int D, int causal,
+             float scale, bool fp8, void* stream) {
+  int rc = check_attn_args(q, k, v, o, lse, B, H, S, D, causal, scale, fp8 ? 1 : 2);
+  if (rc != ATTN_OK) return rc;
+  int* err = nullptr;
+  if ((rc = err_words(&err)) != ATTN_OK) return rc;
+  CUtensorMap tq, tk, tv;
+  if ((rc = make_qkv_map(&tq, q, B, S, H, D, fp8)) != ATTN_OK) return rc;
+  if ((rc = make_qkv_map(&tk, k, B, S, H, D, fp8)) != ATTN_OK) return rc;
+  if ((rc = make_qkv_map(&tv, v, B, S, H, D, fp8)) != ATTN_OK) return rc;
+  AttnParams p{};
+  p.B = B;
+  p.H = H;
+  p.S = S;
+  const int rows_per_cta = 128 * attn_q_tiles(D);
+  p.nQB = (S + rows_per_cta - 1) / rows_per_cta;
+  p.nK = (S + 127) / 128;
+  const float sc = scale > 0.f ? scale : 1.0f / std::sqrt(static_cast<float>(D));
+  p.c_log2 = sc * 1.4426950408889634f;
+  p.o = o;
+  p.lse = lse;
+  p.q_scale = qs;
+  p.k_scale = ks;
+  p.v_scale = vs;
+  p.spin_limit = spin_limit();
+  p.err_word = err;
+  p.err_info = err + 1;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  return fp8 ? dispatch<true>(tq, tk, tv, p, D, causal, st)
+             : dispatch<false>(tq, tk, tv, p, D, causal, st);
+}
+
+// One thread waits on a barrier that nothing arrives at; the bounded wait records a timeout.
+__global__ void selftest_wait_kernel(long long limit, int* err) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    abort_flag = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const WaitCtl ctl{limit, &abort_flag, err, err + 1};
+    (void)wait_bounded(smem_u32(&bar), 0, ctl, 99);
+  }
+  __syncthreads();
+}
+
+}  // namespace
+
+extern "C" {
+
+int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+             int S, int D, int causal, float scale, int dtype, void* stream) {
+  if (dtype != ATTN_BF16 && dtype != ATTN_FP8_E4M3)
+    return fail(ATTN_ERR_INVALID_ARG, "dtype must be ATTN_BF16 (0) or ATTN_FP8_E4M3 (1)");
+  return run_attn(q, k, v, nullptr, nullptr, nullptr, o, lse, B, H, S, D, causal, scale,
+                  dtype == ATTN_FP8_E4M3, stream);
+}
+
+int attn_fwd_fp8(const void* q8, const void* k8, const void* v8, const float* q_scale,
+                 const float* k_scale, const float* v_scale, void* o, float* lse, int B, int H,
+                 int S, int D, int causal, float scale, void* stream) {
+  if (q_scale == nullptr || k_scale == nullptr || v_scale == nullptr)
+    return fail(ATTN_ERR_INVALID_ARG, "q_scale, k_scale and v_scale must be non-null");
+  if ((reinterpret_cast<uintptr_t>(q_scale) | reinterpret_cast<uintptr_t>(k_scale) |
+       reinterpret_cast<uintptr_t>(v_scale)) & 3u)
+    return fail(ATTN_ERR_INVALID_ARG, "scale arrays must be 4-byte aligned");
+  return run_attn(q8, k8, v8, q_scale, k_scale, v_scale, o, lse, B, H, S, D, causal, scale,
+                  true, stream);
+}
+
+int hadamard_rotate_quant_fp8(const void* x, void* out, float* scale, const float* signs, int B,
+                              int H, int S, int D, void* stream) {
+  if (x == nullptr || out == nullptr || scale == nullptr)
+    return fail(ATTN_ERR_INVALID_ARG, "x, out and scale must be non-null device pointers");
+  if (B < 1 || H < 1 || S < 1)
+    return fail(ATTN_ERR_INVALID_ARG, "B, H, S must be >= 1 (got %d, %d, %d)", B, H, S);
+  if (D != 64 && D != 128 && D != 256)
+    return fail(D > 0 ? ATTN_ERR_UNSUPPORTED : ATTN_ERR_INVALID_ARG,
+                "head dimension D = %d not supported (64, 128, 256)", D);
+  if (!aligned16(x) || !aligned16(out) || (signs != nullptr && !aligned16(signs)) ||
+      (reinterpret_cast<uintptr_t>(scale) & 3u))
+    return fail(ATTN_ERR_INVALID_ARG, "x, out, signs must be 16-byte and scale 4-byte aligned");
+  const unsigned long long n = 1ull * B * S * H * D;
+  const int nblk = (S + 127) / 128;
+  if (n > (1ull << 40) / 2 || nblk > 0x7fffffff || H > 65535 || B > 65535)
+    return fail(ATTN_ERR_INVALID_ARG, "tensor too large for the grid");
+  const size_t sbytes = 4ull * B * H * nblk;
+  if (overlap(out, n, x, 2 * n) || overlap(scale, sbytes, x, 2 * n) || overlap(scale, sbytes, out, n))
+    return fail(ATTN_ERR_INVALID_ARG, "outputs overlap the input or each other");
+  QuantParams p{B, H, S, nblk, x, out, scale, signs};
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = D == 64    ? launch_hadamard_quant<64>(p, st)
+                  : D == 128 ? launch_hadamard_quant<128>(p, st)
+                             : launch_hadamard_quant<256>(p, st);
+  if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "quantiser launch failed: %s", cudaGetErrorString(e));
+  return ok();
+}
+
+const char* attn_get_last_error(void) { return g_msg; }
+
+int attn_check(void* stream) {
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "stream synchronize: %s", cudaGetErrorString(e));
+  int* err = nullptr;
+  int rc = err_words(&err);
+  if (rc != ATTN_OK) return rc;
+  int host[2] = {0, 0};
+  e = cudaMemcpy(host, err, sizeof(host), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "error word readback: %s", cudaGetErrorString(e));
+  if (host[0] != 0) {
+    e = cudaMemset(err, 0, sizeof(host));
+    if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "error word reset: %s", cudaGetErrorString(e));
+    e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "error word reset: %s", cudaGetErrorString(e));
+    return fail(host[0], "a kernel's bounded wait ran out (code %d, site %d)", host[0], host[1]);
+  }
+  return ok();
+}
+
+void attn_set_spin_limit(long long cycles) { g_spin_limit.store(cycles > 0 ? cycles : 0); }
+
+int attn_selftest_bounded_wait(long long spin_cycles, void* stream) {
+  if (spin_cycles <= 0) return fail(ATTN_ERR_INVALID_ARG, "spin_cycles must be > 0");
+  int* err = nullptr;
+  int rc = err_words(&err);
+  if (rc != ATTN_OK) return rc;
+  selftest_wait_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(spin_cycles, err);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "self-test launch: %s", cudaGetErrorString(e));
+  return ok();
+}
+
+int attn_version(void) { return 100; }
+
+}  // extern "C"

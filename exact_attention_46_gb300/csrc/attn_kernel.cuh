@@ -1,0 +1,510 @@
+// attn_kernel.cuh -- fused exact-attention forward for sm_103a (tcgen05 + TMA + Tensor Memory).
+//
+// What it computes (hada.io FA3 summary, "Rückblick auf den FlashAttention-Ansatz" and
+// "Überlappung von GEMM und Softmax"): for every query row, O = softmax(scale * q K^T) V over
+// the visible keys and lse = log sum exp, reading Q, K, V once per query block and never
+// writing the score matrix to device memory.  The softmax is computed tile by tile with a
+// running max and running sum (softmax rescaling), which reaches the exact result.
+//
+// How it maps to GB300 (own design; the pages' Hopper schedule -- WGMMA warpgroups,
+// ping-pong between two consumer warpgroups, intra-warpgroup overlap -- is prior art):
+//
+//   CTA = NT query tiles of 128 rows of one (b, h)   (NT = 2, or 1 at D = 256)
+//   warps 0 .. 4*NT-1  : softmax; warp w owns query tile w/4 and Tensor-Memory lanes
+//                        32*(w%4) .. +31, i.e. thread = one query row, so row max / row sum
+//                        need no shuffles
+//   warp 4*NT          : TMA producer: Q tiles once, then K_0, V_0, K_1, V_1, ... into a ring
+//                        of NSLOT shared-memory slots (full / empty mbarriers)
+//   warp 4*NT+1        : MMA issuer (one thread): S_t = Q_t K_j^T into Tensor Memory
+//                        (tcgen05.mma, operands from shared memory), then O_t += P_t V_j with
+//                        P_t read from Tensor Memory where the softmax warps wrote it over S_t
+//
+//   Issue order per key tile j: PV_0(j-1), S_0(j), PV_1(j-1), S_1(j).  While the softmax of
+//   tile 0 works on S_0(j), the tensor core runs PV_1(j-1) and S_1(j), and the other way
+//   round: the two query tiles alternate between the tensor pipe and the exp/ALU pipes (the
+//   role the pages' ping-pong plays on Hopper), with accumulators in Tensor Memory instead
+//   of registers.
+//
+//   Tensor Memory (512 columns x 128 lanes x 32 bit): S_t at column 128*t (P_t overwrites its
+//   first 64 (bf16) or 32 (E4M3) columns), O_t at 128*NT + D*t.
+//
+//   The running max is only raised when a tile's max exceeds it by more than TAU = 8 (log2
+//   units); otherwise the stale max is kept, numerators stay below 2^8, and O and l need no
+//   rescaling.  The result is the same function (the max cancels between numerator and l);
+//   the rescale of O in Tensor Memory is done by the softmax warp that owns the rows, in the
+//   window where S_t(j) is ready and PV_t(j) has not been issued.
+//
+//   FP8 (E4M3) inputs carry one scale per (b, h, 128-token block): the logit multiplier of a
+//   tile is scale*log2e*sq*sk_j; V's block scale sv_j enters as a per-tile factor
+//   r_j = sv_j / max_j sv_j <= 1 folded into the exponent (p' = 2^(x - m + log2 r_j)), the row
+//   sum adds sum(p') / r_j, and the epilogue multiplies by max_j sv_j / l.
+//
+// Every mbarrier wait is bounded (ptx.cuh, wait_bounded): a wait that runs out records
+// ATTN_ERR_TIMEOUT in the device error word, raises the CTA's abort flag, and every role then
+// drains its in-flight copies / MMAs and leaves through the common exit, which frees Tensor
+// Memory.
+#pragma once
+
+#include <atomic>
+#include <cfloat>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_bf16.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace ea46 {
+
+template <int D, bool FP8>
+struct AttnCfg {
+  static constexpr int NT = attn_q_tiles(D);
+  static constexpr int ESZ = FP8 ? 1 : 2;
+  static constexpr int ROW_BYTES = D * ESZ;                    // one token-head row
+  static constexpr int PANEL_ROW = ROW_BYTES >= 128 ? 128 : ROW_BYTES;  // swizzle span
+  static constexpr int NPANEL = ROW_BYTES / PANEL_ROW;
+  static constexpr int PANEL_ELEMS = PANEL_ROW / ESZ;
+  static constexpr int PANEL_BYTES = 128 * PANEL_ROW;          // 128 rows of one panel
+  static constexpr int TILE_BYTES = 128 * ROW_BYTES;
+  static constexpr uint32_t LAYOUT = PANEL_ROW == 128 ? 2u : 4u;   // SW128 / SW64
+  static constexpr uint32_t SBO = 8 * PANEL_ROW;               // stride of 8-row groups
+  static constexpr int SMEM_TILES_BUDGET = 200 * 1024;
+  static constexpr int NSLOT_RAW = (SMEM_TILES_BUDGET - NT * TILE_BYTES) / TILE_BYTES;
+  static constexpr int NSLOT = NSLOT_RAW > 8 ? 8 : NSLOT_RAW;
+  static constexpr int NBAR = 1 + 2 * NSLOT + 3 * NT + 1;
+  static constexpr int SMEM_BYTES_RAW = (NT + NSLOT) * TILE_BYTES + NBAR * 8 + 16;
+  // Request at least ~120 KB so that one CTA (and its 512 TMEM columns) owns the SM.
+  static constexpr int SMEM_BYTES =
+      (SMEM_BYTES_RAW > 120 * 1024 ? SMEM_BYTES_RAW : 120 * 1024) + 1024;
+  static constexpr int NUM_SOFTMAX_WARPS = 4 * NT;
+  static constexpr int LOAD_WARP = NUM_SOFTMAX_WARPS;
+  static constexpr int MMA_WARP = NUM_SOFTMAX_WARPS + 1;
+  static constexpr int THREADS = 32 * (NUM_SOFTMAX_WARPS + 2);
+  static constexpr uint32_t TMEM_COLS = 512;
+  static constexpr int UMMA_K = FP8 ? 32 : 16;                 // K per MMA instruction
+  static constexpr int KSTEPS_QK = ROW_BYTES / 32;             // 32 bytes of K per step
+  static constexpr int STEPS_PER_PANEL = PANEL_ROW / 32;
+  static constexpr int KSTEPS_PV = 128 / UMMA_K;
+  static constexpr int P_COLS = 128 * ESZ / 4;                 // packed P columns (64 / 32)
+  static constexpr uint32_t FMT = FP8 ? 0u : 1u;               // E4M3 / BF16
+  static constexpr uint32_t IDESC_QK = instr_desc(FMT, 0, 128, 128);
+  static constexpr uint32_t IDESC_PV = instr_desc(FMT, 1, 128, D);
+  static_assert(128 * NT + D * NT <= 512, "Tensor Memory budget");
+  static_assert(NSLOT >= 2, "need a K and a V slot");
+  static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
+};
+
+// Where a bounded wait gave up (reported in the error info word).
+enum : int { WHERE_LOAD = 1, WHERE_MMA = 2, WHERE_SOFTMAX = 3, WHERE_DRAIN = 4 };
+
+constexpr float TAU = 8.0f;          // log2 units a tile max may exceed the running max
+constexpr float LN2 = 0.69314718055994530942f;
+
+// Wait that ignores the abort flag: used only to drain in-flight work before exit.
+__device__ __forceinline__ void wait_drain(uint32_t bar, uint32_t parity, long long limit) {
+  if (mbar_try_wait(bar, parity)) return;
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity)) {
+    if (clock64() - t0 > limit) return;
+  }
+}
+
+template <int D, bool FP8, bool CAUSAL>
+__global__ void __launch_bounds__(AttnCfg<D, FP8>::THREADS, 1)
+    attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                    const __grid_constant__ CUtensorMap tmV, const AttnParams p) {
+  using C = AttnCfg<D, FP8>;
+  constexpr int NT = C::NT;
+  constexpr int NSLOT = C::NSLOT;
+
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_u32 = smem_u32(smem_raw);
+  const uint32_t base_u32 = (raw_u32 + 1023u) & ~1023u;
+  uint8_t* base = smem_raw + (base_u32 - raw_u32);
+  const uint32_t sQ = base_u32;                                  // NT tiles
+  const uint32_t sKV = base_u32 + NT * C::TILE_BYTES;            // NSLOT tiles
+  const uint32_t bar0 = sKV + NSLOT * C::TILE_BYTES;             // barriers (8 B each)
+  uint8_t* bar_ptr = base + (bar0 - base_u32);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_ptr + C::NBAR * 8);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  auto BAR_Q = [&]() { return bar0; };
+  auto BAR_KV_FULL = [&](int s) { return bar0 + 8u * (1 + s); };
+  auto BAR_KV_EMPTY = [&](int s) { return bar0 + 8u * (1 + NSLOT + s); };
+  auto BAR_S_FULL = [&](int t) { return bar0 + 8u * (1 + 2 * NSLOT + t); };
+  auto BAR_P_FULL = [&](int t) { return bar0 + 8u * (1 + 2 * NSLOT + NT + t); };
+  auto BAR_O_FULL = [&](int t) { return bar0 + 8u * (1 + 2 * NSLOT + 2 * NT + t); };
+  auto BAR_MMA_DONE = [&]() { return bar0 + 8u * (1 + 2 * NSLOT + 3 * NT); };
+
+  const uint32_t warp = warp_id();
+  const uint32_t lane = lane_id();
+
+  if (threadIdx.x == 0) {
+    mbar_init(BAR_Q(), 1);
+    for (int s = 0; s < NSLOT; ++s) {
+      mbar_init(BAR_KV_FULL(s), 1);
+      mbar_init(BAR_KV_EMPTY(s), 1);
+    }
+    for (int t = 0; t < NT; ++t) {
+      mbar_init(BAR_S_FULL(t), 1);
+      mbar_init(BAR_P_FULL(t), 4);
+      mbar_init(BAR_O_FULL(t), 1);
+    }
+    mbar_init(BAR_MMA_DONE(), 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == C::MMA_WARP) tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
+  if (warp == C::LOAD_WARP && lane == 0) {
+    prefetch_tmap(&tmQ);
+    prefetch_tmap(&tmK);
+    prefetch_tmap(&tmV);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  // ---- work item: (query block, head, batch) ----
+  const int HB = p.H * p.B;
+  int qb, hb;
+  if (CAUSAL) {            // heaviest query blocks first
+    qb = p.nQB - 1 - static_cast<int>(blockIdx.x / HB);
+    hb = static_cast<int>(blockIdx.x % HB);
+  } else {                 // query blocks of one head adjacent (K/V reuse in L2)
+    qb = static_cast<int>(blockIdx.x % p.nQB);
+    hb = static_cast<int>(blockIdx.x / p.nQB);
+  }
+  const int h = hb % p.H;
+  const int b = hb / p.H;
+  const int q0 = qb * 128 * NT;
+  int n_t[NT];
+  int nmax = 0;
+#pragma unroll
+  for (int t = 0; t < NT; ++t) {
+    const int r0 = q0 + 128 * t;
+    n_t[t] = (r0 >= p.S) ? 0 : (CAUSAL ? (r0 / 128 + 1) : p.nK);
+    nmax = n_t[t] > nmax ? n_t[t] : nmax;
+  }
+
+  const WaitCtl ctl{p.spin_limit, abort_flag, p.err_word, p.err_info};
+
+  if (warp == C::LOAD_WARP) {
+    // ======================================================== TMA producer ==
+    if (lane == 0) {
+      const uint64_t pol_q = l2_policy_evict_first();
+      const uint64_t pol_kv = l2_policy_evict_last();
+      uint32_t qbytes = 0;
+#pragma unroll
+      for (int t = 0; t < NT; ++t) qbytes += n_t[t] > 0 ? C::TILE_BYTES : 0;
+      mbar_arrive_expect_tx(BAR_Q(), qbytes);
+#pragma unroll
+      for (int t = 0; t < NT; ++t) {
+        if (n_t[t] == 0) continue;
+#pragma unroll
+        for (int pn = 0; pn < C::NPANEL; ++pn)
+          tma_load_4d(sQ + t * C::TILE_BYTES + pn * C::PANEL_BYTES, &tmQ, BAR_Q(),
+                      pn * C::PANEL_ELEMS, h, q0 + 128 * t, b, pol_q);
+      }
+      int issued = 0;
+      for (int j = 0; j < nmax && !*abort_flag; ++j) {
+        for (int kind = 0; kind < 2; ++kind) {
+          const int slot = issued % NSLOT;
+          const uint32_t phase = (issued / NSLOT) & 1;
+          if (!wait_bounded(BAR_KV_EMPTY(slot), phase ^ 1u, ctl, WHERE_LOAD)) break;
+          mbar_arrive_expect_tx(BAR_KV_FULL(slot), C::TILE_BYTES);
+          const CUtensorMap* m = kind == 0 ? &tmK : &tmV;
+#pragma unroll
+          for (int pn = 0; pn < C::NPANEL; ++pn)
+            tma_load_4d(sKV + slot * C::TILE_BYTES + pn * C::PANEL_BYTES, m, BAR_KV_FULL(slot),
+                        pn * C::PANEL_ELEMS, h, 128 * j, b, pol_kv);
+          ++issued;
+        }
+      }
+      if (*abort_flag) {
+        // Drain: every copy still in flight must land before the CTA may exit.
+        wait_drain(BAR_Q(), 0, p.spin_limit);
+        const int first = issued > NSLOT ? issued - NSLOT : 0;
+        for (int i = first; i < issued; ++i)
+          wait_drain(BAR_KV_FULL(i % NSLOT), (i / NSLOT) & 1, p.spin_limit);
+      }
+    }
+  } else if (warp == C::MMA_WARP) {
+    // ========================================================== MMA issuer ==
+    if (lane == 0) {
+      int consumed = 0;   // ring position
+      bool ok = wait_bounded(BAR_Q(), 0, ctl, WHERE_MMA);
+      tc_fence_after();
+      auto gemm_qk = [&](int t, int slot) {
+        const uint32_t d = tmem + 128u * t;
+#pragma unroll
+        for (int kk = 0; kk < C::KSTEPS_QK; ++kk) {
+          const uint32_t off =
+              (kk / C::STEPS_PER_PANEL) * C::PANEL_BYTES + (kk % C::STEPS_PER_PANEL) * 32;
+          const uint64_t a = smem_desc(sQ + t * C::TILE_BYTES + off, 16, C::SBO, C::LAYOUT);
+          const uint64_t bd = smem_desc(sKV + slot * C::TILE_BYTES + off, 16, C::SBO, C::LAYOUT);
+          if (FP8) mma_f8_ss(d, a, bd, C::IDESC_QK, kk > 0);
+          else     mma_f16_ss(d, a, bd, C::IDESC_QK, kk > 0);
+        }
+      };
+      auto gemm_pv = [&](int t, int slot, bool acc) {
+        const uint32_t d = tmem + 128u * NT + static_cast<uint32_t>(D) * t;
+#pragma unroll
+        for (int kk = 0; kk < C::KSTEPS_PV; ++kk) {
+          const uint32_t a = tmem + 128u * t + 8u * kk;
+          const uint64_t bd = smem_desc(sKV + slot * C::TILE_BYTES + kk * C::UMMA_K * C::PANEL_ROW,
+                                        C::PANEL_BYTES, C::SBO, C::LAYOUT);
+          if (FP8) mma_f8_ts(d, a, bd, C::IDESC_PV, (acc || kk > 0) ? 1u : 0u);
+          else     mma_f16_ts(d, a, bd, C::IDESC_PV, (acc || kk > 0) ? 1u : 0u);
+        }
+      };
+      if (ok) {
+        const int ks = consumed % NSLOT;
+        ok = wait_bounded(BAR_KV_FULL(ks), (consumed / NSLOT) & 1, ctl, WHERE_MMA);
+        ++consumed;
+        if (ok) {
+          tc_fence_after();
+#pragma unroll
+          for (int t = 0; t < NT; ++t) {
+            if (n_t[t] > 0) {
+              gemm_qk(t, ks);
+              mma_commit(BAR_S_FULL(t));
+            }
+          }
+          mma_commit(BAR_KV_EMPTY(ks));
+        }
+      }
+      for (int j = 1; ok && j <= nmax; ++j) {
+        const int vs = consumed % NSLOT;
+        ok = wait_bounded(BAR_KV_FULL(vs), (consumed / NSLOT) & 1, ctl, WHERE_MMA);
+        ++consumed;
+        if (!ok) break;
+        tc_fence_after();
+        int ks = -1;   // K_j is waited for only right before the first S(j) that needs it
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+          if (j - 1 < n_t[t]) {
+            if (!wait_bounded(BAR_P_FULL(t), (j - 1) & 1, ctl, WHERE_MMA)) { ok = false; break; }
+            tc_fence_after();
+            gemm_pv(t, vs, j - 1 > 0);
+            if (j - 1 == n_t[t] - 1) mma_commit(BAR_O_FULL(t));
+          }
+          if (t == NT - 1) mma_commit(BAR_KV_EMPTY(vs));
+          if (j < n_t[t]) {
+            if (ks < 0) {
+              ks = consumed % NSLOT;
+              if (!wait_bounded(BAR_KV_FULL(ks), (consumed / NSLOT) & 1, ctl, WHERE_MMA)) { ok = false; break; }
+              ++consumed;
+              tc_fence_after();
+            }
+            gemm_qk(t, ks);
+            mma_commit(BAR_S_FULL(t));
+          }
+        }
+        if (ok && ks >= 0) mma_commit(BAR_KV_EMPTY(ks));
+      }
+      // Drain: all issued MMAs complete before Tensor Memory is freed.
+      mma_commit(BAR_MMA_DONE());
+      wait_drain(BAR_MMA_DONE(), 0, p.spin_limit);
+    }
+  } else {
+    // ============================================================= softmax ==
+    const int t = static_cast<int>(warp) / 4;
+    const int wq = static_cast<int>(warp) % 4;
+    const int row_local = wq * 32 + static_cast<int>(lane);
+    const int row = q0 + 128 * t + row_local;
+    const uint32_t tl = tmem + (static_cast<uint32_t>(wq * 32) << 16);
+    const uint32_t s_addr = tl + 128u * t;
+    const uint32_t o_addr = tl + 128u * NT + static_cast<uint32_t>(D) * t;
+    const int nt = (q0 + 128 * t >= p.S) ? 0 : (CAUSAL ? ((q0 + 128 * t) / 128 + 1) : p.nK);
+    const size_t blk_base = static_cast<size_t>(hb) * p.nK;   // (b*H + h) * nK
+
+    float sq = 1.f, sv_max = 1.f;
+    if (FP8) {
+      if (p.q_scale != nullptr && nt > 0) sq = p.q_scale[blk_base + (q0 + 128 * t) / 128];
+      if (p.v_scale != nullptr) {
+        sv_max = 0.f;
+        for (int j = 0; j < p.nK; ++j) sv_max = fmaxf(sv_max, p.v_scale[blk_base + j]);
+      }
+    }
+
+    float m_run = -INFINITY;
+    float l_run = 0.f;
+    bool ok = true;
+    for (int j = 0; j < nt; ++j) {
+      if (!wait_bounded(BAR_S_FULL(t), j & 1, ctl, WHERE_SOFTMAX)) { ok = false; break; }
+      tc_fence_after();
+      uint32_t sr[4][32];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmem_ld32(s_addr + 32u * c, sr[c]);
+      tmem_wait_ld();
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+#pragma unroll
+        for (int i = 0; i < 32; ++i) reg_fence(sr[c][i]);
+
+      float cmul = p.c_log2, bias = 0.f, inv_r = 1.f;
+      if (FP8) {
+        const float sk = p.k_scale != nullptr ? p.k_scale[blk_base + j] : 1.f;
+        const float sv = p.v_scale != nullptr ? p.v_scale[blk_base + j] : 1.f;
+        cmul *= sq * sk;
+        const float r = sv / sv_max;
+        bias = __log2f(r);
+        inv_r = sv_max / sv;
+      }
+
+      // masks: causal diagonal tile, or the ragged last key tile
+      if (CAUSAL ? (j == nt - 1) : (j == p.nK - 1 && (p.S & 127) != 0)) {
+        const int lim = CAUSAL ? (row - 128 * j) : (p.S - 128 * j - 1);   // last visible column
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            if (32 * c + i > lim) sr[c][i] = __float_as_uint(-INFINITY);
+      }
+
+      float mx[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) mx[k] = __uint_as_float(sr[k / 2][(k % 2) * 16]);
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const int k = (c * 2 + i / 16) & 7;
+          mx[k] = fmaxf(mx[k], __uint_as_float(sr[c][i]));
+        }
+      const float m_tile =
+          fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * cmul;
+
+      bool rescale = false;
+      float alpha = 1.f;
+      if (j == 0) {
+        m_run = m_tile;
+      } else if (m_tile > m_run + TAU) {
+        alpha = ex2(m_run - m_tile);
+        m_run = m_tile;
+        l_run *= alpha;
+        rescale = true;
+      }
+      const float nb = bias - m_run;
+      float ls[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) ls[k] = 0.f;
+      if (!FP8) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float p0 = ex2(fmaf(__uint_as_float(sr[c][2 * i]), cmul, nb));
+            const float p1 = ex2(fmaf(__uint_as_float(sr[c][2 * i + 1]), cmul, nb));
+            ls[(2 * i) & 7] += p0;
+            ls[(2 * i + 1) & 7] += p1;
+            pk[i] = pack_bf16x2(p0, p1);
+          }
+          tmem_st16(s_addr + 16u * c, pk);
+        }
+      } else {
+#pragma unroll
+        for (int h2 = 0; h2 < 2; ++h2) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            float pv[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int col = 64 * h2 + 4 * i + e;
+              pv[e] = ex2(fmaf(__uint_as_float(sr[col / 32][col % 32]), cmul, nb));
+              ls[(4 * i + e) & 7] += pv[e];
+            }
+            pk[i] = pack_e4m3x4(pv[0], pv[1], pv[2], pv[3]);
+          }
+          tmem_st16(s_addr + 16u * h2, pk);
+        }
+      }
+      l_run += (((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]))) * inv_r;
+      if (__any_sync(0xffffffffu, rescale)) {
+        // O_t holds PV_t(j-1) complete (it preceded S_t(j)); PV_t(j) waits for this warp's
+        // arrival below, so O_t can be rescaled in place now (S_t's registers are dead here).
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld32(o_addr + 32u * c, o);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            reg_fence(o[i]);
+            o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+          }
+          tmem_st32(o_addr + 32u * c, o);
+        }
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(BAR_P_FULL(t));
+    }
+
+    // ---- epilogue: O / l -> bf16, lse ----
+    if (ok && nt > 0 && wait_bounded(BAR_O_FULL(t), 0, ctl, WHERE_SOFTMAX)) {
+      tc_fence_after();
+      const float inv_l = sv_max / l_run;
+      const bool valid = row < p.S;
+      __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(p.o) +
+                            ((static_cast<size_t>(b) * p.S + (valid ? row : 0)) * p.H + h) * D;
+#pragma unroll 1
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t o[32];
+        tmem_ld32(o_addr + 32u * c, o);
+        tmem_wait_ld();
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          reg_fence(o[2 * i]);
+          reg_fence(o[2 * i + 1]);
+          pk[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
+        }
+        if (valid) {
+          uint4* dst = reinterpret_cast<uint4*>(orow + 32 * c);
+#pragma unroll
+          for (int v4 = 0; v4 < 4; ++v4)
+            dst[v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
+        }
+      }
+      if (valid && p.lse != nullptr)
+        p.lse[static_cast<size_t>(hb) * p.S + row] = (m_run + __log2f(l_run)) * LN2;
+    }
+  }
+
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == C::MMA_WARP) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+template <int D, bool FP8, bool CAUSAL>
+cudaError_t launch_attn(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                        const AttnParams& p, cudaStream_t stream) {
+  using C = AttnCfg<D, FP8>;
+  static std::atomic<unsigned long long> configured{0};   // one bit per device
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const unsigned long long bit = 1ull << (dev & 63);
+  if ((configured.load() & bit) == 0) {
+    e = cudaFuncSetAttribute(attn_fwd_kernel<D, FP8, CAUSAL>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    configured.fetch_or(bit);
+  }
+  const long long grid = static_cast<long long>(p.nQB) * p.H * p.B;
+  attn_fwd_kernel<D, FP8, CAUSAL>
+      <<<static_cast<unsigned>(grid), C::THREADS, C::SMEM_BYTES, stream>>>(tq, tk, tv, p);
+  return cudaGetLastError();
+}
+
+}  // namespace ea46

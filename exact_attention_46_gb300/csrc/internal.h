@@ -1,0 +1,46 @@
+// internal.h -- declarations shared by the C-ABI layer and the kernel translation units.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace ea46 {
+
+// Per-launch parameters of the attention kernels (plain values and device pointers).
+struct AttnParams {
+  int B, H, S;
+  int nQB;              // query blocks of 128 * NT rows per (b, h)
+  int nK;               // key tiles of 128 = ceil(S / 128) = scale blocks per (b, h)
+  float c_log2;         // softmax scale * log2(e)
+  void* o;              // [B, S, H, D] bf16
+  float* lse;           // [B, H, S] fp32 or nullptr
+  const float* q_scale; // [B, H, nK] fp32 (FP8 only; nullptr = 1)
+  const float* k_scale;
+  const float* v_scale;
+  long long spin_limit; // cycles a bounded wait may spin
+  int* err_word;        // device error word (first error code)
+  int* err_info;        // where it happened
+};
+
+// Launch one attention forward.  Returns the cudaError_t of the launch.
+template <int D, bool FP8, bool CAUSAL>
+cudaError_t launch_attn(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                        const AttnParams& p, cudaStream_t stream);
+
+// Query-tile count per CTA (two Q tiles share K/V loads; one at D = 256 where
+// two tiles' S and O would not fit the 512 Tensor-Memory columns).
+constexpr int attn_q_tiles(int D) { return D == 256 ? 1 : 2; }
+
+struct QuantParams {
+  int B, H, S, nblk;
+  const void* x;        // [B, S, H, D] bf16
+  void* out;            // [B, S, H, D] E4M3
+  float* scale;         // [B, H, nblk]
+  const float* signs;   // [D] or nullptr
+};
+
+template <int D>
+cudaError_t launch_hadamard_quant(const QuantParams& p, cudaStream_t stream);
+
+}  // namespace ea46

@@ -1,0 +1,98 @@
+"""Python binding of the attention library: torch tensors in, C-ABI calls out.
+
+Argument marshalling only -- every step of the computation runs in the CUDA
+kernels behind include/attn46.h.  torch supplies device memory and the current
+stream.  Tensors are [B, S, H, D] contiguous on the current CUDA device.
+"""
+
+import torch
+
+from . import _lib
+
+__all__ = ["attn_fwd", "attn_fwd_fp8", "hadamard_rotate_quant_fp8", "check",
+           "set_spin_limit", "selftest_bounded_wait", "block_count", "ATTN_BF16", "ATTN_FP8_E4M3"]
+
+ATTN_BF16 = 0
+ATTN_FP8_E4M3 = 1
+TOKEN_BLOCK = 128
+
+
+def block_count(S):
+    """Number of 128-token scale blocks for sequence length S."""
+    return (S + TOKEN_BLOCK - 1) // TOKEN_BLOCK
+
+
+def _stream(stream):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return s.cuda_stream
+
+
+def _ptr(t):
+    return t.data_ptr() if t is not None else None
+
+
+def _check4(*ts):
+    for t in ts:
+        if not (t.is_cuda and t.is_contiguous() and t.dim() == 4):
+            raise ValueError("expected contiguous 4-D CUDA tensors [B, S, H, D]")
+
+
+def attn_fwd(q, k, v, causal=False, scale=0.0, out=None, lse=None, want_lse=True, stream=None):
+    """O (bf16) and lse (fp32 [B, H, S], or None) for bf16 or E4M3 q, k, v.
+
+    E4M3 inputs (torch.float8_e4m3fn or uint8) are taken with unit scales.
+    """
+    _check4(q, k, v)
+    B, S, H, D = q.shape
+    dtype = ATTN_FP8_E4M3 if q.element_size() == 1 else ATTN_BF16
+    if out is None:
+        out = torch.empty((B, S, H, D), dtype=torch.bfloat16, device=q.device)
+    if lse is None and want_lse:
+        lse = torch.empty((B, H, S), dtype=torch.float32, device=q.device)
+    _lib.call("attn_fwd", _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, S, D,
+              int(bool(causal)), float(scale), dtype, _stream(stream))
+    return out, lse
+
+
+def attn_fwd_fp8(q8, k8, v8, q_scale, k_scale, v_scale, causal=False, scale=0.0, out=None,
+                 lse=None, want_lse=True, stream=None):
+    """O (bf16) and lse for E4M3 inputs with per-(b, h, 128-token block) fp32 scales."""
+    _check4(q8, k8, v8)
+    B, S, H, D = q8.shape
+    if out is None:
+        out = torch.empty((B, S, H, D), dtype=torch.bfloat16, device=q8.device)
+    if lse is None and want_lse:
+        lse = torch.empty((B, H, S), dtype=torch.float32, device=q8.device)
+    _lib.call("attn_fwd_fp8", _ptr(q8), _ptr(k8), _ptr(v8), _ptr(q_scale), _ptr(k_scale),
+              _ptr(v_scale), _ptr(out), _ptr(lse), B, H, S, D, int(bool(causal)), float(scale),
+              _stream(stream))
+    return out, lse
+
+
+def hadamard_rotate_quant_fp8(x, signs=None, out=None, scale=None, stream=None):
+    """E4M3 codes (uint8 [B, S, H, D]) and block scales (fp32 [B, H, ceil(S/128)]) of bf16 x.
+
+    ``signs``: fp32 CUDA tensor of D values +-1 (rotate), or None (quantise only).
+    """
+    _check4(x)
+    B, S, H, D = x.shape
+    if out is None:
+        out = torch.empty((B, S, H, D), dtype=torch.uint8, device=x.device)
+    if scale is None:
+        scale = torch.empty((B, H, block_count(S)), dtype=torch.float32, device=x.device)
+    _lib.call("hadamard_rotate_quant_fp8", _ptr(x), _ptr(out), _ptr(scale), _ptr(signs), B, H, S,
+              D, _stream(stream))
+    return out, scale
+
+
+def check(stream=None):
+    """Synchronise the stream and raise AttnError if a kernel's bounded wait ran out."""
+    _lib.call("attn_check", _stream(stream))
+
+
+def set_spin_limit(cycles):
+    _lib.load().attn_set_spin_limit(int(cycles))
+
+
+def selftest_bounded_wait(cycles, stream=None):
+    _lib.call("attn_selftest_bounded_wait", int(cycles), _stream(stream))

@@ -1,0 +1,146 @@
+/*
+ * attn46.h -- C ABI of the fused exact-attention forward library for GB300 (sm_103a).
+ *
+ * The library computes, on one GPU, the attention forward pass
+ *
+ *     O = softmax(scale * Q K^T [+ causal mask]) V,   lse = log-sum-exp per query row,
+ *
+ * tile by tile with an online softmax, never writing the S x S score matrix to
+ * device memory, and the low-precision variant in which Q and K are first
+ * rotated by a random-sign Hadamard matrix and Q, K, V are quantised to FP8
+ * (E4M3) with one scale per 128-token block.
+ *
+ * Sources (web pages, cited by title and section):
+ *   [HADA] "FlashAttention-3: Schnellere und präzisere Attention durch
+ *          Asynchronität und geringe Präzision" (hada.io summary of the FA3
+ *          announcement);
+ *   [NL]   "FlashAttention-3 (NL)" (systems-analysis.info).
+ *
+ * Conventions shared by every entry point:
+ *   - Pointers named q, k, v, o, x, out, lse, *_scale, signs are DEVICE
+ *     pointers owned by the caller; the library never frees or keeps them.
+ *   - Tensor layout is [B, S, H, D] contiguous (one row = one token of one
+ *     head, D contiguous elements); lse is [B, H, S] fp32; block scales are
+ *     [B, H, ceil(S/128)] fp32.  q, k, v, o, x and out must be 16-byte aligned.
+ *   - stream is a cudaStream_t passed as void* (NULL = the legacy default
+ *     stream).  Calls only enqueue work and return; they do not synchronise.
+ *   - Return value: an attn_status.  On any non-OK status nothing was launched
+ *     and attn_get_last_error() describes why.  Device-side failures (a
+ *     bounded wait inside a kernel that ran out) are recorded in a per-device
+ *     error word and reported by attn_check().
+ *   - No C++ exception crosses this boundary.
+ *   - B, H, S >= 1; D in {64, 128, 256}; outputs must not overlap inputs.
+ */
+#ifndef ATTN46_H
+#define ATTN46_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  ATTN_OK = 0,
+  ATTN_ERR_INVALID_ARG = 1,   /* null / misaligned pointer, bad size, overlap, bad enum */
+  ATTN_ERR_UNSUPPORTED = 2,   /* valid request this build does not implement (e.g. D = 96) */
+  ATTN_ERR_CUDA = 3,          /* a CUDA runtime or driver call failed */
+  ATTN_ERR_TIMEOUT = 4        /* a bounded wait inside a kernel ran out (see attn_check) */
+} attn_status;
+
+typedef enum {
+  ATTN_BF16 = 0,              /* q, k, v bf16 */
+  ATTN_FP8_E4M3 = 1           /* q, k, v E4M3 bytes with unit scales */
+} attn_dtype;
+
+/*
+ * attn_fwd -- fused exact attention forward.
+ *   [HADA] "Rückblick auf den FlashAttention-Ansatz": blocks of the inputs are
+ *   loaded on chip, attention is computed per block with softmax rescaling,
+ *   and the exact output is obtained without writing the attention matrix to
+ *   HBM; "Überlappung von GEMM und Softmax": the work is the Q-K GEMM, the
+ *   softmax and the P-V GEMM.
+ *   q, k, v : [B, S, H, D] bf16 (dtype ATTN_BF16) or E4M3 (ATTN_FP8_E4M3, all
+ *             scales taken as 1).
+ *   o       : [B, S, H, D] bf16 output.
+ *   lse     : [B, H, S] fp32 natural-log log-sum-exp of the scaled, masked
+ *             logits, or NULL to skip it.
+ *   causal  : 0 = every query sees every key; 1 = query i sees keys j <= i.
+ *   scale   : logit multiplier; 0 selects 1/sqrt(D); negative or non-finite
+ *             values are rejected.
+ */
+int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+             int B, int H, int S, int D, int causal, float scale, int dtype,
+             void* stream);
+
+/*
+ * attn_fwd_fp8 -- attention forward on E4M3 inputs with per-block scales.
+ *   [NL] "Technische innovaties", item 3, and [HADA] "Niedrige
+ *   FP8-Präzision und incoherent processing": both GEMMs run in FP8; the
+ *   inputs come from hadamard_rotate_quant_fp8.
+ *   q8, k8, v8 : [B, S, H, D] E4M3 bytes; the value of an element is
+ *                code * its block's scale.
+ *   q_scale, k_scale, v_scale : [B, H, ceil(S/128)] fp32 positive scales, as
+ *                written by hadamard_rotate_quant_fp8.
+ *   o, lse, causal, scale : as for attn_fwd (scale refers to the original
+ *                head dimension; the rotation does not change it).
+ *   The softmax numerators are rounded to E4M3 for the P-V GEMM; the row sums
+ *   use the unrounded values.
+ */
+int attn_fwd_fp8(const void* q8, const void* k8, const void* v8,
+                 const float* q_scale, const float* k_scale, const float* v_scale,
+                 void* o, float* lse, int B, int H, int S, int D, int causal,
+                 float scale, void* stream);
+
+/*
+ * hadamard_rotate_quant_fp8 -- random-sign Hadamard rotation + blockwise E4M3 quantisation.
+ *   [NL] "Technische innovaties", item 3, steps 1-3: multiply by a random
+ *   orthogonal matrix, which spreads outliers over the coordinates, then
+ *   quantise to FP8.  [HADA] "Niedrige FP8-Präzision und incoherent
+ *   processing": a Hadamard transform with random signs, O(d log d) per
+ *   head, memory-bandwidth bound.
+ *   x      : [B, S, H, D] bf16 input.
+ *   out    : [B, S, H, D] E4M3 bytes.
+ *   scale  : [B, H, ceil(S/128)] fp32 output; scale = amax / 448 of the
+ *            block's rotated values (1 for an all-zero block).
+ *   signs  : D fp32 values, each +1 or -1, or NULL to quantise without
+ *            rotating.  Each row x (D elements) becomes
+ *            x' = (x * signs) H_D / sqrt(D), H_D the Sylvester Hadamard
+ *            matrix; use the same signs for Q and K.
+ *   out[e] = E4M3_round_nearest_even_saturating(x'[e] / scale).
+ */
+int hadamard_rotate_quant_fp8(const void* x, void* out, float* scale, const float* signs,
+                              int B, int H, int S, int D, void* stream);
+
+/* Message for the last non-OK status returned on the calling host thread ("" if none). */
+const char* attn_get_last_error(void);
+
+/*
+ * attn_check -- synchronise `stream`, then read and clear the current
+ * device's error word.  Returns ATTN_OK, ATTN_ERR_TIMEOUT (a kernel's bounded
+ * wait ran out; its outputs are undefined) or ATTN_ERR_CUDA.
+ */
+int attn_check(void* stream);
+
+/*
+ * attn_set_spin_limit -- cycles (SM clock) a kernel's bounded wait may spin
+ * before it gives up and records ATTN_ERR_TIMEOUT; 0 restores the default
+ * (about 4e9 cycles, two seconds at 2 GHz).  Applies to later launches from
+ * any host thread.
+ */
+void attn_set_spin_limit(long long cycles);
+
+/*
+ * attn_selftest_bounded_wait -- launch one tiny kernel whose bounded wait
+ * targets a barrier nothing ever completes, with the given spin limit, so
+ * the timeout path can be checked without hanging or faulting the GPU.  The
+ * kernel records ATTN_ERR_TIMEOUT and returns; attn_check() then reports it.
+ */
+int attn_selftest_bounded_wait(long long spin_cycles, void* stream);
+
+/* Library ABI version (major * 100 + minor). */
+int attn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN46_H */

@@ -1,0 +1,73 @@
+"""The C-ABI library loads without a GPU, exports every function include/attn46.h
+declares, and rejects bad arguments before touching the device (CPU only)."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from exact_attention_46_gb300 import _lib
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared_functions():
+    names = []
+    inc = os.path.join(ROOT, "include")
+    for fn in sorted(os.listdir(inc)):
+        if fn.endswith(".h"):
+            text = open(os.path.join(inc, fn)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names += re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(\w+)\s*\(", text, flags=re.M)
+    return names
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(_lib.LIB_PATH):
+        import __graft_entry__
+        __graft_entry__.build()
+    return _lib.load()
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = _declared_functions()
+    assert {"attn_fwd", "attn_fwd_fp8", "hadamard_rotate_quant_fp8", "attn_check"} <= set(names)
+    for n in names:
+        assert hasattr(lib, n), n
+        assert n in _lib.SIGNATURES, n
+
+
+def test_version(lib):
+    assert lib.attn_version() == 100
+
+
+FAKE = 1 << 20   # 16-byte aligned non-null fake device addresses: never dereferenced
+
+
+@pytest.mark.parametrize("args,code", [
+    ((None, FAKE, FAKE, FAKE * 4, None, 1, 1, 128, 128, 0, 0.0, 0), 1),
+    ((FAKE, FAKE * 2, FAKE * 3, FAKE * 4, None, 1, 1, 0, 128, 0, 0.0, 0), 1),      # S = 0
+    ((FAKE, FAKE * 2, FAKE * 3, FAKE * 4, None, 0, 1, 128, 128, 0, 0.0, 0), 1),    # B = 0
+    ((FAKE, FAKE * 2, FAKE * 3, FAKE * 4, None, 1, 1, 128, 96, 0, 0.0, 0), 2),     # D = 96
+    ((FAKE, FAKE * 2, FAKE * 3, FAKE * 4, None, 1, 1, 128, 0, 0, 0.0, 0), 1),      # D = 0
+    ((FAKE, FAKE * 2, FAKE * 3, FAKE * 4, None, 1, 1, 128, 128, 2, 0.0, 0), 1),    # causal = 2
+    ((FAKE, FAKE * 2, FAKE * 3, FAKE * 4, None, 1, 1, 128, 128, 0, -1.0, 0), 1),   # scale < 0
+    ((FAKE, FAKE * 2, FAKE * 3, FAKE * 4, None, 1, 1, 128, 128, 0, float("nan"), 0), 1),
+    ((FAKE + 8, FAKE * 2, FAKE * 3, FAKE * 4, None, 1, 1, 128, 128, 0, 0.0, 0), 1),  # misaligned
+    ((FAKE, FAKE * 2, FAKE * 3, FAKE * 2, None, 1, 1, 128, 128, 0, 0.0, 0), 1),    # o aliases k
+    ((FAKE, FAKE * 2, FAKE * 3, FAKE * 4, None, 1, 1, 128, 128, 0, 0.0, 7), 1),    # dtype
+])
+def test_attn_fwd_rejects_bad_arguments_without_launching(lib, args, code):
+    assert lib.attn_fwd(*args, None) == code
+    assert lib.attn_get_last_error()
+
+
+def test_quantiser_and_fp8_reject_bad_arguments(lib):
+    assert lib.hadamard_rotate_quant_fp8(None, FAKE, FAKE * 2, None, 1, 1, 128, 128, None) == 1
+    assert lib.hadamard_rotate_quant_fp8(FAKE, FAKE * 8, FAKE * 16, None, 1, 1, 128, 48, None) == 2
+    assert lib.hadamard_rotate_quant_fp8(FAKE, FAKE * 8, FAKE * 16, FAKE + 4, 1, 1, 128, 128, None) == 1
+    assert lib.attn_fwd_fp8(FAKE, FAKE * 2, FAKE * 3, None, FAKE * 5, FAKE * 6, FAKE * 7, None,
+                            1, 1, 128, 128, 0, 0.0, None) == 1
+    assert lib.attn_selftest_bounded_wait(0, None) == 1
