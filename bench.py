@@ -1,0 +1,490 @@
+#!/usr/bin/env python3
+"""Benchmark of the fused exact-attention forward on GB300 (one JSON line on stdout).
+
+Workload (the D = 128 benchmark family: H = 16, B = 16384 / S, N(0,1) bf16 inputs,
+non-causal), headline S = 8192, B = 2.  One step = the whole hot path on one batch:
+
+  1. BF16 fused attention  O, lse = attn_fwd(Q, K, V)
+  2. FP8 path: Q8, sq = rotate+quantise(Q, signs); K8, sk = rotate+quantise(K, signs);
+     V8, sv = quantise(V); O8, lse8 = attn_fwd_fp8(Q8, K8, V8, sq, sk, sv)
+
+value = attention FLOPs of both passes (4*B*H*S^2*D each) / device time per step, summed
+over ranks (each rank runs its own batch: weak scaling).  Inputs (256 MB of bf16
+Q/K/V/O plus 128 MB of E4M3/O8 tensors) are larger than the 129 MB L2.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl reference times the fp64 CPU oracle (the only reference implementation) on a
+bounded sample of the same workload.
+"""
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "attention fwd TFLOPS (BF16 & FP8) vs S at 1 GB300, % of dense tensor peak"
+TOKENS = 16384
+H, D = 16, 128
+HEADLINE_S = 8192
+SWEEP_S = [512, 1024, 2048, 4096, 8192, 16384]
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def attention_flops(B, Hh, S, Dd, causal=False):
+    """4*B*H*S^2*D (two GEMMs of 2*S*S*D per head); causal counts half."""
+    f = 4 * B * Hh * S * S * Dd
+    return f // 2 if causal else f
+
+
+def quant_bytes(B, S, Hh, Dd):
+    """Algorithmic HBM bytes of one rotate+quantise launch: bf16 in, E4M3 out, fp32 scales."""
+    return B * S * Hh * Dd * 3 + 4 * B * Hh * ((S + 127) // 128)
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return json.load(f), "measured"
+    return FALLBACK_PEAKS, "fallback"
+
+
+def kernel_source_sha():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "exact_attention_46_gb300", "csrc")
+    for name in ("attn_kernel.cuh", "ptx.cuh", "hadamard_quant.cu"):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel, units_per_launch):
+    """dram bytes per launch from the committed ncu summary, or None if stale / absent."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            t = json.load(f)
+    except (OSError, ValueError):
+        return None
+    e = t.get(kernel)
+    if not e or e.get("source_sha") != kernel_source_sha():
+        return None
+    return e["dram_bytes_per_unit"] * units_per_launch
+
+
+# ------------------------------------------------------------------ clocks --
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.proc = None
+        self.lines = []
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", str(gpu_index)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# --------------------------------------------------------------- our arm --
+
+class HotPath:
+    """Device buffers of one batch and the launches of one step."""
+
+    def __init__(self, B, S, case, dev):
+        from exact_attention_46_gb300 import ops, synth
+        self.ops = ops
+        self.B, self.S = B, S
+        q, k, v = synth.make_qkv(B, S, H, D, case)
+        signs = synth.signs(D, synth.seed_for(case, synth.STREAM_SIGNS))
+        self.host = [t.pin_memory() for t in (q, k, v)]
+        self.q, self.k, self.v = (t.to(dev) for t in self.host)
+        self.signs = torch.from_numpy(signs).to(dev)
+        nb = (S + 127) // 128
+        self.o = torch.empty_like(self.q)
+        self.lse = torch.empty((B, H, S), dtype=torch.float32, device=dev)
+        self.o8 = torch.empty_like(self.q)
+        self.lse8 = torch.empty_like(self.lse)
+        self.q8, self.k8, self.v8 = (torch.empty(q.shape, dtype=torch.uint8, device=dev) for _ in range(3))
+        self.sq, self.sk, self.sv = (torch.empty((B, H, nb), dtype=torch.float32, device=dev) for _ in range(3))
+        self.host_o = torch.empty(q.shape, dtype=torch.bfloat16).pin_memory()
+        self.host_o8 = torch.empty(q.shape, dtype=torch.bfloat16).pin_memory()
+        self.launches_per_step = 5
+
+    def step(self, ev=None):
+        ops = self.ops
+        if ev is not None:
+            ev[0].record()
+        ops.attn_fwd(self.q, self.k, self.v, out=self.o, lse=self.lse)
+        if ev is not None:
+            ev[1].record()
+        ops.hadamard_rotate_quant_fp8(self.q, self.signs, out=self.q8, scale=self.sq)
+        ops.hadamard_rotate_quant_fp8(self.k, self.signs, out=self.k8, scale=self.sk)
+        ops.hadamard_rotate_quant_fp8(self.v, None, out=self.v8, scale=self.sv)
+        if ev is not None:
+            ev[2].record()
+        ops.attn_fwd_fp8(self.q8, self.k8, self.v8, self.sq, self.sk, self.sv, out=self.o8, lse=self.lse8)
+        if ev is not None:
+            ev[3].record()
+
+    def step_e2e(self):
+        """The same step through the public API from pinned host buffers and back."""
+        for h, d in zip(self.host, (self.q, self.k, self.v)):
+            d.copy_(h, non_blocking=True)
+        self.step()
+        self.host_o.copy_(self.o, non_blocking=True)
+        self.host_o8.copy_(self.o8, non_blocking=True)
+
+    @property
+    def flops(self):
+        return 2 * attention_flops(self.B, H, self.S, D)
+
+    @property
+    def h2d_bytes(self):
+        return sum(t.numel() * t.element_size() for t in self.host)
+
+    @property
+    def d2h_bytes(self):
+        return self.host_o.numel() * 2 + self.host_o8.numel() * 2
+
+
+def barrier(dist_on):
+    if dist_on:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+
+
+def max_over_ranks(x, dist_on, dev):
+    if not dist_on:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(x, dist_on, dev):
+    if not dist_on:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.SUM)
+    return float(t.item())
+
+
+def sweep(dev):
+    """BF16 and FP8 attention TFLOPS vs S (device time, 10 launches each)."""
+    from exact_attention_46_gb300 import ops
+    out = []
+    for S in SWEEP_S:
+        B = TOKENS // S
+        g = torch.Generator(device=dev).manual_seed(S)
+        q, k, v = (torch.randn((B, S, H, D), generator=g, device=dev, dtype=torch.float32).to(torch.bfloat16)
+                   for _ in range(3))
+        o = torch.empty_like(q)
+        lse = torch.empty((B, H, S), device=dev)
+        s = torch.where(torch.rand(D, generator=g, device=dev) < 0.5, -1.0, 1.0)
+        q8, sq = ops.hadamard_rotate_quant_fp8(q, s)
+        k8, sk = ops.hadamard_rotate_quant_fp8(k, s)
+        v8, sv = ops.hadamard_rotate_quant_fp8(v, None)
+        res = {"S": S, "B": B}
+        for name, fn in (("bf16", lambda: ops.attn_fwd(q, k, v, out=o, lse=lse)),
+                         ("fp8", lambda: ops.attn_fwd_fp8(q8, k8, v8, sq, sk, sv, out=o, lse=lse))):
+            for _ in range(3):
+                fn()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
+            e0.record()
+            for _ in range(10):
+                fn()
+            e1.record()
+            torch.cuda.synchronize()
+            ms = e0.elapsed_time(e1) / 10
+            res[name + "_tflops"] = round(attention_flops(B, H, S, D) / ms / 1e9, 1)
+        ops.check()
+        out.append(res)
+        del q, k, v, o, q8, k8, v8
+    return out
+
+
+class OracleSample:
+    """A bounded sample of the workload for the fp64 oracle: one head at the headline S.
+
+    One sample step = the oracle's rotate + quantise of one 128-token block of each of Q, K
+    and V (the quantisers' share of the step), then the BF16 pass (exact attention) and the
+    FP8 pass (attention on the de-quantised inputs with E4M3-rounded numerators) of the 128
+    query rows of one block against all S keys.  K and V of the head are quantised once when
+    the sample is set up, as the full step would have done.
+    """
+
+    ROWS = 128
+
+    def __init__(self):
+        from exact_attention_46_gb300 import synth
+        from oracle import quantise
+        S = HEADLINE_S
+        self.q, self.k, self.v = (t.to(torch.float64).numpy() for t in synth.make_qkv(1, S, 1, D, case=2))
+        self.s = synth.signs(D, synth.seed_for(2, synth.STREAM_SIGNS)).astype(np.float64)
+        Qq = quantise.quantise_blocks(self.q, self.s)
+        Kq = quantise.quantise_blocks(self.k, self.s)
+        Vq = quantise.quantise_blocks(self.v, None)
+        self.qd = quantise.dequantise(Qq["q"], Qq["scale"])
+        self.kd = quantise.dequantise(Kq["q"], Kq["scale"])
+        self.vd = quantise.dequantise(Vq["q"], Vq["scale"])
+        self.nblk = S // self.ROWS
+
+    def step(self, i):
+        from oracle import attention as oracle_attention
+        from oracle import fp8_path as oracle_fp8
+        from oracle import quantise
+        blk = i % self.nblk
+        sl = slice(blk * self.ROWS, (blk + 1) * self.ROWS)
+        quantise.quantise_blocks(self.q[:, sl], self.s)
+        quantise.quantise_blocks(self.k[:, sl], self.s)
+        quantise.quantise_blocks(self.v[:, sl], None)
+        rows = np.arange(sl.start, sl.stop)
+        oracle_attention.attention(self.q, self.k, self.v, rows=rows)
+        oracle_fp8.attention_rounded_p(self.qd, self.kd, self.vd, 1.0 / math.sqrt(D), rows=rows)
+
+    @property
+    def flops_per_step(self):
+        return 2 * self.ROWS * 4 * HEADLINE_S * D
+
+    def describe(self, steps, seconds):
+        return (f"fp64 numpy oracle: {steps} steps of (rotate+quantise of one 128-token block of Q, K, V; "
+                f"BF16 pass and FP8 pass of the 128 query rows of that block against all "
+                f"{HEADLINE_S} keys), one head, D={D}; {seconds:.1f} s")
+
+
+def blas_threads():
+    cores = os.cpu_count()
+    try:
+        from threadpoolctl import threadpool_info
+        n = max((i.get("num_threads", 0) for i in threadpool_info()), default=0)
+        return n or cores
+    except ImportError:
+        return cores
+
+
+def cpu_baseline_sample(budget_s=12.0):
+    """The oracle as it stands, timed on the host cores for about ``budget_s`` seconds."""
+    smp = OracleSample()
+    smp.step(0)
+    n, t0 = 0, time.perf_counter()
+    while time.perf_counter() - t0 < budget_s:
+        smp.step(n + 1)
+        n += 1
+    dt = time.perf_counter() - t0
+    return {"value": n * smp.flops_per_step / dt / 1e12, "unit": "TFLOPS", "cores": blas_threads(),
+            "kind": "oracle", "sample": smp.describe(n, dt)}
+
+
+def run_ours(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist_on = world > 1
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if dist_on:
+        torch.distributed.init_process_group("nccl", device_id=dev)
+    import __graft_entry__
+    __graft_entry__.build()
+    from exact_attention_46_gb300 import ops
+
+    B, S = TOKENS // HEADLINE_S, HEADLINE_S
+    hp = HotPath(B, S, case=2 + 1000 * rank, dev=dev)
+    for _ in range(args.warmup):
+        hp.step()
+    ops.check()
+
+    # device-timed region
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    barrier(dist_on)
+    clocks = ClockSampler(local)
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_start.record()
+    for i in range(args.steps):
+        hp.step(ev[i])
+    t_end.record()
+    barrier(dist_on)
+    clk = clocks.stop()
+    ops.check()
+    ms = t_start.elapsed_time(t_end) / args.steps
+    ms_max = max_over_ranks(ms, dist_on, dev)
+    flops_all = sum_over_ranks(float(hp.flops), dist_on, dev)
+    bf16_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
+    quant_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
+    fp8_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in ev)
+
+    # end-to-end through the public API with host buffers
+    n_e2e = max(3, min(args.steps, 20))
+    for _ in range(2):
+        hp.step_e2e()
+    barrier(dist_on)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(n_e2e):
+        hp.step_e2e()
+    e1.record()
+    barrier(dist_on)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / n_e2e, dist_on, dev)
+
+    sw = sweep(dev) if (args.sweep and rank == 0) else None
+    peaks, peak_src = load_peaks()
+    cpu = cpu_baseline_sample() if (rank == 0 and world == 1 and args.cpu_baseline) else None
+
+    if rank == 0:
+        f1 = attention_flops(B, H, S, D)
+        bf16_tflops = f1 / bf16_ms / 1e9
+        fp8_tflops = f1 / fp8_ms / 1e9
+        qbytes = 3 * quant_bytes(B, S, H, D)
+        peak_bf16 = peaks["bf16_tflops"]
+        traffic = profiled_traffic("attn_fwd_bf16_d128", B * H * S)
+        line = {
+            "metric": METRIC,
+            "value": round(flops_all / ms_max / 1e9, 1),
+            "unit": "TFLOPS",
+            "n_gpus": world,
+            "steps": args.steps,
+            "warmup": args.warmup,
+            "ms_per_step": round(ms_max, 4),
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "bf16 and e4m3 inputs, fp32 accumulate",
+            "data": "synthetic: seeded N(0,1) bf16 Q/K/V (SplitMix64 + Box-Muller)",
+            "config": {"workload": f"fused attention fwd, BF16 pass + FP8 pass (Hadamard-rotated Q/K), "
+                                   f"B={B} S={S} H={H} D={D} non-causal",
+                       "global_batch": B * world, "seq_len": S, "heads": H, "head_dim": D,
+                       "causal": False, "parallelism": f"dp{world}" if world > 1 else "single GPU",
+                       "l2": "inputs larger than L2 (256 MB bf16 Q/K/V/O + 128 MB FP8 path tensors)",
+                       "step": "attn_fwd bf16 + 3x hadamard_rotate_quant_fp8 + attn_fwd_fp8"},
+            "roofline": {"kernel": "attn_fwd bf16 D=128", "bound": "tensor",
+                         "achieved": round(bf16_tflops, 1), "peak": peak_bf16,
+                         "unit": "TFLOPS", "frac": round(bf16_tflops / peak_bf16, 4),
+                         "traffic": traffic,
+                         "peak_source": f"{peak_src} bf16 burst (cuBLAS)"},
+            "kernels": {
+                "attn_fwd_bf16": {"ms": round(bf16_ms, 4), "tflops": round(bf16_tflops, 1),
+                                  "frac_of_bf16_peak": round(bf16_tflops / peak_bf16, 4)},
+                "attn_fwd_fp8": {"ms": round(fp8_ms, 4), "tflops": round(fp8_tflops, 1),
+                                 "frac_of_fp8_peak": round(fp8_tflops / (2 * peak_bf16), 4),
+                                 "fp8_peak_tflops": 2 * peak_bf16},
+                "hadamard_rotate_quant_fp8_x3": {"ms": round(quant_ms, 4),
+                                                 "gbs": round(qbytes / quant_ms / 1e6, 1),
+                                                 "frac_of_hbm": round(qbytes / quant_ms / 1e6 / peaks["hbm_gbs"], 4)},
+            },
+            "e2e": {"value": round(flops_all / e2e_ms / 1e9, 1), "unit": "TFLOPS",
+                    "h2d_bytes_per_step": hp.h2d_bytes, "d2h_bytes_per_step": hp.d2h_bytes},
+            "gpu_launches": hp.launches_per_step * args.steps,
+            "clocks": clk,
+            "cpu_baseline": cpu,
+            "sweep": sw,
+        }
+        print(json.dumps(line), flush=True)
+    if dist_on:
+        torch.distributed.destroy_process_group()
+
+
+# --------------------------------------------------------- reference arm --
+
+def run_reference(args):
+    """The fp64 CPU oracle, timed on the host cores, same metric and workload (bounded sample)."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    smp = OracleSample()
+    for i in range(args.warmup):
+        smp.step(i)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        smp.step(args.warmup + i)
+    total = time.perf_counter() - t0
+    dt = total / args.steps
+    val = smp.flops_per_step / dt / 1e12
+    cpu = {"value": round(val, 6), "unit": "TFLOPS", "cores": blas_threads(), "kind": "oracle",
+           "sample": smp.describe(args.steps, total)}
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": round(val, 6), "unit": "TFLOPS",
+        "n_gpus": int(os.environ.get("WORLD_SIZE", "1")), "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(dt * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (same seeded generator)",
+        "config": {"workload": f"fused attention fwd, BF16 pass + FP8 pass (Hadamard-rotated Q/K), "
+                               f"B={TOKENS // HEADLINE_S} S={HEADLINE_S} H={H} D={D} non-causal; "
+                               "bounded sample per step", "seq_len": HEADLINE_S},
+        "cpu_baseline": cpu,
+        "e2e": {"value": round(val, 6), "unit": "TFLOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-sweep", dest="sweep", action="store_false")
+    ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -180,3 +180,23 @@ def test_rotated_quantiser_rotates_before_scaling():
     out = quantise.quantise_blocks(x, s)
     np.testing.assert_allclose(out["rotated"], hadamard.rotate(x, s), atol=1e-13)
     np.testing.assert_allclose(out["scale"][0, 0, 0], np.abs(hadamard.rotate(x, s)).max() / 448.0, rtol=1e-14)
+
+
+def test_fp32_rounding_decision_differs_from_fp64_only_at_exact_ties():
+    # amax = 26 = 2 * 13 makes x * 448 / 26 = x * 224 / 13 an exact E4M3 midpoint for bf16
+    # values x = 39 * 2^k; elsewhere the fp32 decision equals rounding the exact quotient.
+    B, S, H, D = 1, 128, 1, 128
+    x = RNG.standard_normal((B, S, H, D))
+    x = torch.from_numpy(x).to(torch.bfloat16).double().numpy()
+    x[0, 0, 0, 0] = 26.0
+    x[0, 1:40, 0, 1] = 39 * 2.0 ** -5                      # exact ties in real arithmetic
+    out = quantise.quantise_blocks(x)
+    exact = x * 448.0 / 26.0
+    q64 = e4m3.round_e4m3(exact)
+    lo = e4m3.round_e4m3(exact * (1 - 1e-9))
+    hi = e4m3.round_e4m3(exact * (1 + 1e-9))
+    tie = lo != hi                                          # a midpoint sits within 1e-9
+    assert tie[0, 1:40, 0, 1].all()
+    diff = out["q"] != q64
+    assert not (diff & ~tie).any()
+    assert ((out["q"] == lo) | (out["q"] == hi)).all()
