@@ -71,7 +71,7 @@ struct AttnCfg {
   static constexpr int SMEM_TILES_BUDGET = 200 * 1024;
   static constexpr int NSLOT_RAW = (SMEM_TILES_BUDGET - NT * TILE_BYTES) / TILE_BYTES;
   static constexpr int NSLOT = NSLOT_RAW > 8 ? 8 : NSLOT_RAW;
-  static constexpr int NBAR = 1 + 2 * NSLOT + 3 * NT + 1;
+  static constexpr int NBAR = 2 + 2 * NSLOT + 4 * NT + 1;
   static constexpr int SMEM_BYTES_RAW = (NT + NSLOT) * TILE_BYTES + NBAR * 8 + 16;
   // Request at least ~120 KB so that one CTA (and its 512 TMEM columns) owns the SM.
   static constexpr int SMEM_BYTES =
@@ -128,19 +128,22 @@ __global__ void __launch_bounds__(AttnCfg<D, FP8>::THREADS, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_ptr + C::NBAR * 8);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
-  auto BAR_Q = [&]() { return bar0; };
-  auto BAR_KV_FULL = [&](int s) { return bar0 + 8u * (1 + s); };
-  auto BAR_KV_EMPTY = [&](int s) { return bar0 + 8u * (1 + NSLOT + s); };
-  auto BAR_S_FULL = [&](int t) { return bar0 + 8u * (1 + 2 * NSLOT + t); };
-  auto BAR_P_FULL = [&](int t) { return bar0 + 8u * (1 + 2 * NSLOT + NT + t); };
-  auto BAR_O_FULL = [&](int t) { return bar0 + 8u * (1 + 2 * NSLOT + 2 * NT + t); };
-  auto BAR_MMA_DONE = [&]() { return bar0 + 8u * (1 + 2 * NSLOT + 3 * NT); };
+  auto BAR_Q_FULL = [&]() { return bar0; };
+  auto BAR_Q_EMPTY = [&]() { return bar0 + 8u; };
+  auto BAR_KV_FULL = [&](int s) { return bar0 + 8u * (2 + s); };
+  auto BAR_KV_EMPTY = [&](int s) { return bar0 + 8u * (2 + NSLOT + s); };
+  auto BAR_S_FULL = [&](int t) { return bar0 + 8u * (2 + 2 * NSLOT + t); };
+  auto BAR_P_FULL = [&](int t) { return bar0 + 8u * (2 + 2 * NSLOT + NT + t); };
+  auto BAR_O_FULL = [&](int t) { return bar0 + 8u * (2 + 2 * NSLOT + 2 * NT + t); };
+  auto BAR_O_EMPTY = [&](int t) { return bar0 + 8u * (2 + 2 * NSLOT + 3 * NT + t); };
+  auto BAR_MMA_DONE = [&]() { return bar0 + 8u * (2 + 2 * NSLOT + 4 * NT); };
 
   const uint32_t warp = warp_id();
   const uint32_t lane = lane_id();
 
   if (threadIdx.x == 0) {
-    mbar_init(BAR_Q(), 1);
+    mbar_init(BAR_Q_FULL(), 1);
+    mbar_init(BAR_Q_EMPTY(), 1);
     for (int s = 0; s < NSLOT; ++s) {
       mbar_init(BAR_KV_FULL(s), 1);
       mbar_init(BAR_KV_EMPTY(s), 1);
@@ -149,6 +152,7 @@ __global__ void __launch_bounds__(AttnCfg<D, FP8>::THREADS, 1)
       mbar_init(BAR_S_FULL(t), 1);
       mbar_init(BAR_P_FULL(t), 4);
       mbar_init(BAR_O_FULL(t), 1);
+      mbar_init(BAR_O_EMPTY(t), 4);
     }
     mbar_init(BAR_MMA_DONE(), 1);
     *abort_flag = 0;
@@ -165,27 +169,36 @@ __global__ void __launch_bounds__(AttnCfg<D, FP8>::THREADS, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  // ---- work item: (query block, head, batch) ----
+  // ---- persistent schedule over work items (query block, head, batch) ----
+  // Item order: causal -> heaviest query blocks first; otherwise the query blocks of one head
+  // are adjacent (a head's K/V is read from HBM once, then from L2).  CTA k takes item
+  // n*G + k in even rounds n and n*G + G-1-k in odd rounds (zig-zag), G = gridDim.x.
   const int HB = p.H * p.B;
-  int qb, hb;
-  if (CAUSAL) {            // heaviest query blocks first
-    qb = p.nQB - 1 - static_cast<int>(blockIdx.x / HB);
-    hb = static_cast<int>(blockIdx.x % HB);
-  } else {                 // query blocks of one head adjacent (K/V reuse in L2)
-    qb = static_cast<int>(blockIdx.x % p.nQB);
-    hb = static_cast<int>(blockIdx.x / p.nQB);
-  }
-  const int h = hb % p.H;
-  const int b = hb / p.H;
-  const int q0 = qb * 128 * NT;
-  int n_t[NT];
-  int nmax = 0;
+  const int n_items = p.nQB * HB;
+  const int G = static_cast<int>(gridDim.x);
+  const int k_cta = static_cast<int>(blockIdx.x);
+  auto item_of = [&](int n) { return n * G + ((n & 1) ? (G - 1 - k_cta) : k_cta); };
+  struct Item { int h, b, q0, hb, nmax; int n[NT]; };
+  auto decode = [&](int item, Item& it) {
+    int qb;
+    if (CAUSAL) {
+      qb = p.nQB - 1 - item / HB;
+      it.hb = item % HB;
+    } else {
+      qb = item % p.nQB;
+      it.hb = item / p.nQB;
+    }
+    it.h = it.hb % p.H;
+    it.b = it.hb / p.H;
+    it.q0 = qb * 128 * NT;
+    it.nmax = 0;
 #pragma unroll
-  for (int t = 0; t < NT; ++t) {
-    const int r0 = q0 + 128 * t;
-    n_t[t] = (r0 >= p.S) ? 0 : (CAUSAL ? (r0 / 128 + 1) : p.nK);
-    nmax = n_t[t] > nmax ? n_t[t] : nmax;
-  }
+    for (int t = 0; t < NT; ++t) {
+      const int r0 = it.q0 + 128 * t;
+      it.n[t] = (r0 >= p.S) ? 0 : (CAUSAL ? (r0 / 128 + 1) : p.nK);
+      it.nmax = it.n[t] > it.nmax ? it.n[t] : it.nmax;
+    }
+  };
 
   const WaitCtl ctl{p.spin_limit, abort_flag, p.err_word, p.err_info};
 
@@ -194,36 +207,45 @@ __global__ void __launch_bounds__(AttnCfg<D, FP8>::THREADS, 1)
     if (lane == 0) {
       const uint64_t pol_q = l2_policy_evict_first();
       const uint64_t pol_kv = l2_policy_evict_last();
-      uint32_t qbytes = 0;
+      int issued = 0, q_issued = 0;
+      for (int n = 0; n * G < n_items && !*abort_flag; ++n) {
+        const int item = item_of(n);
+        if (item >= n_items) break;
+        Item it;
+        decode(item, it);
+        // The Q buffer is released by the MMA warp after the previous item's last S MMA.
+        if (!wait_bounded(BAR_Q_EMPTY(), (q_issued & 1) ^ 1u, ctl, WHERE_LOAD)) break;
+        uint32_t qbytes = 0;
 #pragma unroll
-      for (int t = 0; t < NT; ++t) qbytes += n_t[t] > 0 ? C::TILE_BYTES : 0;
-      mbar_arrive_expect_tx(BAR_Q(), qbytes);
+        for (int t = 0; t < NT; ++t) qbytes += it.n[t] > 0 ? C::TILE_BYTES : 0;
+        mbar_arrive_expect_tx(BAR_Q_FULL(), qbytes);
 #pragma unroll
-      for (int t = 0; t < NT; ++t) {
-        if (n_t[t] == 0) continue;
-#pragma unroll
-        for (int pn = 0; pn < C::NPANEL; ++pn)
-          tma_load_4d(sQ + t * C::TILE_BYTES + pn * C::PANEL_BYTES, &tmQ, BAR_Q(),
-                      pn * C::PANEL_ELEMS, h, q0 + 128 * t, b, pol_q);
-      }
-      int issued = 0;
-      for (int j = 0; j < nmax && !*abort_flag; ++j) {
-        for (int kind = 0; kind < 2; ++kind) {
-          const int slot = issued % NSLOT;
-          const uint32_t phase = (issued / NSLOT) & 1;
-          if (!wait_bounded(BAR_KV_EMPTY(slot), phase ^ 1u, ctl, WHERE_LOAD)) break;
-          mbar_arrive_expect_tx(BAR_KV_FULL(slot), C::TILE_BYTES);
-          const CUtensorMap* m = kind == 0 ? &tmK : &tmV;
+        for (int t = 0; t < NT; ++t) {
+          if (it.n[t] == 0) continue;
 #pragma unroll
           for (int pn = 0; pn < C::NPANEL; ++pn)
-            tma_load_4d(sKV + slot * C::TILE_BYTES + pn * C::PANEL_BYTES, m, BAR_KV_FULL(slot),
-                        pn * C::PANEL_ELEMS, h, 128 * j, b, pol_kv);
-          ++issued;
+            tma_load_4d(sQ + t * C::TILE_BYTES + pn * C::PANEL_BYTES, &tmQ, BAR_Q_FULL(),
+                        pn * C::PANEL_ELEMS, it.h, it.q0 + 128 * t, it.b, pol_q);
+        }
+        ++q_issued;
+        for (int j = 0; j < it.nmax && !*abort_flag; ++j) {
+          for (int kind = 0; kind < 2; ++kind) {
+            const int slot = issued % NSLOT;
+            const uint32_t phase = (issued / NSLOT) & 1;
+            if (!wait_bounded(BAR_KV_EMPTY(slot), phase ^ 1u, ctl, WHERE_LOAD)) break;
+            mbar_arrive_expect_tx(BAR_KV_FULL(slot), C::TILE_BYTES);
+            const CUtensorMap* m = kind == 0 ? &tmK : &tmV;
+#pragma unroll
+            for (int pn = 0; pn < C::NPANEL; ++pn)
+              tma_load_4d(sKV + slot * C::TILE_BYTES + pn * C::PANEL_BYTES, m, BAR_KV_FULL(slot),
+                          pn * C::PANEL_ELEMS, it.h, 128 * j, it.b, pol_kv);
+            ++issued;
+          }
         }
       }
       if (*abort_flag) {
         // Drain: every copy still in flight must land before the CTA may exit.
-        wait_drain(BAR_Q(), 0, p.spin_limit);
+        if (q_issued > 0) wait_drain(BAR_Q_FULL(), (q_issued - 1) & 1, p.spin_limit);
         const int first = issued > NSLOT ? issued - NSLOT : 0;
         for (int i = first; i < issued; ++i)
           wait_drain(BAR_KV_FULL(i % NSLOT), (i / NSLOT) & 1, p.spin_limit);
@@ -232,76 +254,102 @@ __global__ void __launch_bounds__(AttnCfg<D, FP8>::THREADS, 1)
   } else if (warp == C::MMA_WARP) {
     // ========================================================== MMA issuer ==
     if (lane == 0) {
-      int consumed = 0;   // ring position
-      bool ok = wait_bounded(BAR_Q(), 0, ctl, WHERE_MMA);
-      tc_fence_after();
+      // Descriptors are built once; a K-step advances the start address field (bits 0-13,
+      // in 16-byte units) by adding to the low word.
+      const uint64_t dq0 = smem_desc(sQ, 16, C::SBO, C::LAYOUT);
+      const uint64_t dkv0 = smem_desc(sKV, 16, C::SBO, C::LAYOUT);
+      const uint64_t dv0 = smem_desc(sKV, C::PANEL_BYTES, C::SBO, C::LAYOUT);
       auto gemm_qk = [&](int t, int slot) {
         const uint32_t d = tmem + 128u * t;
+        const uint64_t a0 = dq0 + ((t * C::TILE_BYTES) >> 4);
+        const uint64_t b0 = dkv0 + ((slot * C::TILE_BYTES) >> 4);
 #pragma unroll
         for (int kk = 0; kk < C::KSTEPS_QK; ++kk) {
           const uint32_t off =
-              (kk / C::STEPS_PER_PANEL) * C::PANEL_BYTES + (kk % C::STEPS_PER_PANEL) * 32;
-          const uint64_t a = smem_desc(sQ + t * C::TILE_BYTES + off, 16, C::SBO, C::LAYOUT);
-          const uint64_t bd = smem_desc(sKV + slot * C::TILE_BYTES + off, 16, C::SBO, C::LAYOUT);
-          if (FP8) mma_f8_ss(d, a, bd, C::IDESC_QK, kk > 0);
-          else     mma_f16_ss(d, a, bd, C::IDESC_QK, kk > 0);
+              ((kk / C::STEPS_PER_PANEL) * C::PANEL_BYTES + (kk % C::STEPS_PER_PANEL) * 32) >> 4;
+          if (FP8) mma_f8_ss(d, a0 + off, b0 + off, C::IDESC_QK, kk > 0);
+          else     mma_f16_ss(d, a0 + off, b0 + off, C::IDESC_QK, kk > 0);
         }
       };
       auto gemm_pv = [&](int t, int slot, bool acc) {
         const uint32_t d = tmem + 128u * NT + static_cast<uint32_t>(D) * t;
+        const uint64_t b0 = dv0 + ((slot * C::TILE_BYTES) >> 4);
 #pragma unroll
         for (int kk = 0; kk < C::KSTEPS_PV; ++kk) {
           const uint32_t a = tmem + 128u * t + 8u * kk;
-          const uint64_t bd = smem_desc(sKV + slot * C::TILE_BYTES + kk * C::UMMA_K * C::PANEL_ROW,
-                                        C::PANEL_BYTES, C::SBO, C::LAYOUT);
-          if (FP8) mma_f8_ts(d, a, bd, C::IDESC_PV, (acc || kk > 0) ? 1u : 0u);
-          else     mma_f16_ts(d, a, bd, C::IDESC_PV, (acc || kk > 0) ? 1u : 0u);
+          const uint32_t off = (kk * C::UMMA_K * C::PANEL_ROW) >> 4;
+          if (FP8) mma_f8_ts(d, a, b0 + off, C::IDESC_PV, (acc || kk > 0) ? 1u : 0u);
+          else     mma_f16_ts(d, a, b0 + off, C::IDESC_PV, (acc || kk > 0) ? 1u : 0u);
         }
       };
-      if (ok) {
-        const int ks = consumed % NSLOT;
-        ok = wait_bounded(BAR_KV_FULL(ks), (consumed / NSLOT) & 1, ctl, WHERE_MMA);
-        ++consumed;
-        if (ok) {
+      int consumed = 0;          // K/V ring position
+      int pc[NT], ouse[NT];      // P phases consumed, and O uses completed, per query tile
+#pragma unroll
+      for (int t = 0; t < NT; ++t) pc[t] = ouse[t] = 0;
+      bool ok = true;
+      for (int n = 0; ok && n * G < n_items; ++n) {
+        const int item = item_of(n);
+        if (item >= n_items) break;
+        Item it;
+        decode(item, it);
+        ok = wait_bounded(BAR_Q_FULL(), n & 1, ctl, WHERE_MMA);
+        if (!ok) break;
+        {
+          const int ks = consumed % NSLOT;
+          ok = wait_bounded(BAR_KV_FULL(ks), (consumed / NSLOT) & 1, ctl, WHERE_MMA);
+          ++consumed;
+          if (!ok) break;
           tc_fence_after();
 #pragma unroll
           for (int t = 0; t < NT; ++t) {
-            if (n_t[t] > 0) {
+            if (it.n[t] > 0) {
               gemm_qk(t, ks);
               mma_commit(BAR_S_FULL(t));
             }
           }
+          if (it.nmax == 1) mma_commit(BAR_Q_EMPTY());
           mma_commit(BAR_KV_EMPTY(ks));
         }
-      }
-      for (int j = 1; ok && j <= nmax; ++j) {
-        const int vs = consumed % NSLOT;
-        ok = wait_bounded(BAR_KV_FULL(vs), (consumed / NSLOT) & 1, ctl, WHERE_MMA);
-        ++consumed;
-        if (!ok) break;
-        tc_fence_after();
-        int ks = -1;   // K_j is waited for only right before the first S(j) that needs it
+        for (int j = 1; ok && j <= it.nmax; ++j) {
+          const int vs = consumed % NSLOT;
+          ok = wait_bounded(BAR_KV_FULL(vs), (consumed / NSLOT) & 1, ctl, WHERE_MMA);
+          ++consumed;
+          if (!ok) break;
+          tc_fence_after();
+          int ks = -1;   // K_j is waited for only right before the first S(j) that needs it
 #pragma unroll
-        for (int t = 0; t < NT; ++t) {
-          if (j - 1 < n_t[t]) {
-            if (!wait_bounded(BAR_P_FULL(t), (j - 1) & 1, ctl, WHERE_MMA)) { ok = false; break; }
-            tc_fence_after();
-            gemm_pv(t, vs, j - 1 > 0);
-            if (j - 1 == n_t[t] - 1) mma_commit(BAR_O_FULL(t));
-          }
-          if (t == NT - 1) mma_commit(BAR_KV_EMPTY(vs));
-          if (j < n_t[t]) {
-            if (ks < 0) {
-              ks = consumed % NSLOT;
-              if (!wait_bounded(BAR_KV_FULL(ks), (consumed / NSLOT) & 1, ctl, WHERE_MMA)) { ok = false; break; }
-              ++consumed;
+          for (int t = 0; t < NT; ++t) {
+            if (j - 1 < it.n[t]) {
+              if (j - 1 == 0) {
+                // O_t is free once the softmax warps have read the previous item's O_t.
+                if (!wait_bounded(BAR_O_EMPTY(t), (ouse[t] & 1) ^ 1, ctl, WHERE_MMA)) { ok = false; break; }
+              }
+              if (!wait_bounded(BAR_P_FULL(t), pc[t] & 1, ctl, WHERE_MMA)) { ok = false; break; }
+              ++pc[t];
               tc_fence_after();
+              gemm_pv(t, vs, j - 1 > 0);
+              if (j - 1 == it.n[t] - 1) {
+                mma_commit(BAR_O_FULL(t));
+                ++ouse[t];
+              }
             }
-            gemm_qk(t, ks);
-            mma_commit(BAR_S_FULL(t));
+            if (t == NT - 1) mma_commit(BAR_KV_EMPTY(vs));
+            if (j < it.n[t]) {
+              if (ks < 0) {
+                ks = consumed % NSLOT;
+                if (!wait_bounded(BAR_KV_FULL(ks), (consumed / NSLOT) & 1, ctl, WHERE_MMA)) { ok = false; break; }
+                ++consumed;
+                tc_fence_after();
+              }
+              gemm_qk(t, ks);
+              mma_commit(BAR_S_FULL(t));
+            }
+          }
+          if (ok && ks >= 0) {
+            if (j == it.nmax - 1) mma_commit(BAR_Q_EMPTY());
+            mma_commit(BAR_KV_EMPTY(ks));
           }
         }
-        if (ok && ks >= 0) mma_commit(BAR_KV_EMPTY(ks));
       }
       // Drain: all issued MMAs complete before Tensor Memory is freed.
       mma_commit(BAR_MMA_DONE());
@@ -312,147 +360,172 @@ __global__ void __launch_bounds__(AttnCfg<D, FP8>::THREADS, 1)
     const int t = static_cast<int>(warp) / 4;
     const int wq = static_cast<int>(warp) % 4;
     const int row_local = wq * 32 + static_cast<int>(lane);
-    const int row = q0 + 128 * t + row_local;
     const uint32_t tl = tmem + (static_cast<uint32_t>(wq * 32) << 16);
     const uint32_t s_addr = tl + 128u * t;
     const uint32_t o_addr = tl + 128u * NT + static_cast<uint32_t>(D) * t;
-    const int nt = (q0 + 128 * t >= p.S) ? 0 : (CAUSAL ? ((q0 + 128 * t) / 128 + 1) : p.nK);
-    const size_t blk_base = static_cast<size_t>(hb) * p.nK;   // (b*H + h) * nK
-
-    float sq = 1.f, sv_max = 1.f;
-    if (FP8) {
-      if (p.q_scale != nullptr && nt > 0) sq = p.q_scale[blk_base + (q0 + 128 * t) / 128];
-      if (p.v_scale != nullptr) {
-        sv_max = 0.f;
-        for (int j = 0; j < p.nK; ++j) sv_max = fmaxf(sv_max, p.v_scale[blk_base + j]);
-      }
-    }
-
-    float m_run = -INFINITY;
-    float l_run = 0.f;
+    int sc = 0, ouse = 0;      // S phases consumed, O uses completed (this tile)
     bool ok = true;
-    for (int j = 0; j < nt; ++j) {
-      if (!wait_bounded(BAR_S_FULL(t), j & 1, ctl, WHERE_SOFTMAX)) { ok = false; break; }
-      tc_fence_after();
-      uint32_t sr[4][32];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld32(s_addr + 32u * c, sr[c]);
-      tmem_wait_ld();
-#pragma unroll
-      for (int c = 0; c < 4; ++c)
-#pragma unroll
-        for (int i = 0; i < 32; ++i) reg_fence(sr[c][i]);
+    for (int n = 0; ok && n * G < n_items; ++n) {
+      const int item = item_of(n);
+      if (item >= n_items) break;
+      Item it;
+      decode(item, it);
+      const int r0 = it.q0 + 128 * t;
+      const int nt = (r0 >= p.S) ? 0 : (CAUSAL ? (r0 / 128 + 1) : p.nK);
+      if (nt == 0) continue;
+      const int row = it.q0 + 128 * t + row_local;
+      const size_t blk_base = static_cast<size_t>(it.hb) * p.nK;   // (b*H + h) * nK
 
-      float cmul = p.c_log2, bias = 0.f, inv_r = 1.f;
+      float sq = 1.f, sv_max = 1.f;
       if (FP8) {
-        const float sk = p.k_scale != nullptr ? p.k_scale[blk_base + j] : 1.f;
-        const float sv = p.v_scale != nullptr ? p.v_scale[blk_base + j] : 1.f;
-        cmul *= sq * sk;
-        const float r = sv / sv_max;
-        bias = __log2f(r);
-        inv_r = sv_max / sv;
+        if (p.q_scale != nullptr) sq = p.q_scale[blk_base + (it.q0 + 128 * t) / 128];
+        if (p.v_scale != nullptr) {
+          sv_max = 0.f;
+          for (int j = static_cast<int>(lane); j < p.nK; j += 32) sv_max = fmaxf(sv_max, p.v_scale[blk_base + j]);
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) sv_max = fmaxf(sv_max, __shfl_xor_sync(0xffffffffu, sv_max, o));
+        }
       }
 
-      // masks: causal diagonal tile, or the ragged last key tile
-      if (CAUSAL ? (j == nt - 1) : (j == p.nK - 1 && (p.S & 127) != 0)) {
-        const int lim = CAUSAL ? (row - 128 * j) : (p.S - 128 * j - 1);   // last visible column
+      float m_run = -INFINITY;
+      float l_run = 0.f;
+      for (int j = 0; j < nt; ++j) {
+        // Per-tile FP8 scales are read before waiting for S, so the loads overlap the wait.
+        float cmul = p.c_log2, bias = 0.f, inv_r = 1.f;
+        if (FP8) {
+          const float sk = p.k_scale != nullptr ? p.k_scale[blk_base + j] : 1.f;
+          const float sv = p.v_scale != nullptr ? p.v_scale[blk_base + j] : 1.f;
+          cmul *= sq * sk;
+          bias = __log2f(sv / sv_max);
+          inv_r = sv_max / sv;
+        }
+        if (!wait_bounded(BAR_S_FULL(t), sc & 1, ctl, WHERE_SOFTMAX)) { ok = false; break; }
+        ++sc;
+        tc_fence_after();
+        uint32_t sr[4][32];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tmem_ld32(s_addr + 32u * c, sr[c]);
+        tmem_wait_ld();
 #pragma unroll
         for (int c = 0; c < 4; ++c)
 #pragma unroll
-          for (int i = 0; i < 32; ++i)
-            if (32 * c + i > lim) sr[c][i] = __float_as_uint(-INFINITY);
-      }
+          for (int i = 0; i < 32; ++i) reg_fence(sr[c][i]);
 
-      float mx[8];
+        // masks: causal diagonal tile, or the ragged last key tile
+        if (CAUSAL ? (j == nt - 1) : (j == p.nK - 1 && (p.S & 127) != 0)) {
+          const int lim = CAUSAL ? (row - 128 * j) : (p.S - 128 * j - 1);   // last visible column
 #pragma unroll
-      for (int k = 0; k < 8; ++k) mx[k] = __uint_as_float(sr[k / 2][(k % 2) * 16]);
+          for (int c = 0; c < 4; ++c)
 #pragma unroll
-      for (int c = 0; c < 4; ++c)
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const int k = (c * 2 + i / 16) & 7;
-          mx[k] = fmaxf(mx[k], __uint_as_float(sr[c][i]));
+            for (int i = 0; i < 32; ++i)
+              if (32 * c + i > lim) sr[c][i] = __float_as_uint(-INFINITY);
         }
-      const float m_tile =
-          fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * cmul;
 
-      bool rescale = false;
-      float alpha = 1.f;
-      if (j == 0) {
-        m_run = m_tile;
-      } else if (m_tile > m_run + TAU) {
-        alpha = ex2(m_run - m_tile);
-        m_run = m_tile;
-        l_run *= alpha;
-        rescale = true;
-      }
-      const float nb = bias - m_run;
-      float ls[8];
+        float mx[8];
 #pragma unroll
-      for (int k = 0; k < 8; ++k) ls[k] = 0.f;
-      if (!FP8) {
+        for (int k = 0; k < 8; ++k) mx[k] = __uint_as_float(sr[k / 2][(k % 2) * 16]);
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t pk[16];
+        for (int c = 0; c < 4; ++c)
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const float p0 = ex2(fmaf(__uint_as_float(sr[c][2 * i]), cmul, nb));
-            const float p1 = ex2(fmaf(__uint_as_float(sr[c][2 * i + 1]), cmul, nb));
-            ls[(2 * i) & 7] += p0;
-            ls[(2 * i + 1) & 7] += p1;
-            pk[i] = pack_bf16x2(p0, p1);
+          for (int i = 0; i < 32; i += 2) {
+            const int k = (c * 2 + i / 16) & 7;
+            mx[k] = max3(mx[k], __uint_as_float(sr[c][i]), __uint_as_float(sr[c][i + 1]));
           }
-          tmem_st16(s_addr + 16u * c, pk);
+        const float m_tile =
+            max3(max3(mx[0], mx[1], mx[2]), max3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7])) * cmul;
+
+        bool rescale = false;
+        float alpha = 1.f;
+        if (j == 0) {
+          m_run = m_tile;
+        } else if (m_tile > m_run + TAU) {
+          alpha = ex2(m_run - m_tile);
+          m_run = m_tile;
+          l_run *= alpha;
+          rescale = true;
         }
-      } else {
+
+        const float nb = bias - m_run;
+        const uint64_t c2 = f2_pack(cmul, cmul);
+        const uint64_t nb2 = f2_pack(nb, nb);
+        uint64_t ls2[4];
 #pragma unroll
-        for (int h2 = 0; h2 < 2; ++h2) {
-          uint32_t pk[16];
+        for (int k = 0; k < 4; ++k) ls2[k] = f2_pack(0.f, 0.f);
+        if (!FP8) {
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            float pv[4];
+          for (int c = 0; c < 4; ++c) {
+            uint32_t pk[16];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int col = 64 * h2 + 4 * i + e;
-              pv[e] = ex2(fmaf(__uint_as_float(sr[col / 32][col % 32]), cmul, nb));
-              ls[(4 * i + e) & 7] += pv[e];
+            for (int i = 0; i < 16; ++i) {
+              const uint64_t x2 = f2_fma(f2_pack(__uint_as_float(sr[c][2 * i]), __uint_as_float(sr[c][2 * i + 1])), c2, nb2);
+              float x0, x1;
+              f2_unpack(x2, x0, x1);
+              const float p0 = ex2(x0), p1 = ex2(x1);
+              ls2[i & 3] = f2_add(ls2[i & 3], f2_pack(p0, p1));
+              pk[i] = pack_bf16x2(p0, p1);
             }
-            pk[i] = pack_e4m3x4(pv[0], pv[1], pv[2], pv[3]);
+            tmem_st16(s_addr + 16u * c, pk);
           }
-          tmem_st16(s_addr + 16u * h2, pk);
-        }
-      }
-      l_run += (((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]))) * inv_r;
-      if (__any_sync(0xffffffffu, rescale)) {
-        // O_t holds PV_t(j-1) complete (it preceded S_t(j)); PV_t(j) waits for this warp's
-        // arrival below, so O_t can be rescaled in place now (S_t's registers are dead here).
-#pragma unroll 1
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t o[32];
-          tmem_ld32(o_addr + 32u * c, o);
-          tmem_wait_ld();
+        } else {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            reg_fence(o[i]);
-            o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+          for (int h2 = 0; h2 < 2; ++h2) {
+            uint32_t pk[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              float pv[4];
+#pragma unroll
+              for (int e = 0; e < 4; e += 2) {
+                const int col = 64 * h2 + 4 * i + e;
+                const uint64_t x2 = f2_fma(f2_pack(__uint_as_float(sr[col / 32][col % 32]),
+                                                   __uint_as_float(sr[col / 32][col % 32 + 1])), c2, nb2);
+                float x0, x1;
+                f2_unpack(x2, x0, x1);
+                pv[e] = ex2(x0);
+                pv[e + 1] = ex2(x1);
+                ls2[(2 * i + e / 2) & 3] = f2_add(ls2[(2 * i + e / 2) & 3], f2_pack(pv[e], pv[e + 1]));
+              }
+              pk[i] = pack_e4m3x4(pv[0], pv[1], pv[2], pv[3]);
+            }
+            tmem_st16(s_addr + 16u * h2, pk);
           }
-          tmem_st32(o_addr + 32u * c, o);
         }
+        {
+          const uint64_t t2 = f2_add(f2_add(ls2[0], ls2[1]), f2_add(ls2[2], ls2[3]));
+          float a0, a1;
+          f2_unpack(t2, a0, a1);
+          l_run += (a0 + a1) * inv_r;
+        }
+        if (__any_sync(0xffffffffu, rescale)) {
+          // O_t holds PV_t(j-1) complete (it preceded S_t(j)); PV_t(j) waits for this warp's
+          // arrival below, so O_t can be rescaled in place now (S_t's registers are dead here).
+#pragma unroll 1
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t o[32];
+            tmem_ld32(o_addr + 32u * c, o);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              reg_fence(o[i]);
+              o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+            }
+            tmem_st32(o_addr + 32u * c, o);
+          }
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(BAR_P_FULL(t));
       }
-      tmem_wait_st();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(BAR_P_FULL(t));
-    }
+      if (!ok) break;
 
-    // ---- epilogue: O / l -> bf16, lse ----
-    if (ok && nt > 0 && wait_bounded(BAR_O_FULL(t), 0, ctl, WHERE_SOFTMAX)) {
+      // ---- epilogue: O / l -> bf16, lse; then hand O_t back to the MMA warp ----
+      if (!wait_bounded(BAR_O_FULL(t), ouse & 1, ctl, WHERE_SOFTMAX)) { ok = false; break; }
+      ++ouse;
       tc_fence_after();
       const float inv_l = sv_max / l_run;
       const bool valid = row < p.S;
       __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(p.o) +
-                            ((static_cast<size_t>(b) * p.S + (valid ? row : 0)) * p.H + h) * D;
+                            ((static_cast<size_t>(it.b) * p.S + (valid ? row : 0)) * p.H + it.h) * D;
 #pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {
         uint32_t o[32];
@@ -472,8 +545,11 @@ __global__ void __launch_bounds__(AttnCfg<D, FP8>::THREADS, 1)
             dst[v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
         }
       }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(BAR_O_EMPTY(t));
       if (valid && p.lse != nullptr)
-        p.lse[static_cast<size_t>(hb) * p.S + row] = (m_run + __log2f(l_run)) * LN2;
+        p.lse[static_cast<size_t>(it.hb) * p.S + row] = (m_run + __log2f(l_run)) * LN2;
     }
   }
 
@@ -501,7 +577,15 @@ cudaError_t launch_attn(const CUtensorMap& tq, const CUtensorMap& tk, const CUte
     if (e != cudaSuccess) return e;
     configured.fetch_or(bit);
   }
-  const long long grid = static_cast<long long>(p.nQB) * p.H * p.B;
+  static int sm_count[64] = {0};
+  if (sm_count[dev & 63] == 0) {
+    int n = 0;
+    e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    sm_count[dev & 63] = n;
+  }
+  const long long items = static_cast<long long>(p.nQB) * p.H * p.B;
+  const long long grid = items < sm_count[dev & 63] ? items : sm_count[dev & 63];   // persistent
   attn_fwd_kernel<D, FP8, CAUSAL>
       <<<static_cast<unsigned>(grid), C::THREADS, C::SMEM_BYTES, stream>>>(tq, tk, tv, p);
   return cudaGetLastError();
