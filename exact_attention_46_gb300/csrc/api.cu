@@ -265,11 +265,16 @@ int hadamard_rotate_quant_fp8(const void* x, void* out, float* scale, const floa
   const size_t sbytes = 4ull * B * H * nblk;
   if (overlap(out, n, x, 2 * n) || overlap(scale, sbytes, x, 2 * n) || overlap(scale, sbytes, out, n))
     return fail(ATTN_ERR_INVALID_ARG, "outputs overlap the input or each other");
-  QuantParams p{B, H, S, nblk, x, out, scale, signs};
+  int* err = nullptr;
+  int rc = err_words(&err);
+  if (rc != ATTN_OK) return rc;
+  CUtensorMap tx;
+  if ((rc = make_qkv_map(&tx, x, B, S, H, D, false)) != ATTN_OK) return rc;
+  QuantParams p{B, H, S, nblk, out, scale, signs, spin_limit(), err, err + 1};
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  cudaError_t e = D == 64    ? launch_hadamard_quant<64>(p, st)
-                  : D == 128 ? launch_hadamard_quant<128>(p, st)
-                             : launch_hadamard_quant<256>(p, st);
+  cudaError_t e = D == 64    ? launch_hadamard_quant<64>(tx, p, st)
+                  : D == 128 ? launch_hadamard_quant<128>(tx, p, st)
+                             : launch_hadamard_quant<256>(tx, p, st);
   if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "quantiser launch failed: %s", cudaGetErrorString(e));
   return ok();
 }

@@ -5,16 +5,21 @@
 // [B, S, H, D] bf16 tensor becomes x' = (x * signs) H_D / sqrt(D) (H_D the Sylvester
 // Hadamard matrix; no rotation when signs is null), each (b, h, 128-token block) gets one
 // scale = amax(|x'|) / 448 (1 for an all-zero block), and out = E4M3(x' / scale), rounded to
-// nearest even and saturating.
+// nearest even and saturating.  The rounded quotient is formed in fp32 as
+// y * (448 / amax(y)) with y = (x * signs) H_D the unnormalised transform.
 //
 // Design: the transform is O(D log D) per row and the kernel is bound by HBM traffic
-// (2 bytes read + 1 byte written per element), so it stays on the FP32 pipes: no tensor
-// cores.  One CTA = one (b, h, token block) = 128 rows; 4 lanes share a row, each holding
-// D/4 elements chosen so that every 16-byte load of a row segment is contiguous across the
-// 4 lanes (element index = 32*i + 8*part + e).  Butterflies over index bits 0-2 (e) and
-// 5.. (i) stay inside a thread; bits 3-4 (part) take two shuffle stages.  The block amax is
-// a warp shuffle reduction plus one shared-memory pass; values stay in registers between
-// the two phases, so the input is read exactly once.
+// (2 bytes read + 1 byte written per element) once its instruction count is low, so it stays
+// on the FP32 pipes: no tensor cores.  Persistent CTAs stream blocks of 128 rows through a
+// ring of shared-memory stages filled by TMA (the same 128-byte-swizzled box the attention
+// kernel uses), so the loads of the next blocks are in flight while a block is transformed.
+// A thread owns one row (two adjacent lanes share a row at D = 256), so every butterfly
+// stage runs in registers without shuffles (one shuffle stage at D = 256); the 32 lanes of
+// a warp read the same 16-byte chunk of 32 rows, which the swizzle makes conflict-free.  The
+// random signs are applied as XOR masks on the packed bf16 words, read from a small
+// shared-memory table by broadcast.  Rows beyond S arrive zero-filled and are never stored.
+// Codes go straight to global memory, 16 bytes at a time.
+#include <atomic>
 #include <cstdint>
 #include <cuda_bf16.h>
 
@@ -26,110 +31,196 @@ namespace ea46 {
 namespace {
 
 constexpr int QROWS = 128;            // tokens per scale block
-constexpr int QTHREADS = QROWS * 4;   // 4 lanes per row
+
+template <int D>
+struct QCfg {
+  static constexpr int TPR = D > 128 ? D / 128 : 1;                        // threads per row
+  static constexpr int VPT = D / TPR;                                      // values per thread
+  static constexpr int THREADS = QROWS * TPR;
+  static constexpr int ROW_BYTES = D * 2;                                  // bf16 row
+  static constexpr int PANEL_BYTES = 128 * 128;                            // 128 rows x 128 B
+  static constexpr int NPANEL = ROW_BYTES / 128;                           // 1, 2, 4
+  static constexpr int STAGE_BYTES = QROWS * ROW_BYTES;
+  static constexpr int CTAS_PER_SM = D == 64 ? 4 : (D == 128 ? 3 : 1);
+  static constexpr int NSTAGE = D == 256 ? 3 : 2;
+  static constexpr int NWARPS = THREADS / 32;
+  static constexpr int SMEM_BYTES =
+      NSTAGE * STAGE_BYTES + 1024 + 8 * NSTAGE + 4 * (D / 2) + 2 * NWARPS * 4 + 16;
+  static_assert(SMEM_BYTES * CTAS_PER_SM <= 227 * 1024, "shared memory budget");
+};
 
 template <int D, bool ROTATE>
-__global__ void __launch_bounds__(QTHREADS)
-    hadamard_quant_kernel(const QuantParams p) {
-  constexpr int NI = D / 32;          // 16-byte groups per thread
-  constexpr int VPT = D / 4;          // values per thread
-  __shared__ float warp_max[QTHREADS / 32];
+__global__ void __launch_bounds__(QCfg<D>::THREADS, QCfg<D>::CTAS_PER_SM)
+    hadamard_quant_kernel(const __grid_constant__ CUtensorMap tmX, const QuantParams p) {
+  using C = QCfg<D>;
+  constexpr int VPT = C::VPT;
+  constexpr int NSTAGE = C::NSTAGE;
+  constexpr int NW = VPT / 8;         // 16-byte input chunks per thread
 
-  const int blk = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_u32 = smem_u32(smem_raw);
+  const uint32_t base_u32 = (raw_u32 + 1023u) & ~1023u;
+  uint8_t* base = smem_raw + (base_u32 - raw_u32);
+  // layout: stages (1024-aligned) | sign masks [D/2] (16-byte vector reads) | barriers | warp maxima
+  uint32_t* sign_mask = reinterpret_cast<uint32_t*>(base + NSTAGE * C::STAGE_BYTES);                // [D/2]
+  const uint32_t bar0 = base_u32 + NSTAGE * C::STAGE_BYTES + 4 * (D / 2);
+  float* warp_max = reinterpret_cast<float*>(base + NSTAGE * C::STAGE_BYTES + 4 * (D / 2) + 8 * NSTAGE);  // [2][NWARPS]
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(warp_max + 2 * C::NWARPS);
+  static_assert((C::STAGE_BYTES * NSTAGE) % 16 == 0 && (4 * (D / 2)) % 8 == 0, "alignment");
+
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int part = lane & 3;
-  const int r = warp * 8 + (lane >> 2);          // row within the block
-  const int tok = blk * QROWS + r;
-  const bool valid = tok < p.S;
-  const size_t row_off = (static_cast<size_t>(b) * p.S + (valid ? tok : 0)) * p.H + h;
+  // row and the part of it this thread owns (TPR = 2: adjacent lanes share a row)
+  const int r = static_cast<int>(threadIdx.x) / C::TPR;
+  const int half = static_cast<int>(threadIdx.x) % C::TPR;
+  const int nblocks = p.nblk * p.H * p.B;
 
-  float v[VPT];
-  const uint4* src = reinterpret_cast<const uint4*>(
-      reinterpret_cast<const __nv_bfloat16*>(p.x) + row_off * D);
-#pragma unroll
-  for (int i = 0; i < NI; ++i) {
-    uint4 w = valid ? __ldg(src + 4 * i + part) : make_uint4(0, 0, 0, 0);
-    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      v[8 * i + 2 * k] = __uint_as_float(ws[k] << 16);
-      v[8 * i + 2 * k + 1] = __uint_as_float(ws[k] & 0xFFFF0000u);
-    }
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < NSTAGE; ++s) mbar_init(bar0 + 8u * s, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+    prefetch_tmap(&tmX);
   }
+  // bit 15 flips the even element of a packed bf16 pair, bit 31 the odd one
+  for (int w = static_cast<int>(threadIdx.x); w < D / 2; w += C::THREADS)
+    sign_mask[w] = ROTATE ? ((p.signs[2 * w] < 0.f ? 0x00008000u : 0u) |
+                             (p.signs[2 * w + 1] < 0.f ? 0x80000000u : 0u))
+                          : 0u;
+  __syncthreads();
+  const WaitCtl ctl{p.spin_limit, abort_flag, p.err_word, p.err_info};
 
-  if (ROTATE) {
-    const float4* sg = reinterpret_cast<const float4*>(p.signs);
+  int n_issued = 0;                 // thread 0 only: blocks whose load has been issued
+  auto issue = [&](int k) {         // k-th block of this CTA into stage k % NSTAGE
+    const int bi = static_cast<int>(blockIdx.x) + k * static_cast<int>(gridDim.x);
+    const int h = bi % p.H, blk = (bi / p.H) % p.nblk, b = bi / (p.H * p.nblk);
+    const uint32_t st = base_u32 + (k % NSTAGE) * C::STAGE_BYTES;
+    const uint32_t bar = bar0 + 8u * (k % NSTAGE);
+    mbar_arrive_expect_tx(bar, C::STAGE_BYTES);
 #pragma unroll
-    for (int i = 0; i < NI; ++i) {
-      const float4 s0 = __ldg(sg + 8 * i + 2 * part);
-      const float4 s1 = __ldg(sg + 8 * i + 2 * part + 1);
-      v[8 * i + 0] *= s0.x; v[8 * i + 1] *= s0.y; v[8 * i + 2] *= s0.z; v[8 * i + 3] *= s0.w;
-      v[8 * i + 4] *= s1.x; v[8 * i + 5] *= s1.y; v[8 * i + 6] *= s1.z; v[8 * i + 7] *= s1.w;
-    }
-    // index bits 0-2: inside each 8-group
+    for (int pn = 0; pn < C::NPANEL; ++pn)
+      tma_load_4d(st + pn * C::PANEL_BYTES, &tmX, bar, 64 * pn, h, blk * QROWS, b,
+                  l2_policy_evict_first());
+    n_issued = k + 1;
+  };
+  const int my_blocks = (nblocks - static_cast<int>(blockIdx.x) + static_cast<int>(gridDim.x) - 1) /
+                        static_cast<int>(gridDim.x);
+  if (threadIdx.x == 0)
+    for (int k = 0; k < NSTAGE && k < my_blocks; ++k) issue(k);
+
+  for (int k = 0; k < my_blocks; ++k) {
+    // Blocks are numbered head-fastest: the CTAs running at one time read all heads of the
+    // same tokens, i.e. contiguous memory.
+    const int bi = static_cast<int>(blockIdx.x) + k * static_cast<int>(gridDim.x);
+    const int h = bi % p.H, blk = (bi / p.H) % p.nblk, b = bi / (p.H * p.nblk);
+    const int hb = b * p.H + h;
+    const int stage = k % NSTAGE;
+    const uint32_t st = base_u32 + stage * C::STAGE_BYTES;
+    const bool ok = wait_bounded(bar0 + 8u * stage, (k / NSTAGE) & 1, ctl, 10);
+
+    float v[VPT];
 #pragma unroll
-    for (int hs = 1; hs < 8; hs <<= 1)
+    for (int c = 0; c < NW; ++c) {
+      const int idx = half * VPT + 8 * c;                  // first element of the chunk
+      const int pn = idx / 64, cc = (idx % 64) / 8;        // panel, 16-byte chunk in the row
+      const uint32_t addr = st + pn * C::PANEL_BYTES + r * 128 + ((cc ^ (r & 7)) << 4);
+      uint32_t w[4];
+      asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                   : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]) : "r"(addr));
+      if (ROTATE) {
+        const uint4 m = reinterpret_cast<const uint4*>(sign_mask)[idx / 8];
+        w[0] ^= m.x; w[1] ^= m.y; w[2] ^= m.z; w[3] ^= m.w;
+      }
 #pragma unroll
-      for (int i = 0; i < NI; ++i)
-#pragma unroll
-        for (int e = 0; e < 8; ++e)
-          if ((e & hs) == 0) {
-            const float a = v[8 * i + e], c = v[8 * i + e + hs];
-            v[8 * i + e] = a + c;
-            v[8 * i + e + hs] = a - c;
-          }
-    // index bits 3-4: across the 4 lanes of the row
-#pragma unroll
-    for (int lm = 1; lm < 4; lm <<= 1) {
-      const bool upper = (part & lm) != 0;
-#pragma unroll
-      for (int k = 0; k < VPT; ++k) {
-        const float o = __shfl_xor_sync(0xffffffffu, v[k], lm);
-        v[k] = upper ? (o - v[k]) : (v[k] + o);
+      for (int q = 0; q < 4; ++q) {
+        v[8 * c + 2 * q] = __uint_as_float(w[q] << 16);
+        v[8 * c + 2 * q + 1] = __uint_as_float(w[q] & 0xFFFF0000u);
       }
     }
-    // index bits 5..: across the 8-groups of a thread
+
+    // The values are in registers: refill the stage now, so the next blocks' loads stay in
+    // flight while this one is transformed.
+    if (__syncthreads_or(!ok)) break;
+    if (threadIdx.x == 0 && k + NSTAGE < my_blocks) issue(k + NSTAGE);
+
+    if (ROTATE) {
+      // butterflies over the index bits held by this thread: bit 0 pairs the two halves of a
+      // packed pair, every higher bit pairs whole pairs, done with f32x2 add/sub
 #pragma unroll
-    for (int is = 1; is < NI; is <<= 1)
+      for (int e = 0; e < VPT; e += 2) {
+        const float a = v[e], c2 = v[e + 1];
+        v[e] = a + c2;
+        v[e + 1] = a - c2;
+      }
 #pragma unroll
-      for (int i = 0; i < NI; ++i)
-        if ((i & is) == 0)
+      for (int hs = 2; hs < VPT; hs <<= 1)
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const float a = v[8 * i + e], c = v[8 * i + is * 8 + e];
-            v[8 * i + e] = a + c;
-            v[8 * i + is * 8 + e] = a - c;
+        for (int e = 0; e < VPT; e += 2)
+          if ((e & hs) == 0) {
+            const uint64_t a2 = f2_pack(v[e], v[e + 1]), b2 = f2_pack(v[e + hs], v[e + hs + 1]);
+            f2_unpack(f2_add(a2, b2), v[e], v[e + 1]);
+            f2_unpack(f2_sub(a2, b2), v[e + hs], v[e + hs + 1]);
           }
+      if (C::TPR == 2) {
+        // the top index bit lives in the adjacent lane: lower half a+b, upper half a-b
+        const float sgn = half ? -1.f : 1.f;
+#pragma unroll
+        for (int e = 0; e < VPT; e += 2) {
+          const float o0 = __shfl_xor_sync(0xffffffffu, v[e], 1);
+          const float o1 = __shfl_xor_sync(0xffffffffu, v[e + 1], 1);
+          const uint64_t r2 = f2_fma(f2_pack(v[e], v[e + 1]), f2_pack(sgn, sgn), f2_pack(o0, o1));
+          f2_unpack(r2, v[e], v[e + 1]);
+        }
+      }
+    }
+
+    float amax = 0.f;
+#pragma unroll
+    for (int e = 0; e < VPT; e += 2) amax = max3(amax, fabsf(v[e]), fabsf(v[e + 1]));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    float* wm = warp_max + C::NWARPS * (k & 1);
+    if (lane == 0) wm[warp] = amax;
+    __syncthreads();
+    amax = wm[0];
+#pragma unroll
+    for (int w = 1; w < C::NWARPS; ++w) amax = fmaxf(amax, wm[w]);
+
+    const float inv = amax > 0.f ? 448.f / amax : 0.f;
+    if (threadIdx.x == 0) {
+      const float norm = ROTATE ? rsqrtf(static_cast<float>(D)) : 1.f;
+      p.scale[static_cast<size_t>(hb) * p.nblk + blk] = amax > 0.f ? (amax * norm) / 448.f : 1.f;
+    }
+    const int tok = blk * QROWS + r;
+    if (tok < p.S) {
+      uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(p.out) +
+                                            ((static_cast<size_t>(b) * p.S + tok) * p.H + h) * D +
+                                            half * VPT);
+      const uint64_t inv2 = f2_pack(inv, inv);
+#pragma unroll
+      for (int c = 0; c < VPT / 16; ++c) {
+        uint32_t wq[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          float y[4];
+#pragma unroll
+          for (int e = 0; e < 4; e += 2)
+            f2_unpack(f2_mul(f2_pack(v[16 * c + 4 * q + e], v[16 * c + 4 * q + e + 1]), inv2), y[e], y[e + 1]);
+          wq[q] = pack_e4m3x4(y[0], y[1], y[2], y[3]);
+        }
+        dst[c] = make_uint4(wq[0], wq[1], wq[2], wq[3]);
+      }
+    }
   }
 
-  float amax = 0.f;
-#pragma unroll
-  for (int k = 0; k < VPT; ++k) amax = fmaxf(amax, fabsf(v[k]));
-  if (!valid) amax = 0.f;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-  if (lane == 0) warp_max[warp] = amax;
-  __syncthreads();
-  amax = warp_max[0];
-#pragma unroll
-  for (int w = 1; w < QTHREADS / 32; ++w) amax = fmaxf(amax, warp_max[w]);
-
-  // x' = y / sqrt(D); scale = amax(x') / 448; code = E4M3(x' / scale) = E4M3(y * 448 / amax(y)).
-  const float inv = amax > 0.f ? 448.f / amax : 0.f;
-  if (threadIdx.x == 0) {
-    const float norm = ROTATE ? rsqrtf(static_cast<float>(D)) : 1.f;
-    p.scale[(static_cast<size_t>(b) * p.H + h) * p.nblk + blk] =
-        amax > 0.f ? (amax * norm) / 448.f : 1.f;
-  }
-  if (valid) {
-    uint2* dst = reinterpret_cast<uint2*>(reinterpret_cast<uint8_t*>(p.out) + row_off * D);
-#pragma unroll
-    for (int i = 0; i < NI; ++i) {
-      const uint32_t lo = pack_e4m3x4(v[8 * i] * inv, v[8 * i + 1] * inv, v[8 * i + 2] * inv,
-                                      v[8 * i + 3] * inv);
-      const uint32_t hi = pack_e4m3x4(v[8 * i + 4] * inv, v[8 * i + 5] * inv,
-                                      v[8 * i + 6] * inv, v[8 * i + 7] * inv);
-      dst[4 * i + part] = make_uint2(lo, hi);
+  // On an abort, copies still in flight must land before the CTA exits.
+  if (threadIdx.x == 0 && *abort_flag) {
+    for (int s = 0; s < NSTAGE; ++s) {
+      int last = -1;
+      for (int k = s; k < n_issued; k += NSTAGE) last = k;
+      if (last >= 0) {
+        const long long t0 = clock64();
+        while (!mbar_try_wait(bar0 + 8u * s, (last / NSTAGE) & 1))
+          if (clock64() - t0 > p.spin_limit) break;
+      }
     }
   }
 }
@@ -137,17 +228,37 @@ __global__ void __launch_bounds__(QTHREADS)
 }  // namespace
 
 template <int D>
-cudaError_t launch_hadamard_quant(const QuantParams& p, cudaStream_t stream) {
-  const dim3 grid(p.nblk, p.H, p.B);
+cudaError_t launch_hadamard_quant(const CUtensorMap& tx, const QuantParams& p, cudaStream_t stream) {
+  using C = QCfg<D>;
+  static std::atomic<unsigned long long> configured{0};
+  static int sm_count[64] = {0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const unsigned long long bit = 1ull << (dev & 63);
+  if ((configured.load() & bit) == 0) {
+    e = cudaFuncSetAttribute(hadamard_quant_kernel<D, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(hadamard_quant_kernel<D, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    int n = 0;
+    e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    sm_count[dev & 63] = n;
+    configured.fetch_or(bit);
+  }
+  const long long nblocks = static_cast<long long>(p.nblk) * p.H * p.B;
+  const long long cap = static_cast<long long>(sm_count[dev & 63]) * C::CTAS_PER_SM;
+  const unsigned grid = static_cast<unsigned>(nblocks < cap ? nblocks : cap);
   if (p.signs != nullptr)
-    hadamard_quant_kernel<D, true><<<grid, QTHREADS, 0, stream>>>(p);
+    hadamard_quant_kernel<D, true><<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(tx, p);
   else
-    hadamard_quant_kernel<D, false><<<grid, QTHREADS, 0, stream>>>(p);
+    hadamard_quant_kernel<D, false><<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(tx, p);
   return cudaGetLastError();
 }
 
-template cudaError_t launch_hadamard_quant<64>(const QuantParams&, cudaStream_t);
-template cudaError_t launch_hadamard_quant<128>(const QuantParams&, cudaStream_t);
-template cudaError_t launch_hadamard_quant<256>(const QuantParams&, cudaStream_t);
+template cudaError_t launch_hadamard_quant<64>(const CUtensorMap&, const QuantParams&, cudaStream_t);
+template cudaError_t launch_hadamard_quant<128>(const CUtensorMap&, const QuantParams&, cudaStream_t);
+template cudaError_t launch_hadamard_quant<256>(const CUtensorMap&, const QuantParams&, cudaStream_t);
 
 }  // namespace ea46

@@ -34,13 +34,16 @@ constexpr int attn_q_tiles(int D) { return D == 256 ? 1 : 2; }
 
 struct QuantParams {
   int B, H, S, nblk;
-  const void* x;        // [B, S, H, D] bf16
   void* out;            // [B, S, H, D] E4M3
   float* scale;         // [B, H, nblk]
   const float* signs;   // [D] or nullptr
+  long long spin_limit; // cycles a bounded wait may spin
+  int* err_word;        // device error word
+  int* err_info;
 };
 
+// x is read through `tx`, the same [B, S, H, D] bf16 tensor map the attention kernel uses.
 template <int D>
-cudaError_t launch_hadamard_quant(const QuantParams& p, cudaStream_t stream);
+cudaError_t launch_hadamard_quant(const CUtensorMap& tx, const QuantParams& p, cudaStream_t stream);
 
 }  // namespace ea46

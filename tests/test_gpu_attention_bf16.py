@@ -47,6 +47,14 @@ def test_full_rows_small(S, D, causal):
     run_and_check(2, S, 3, D, causal, case=1)
 
 
+@pytest.mark.parametrize("D", [64, 128, 256])
+@pytest.mark.parametrize("causal", [False, True])
+def test_full_rows_more_items_than_sms(D, causal):
+    # 8 * 24 heads * ceil(300 / rows per CTA) items > 152 CTAs: every CTA of the persistent
+    # kernel walks several items, and the ragged tail sits in the last query block.
+    run_and_check(8, 300, 24, D, causal, case=11)
+
+
 @pytest.mark.parametrize("S", [512, 1024, 2048, 4096, 8192, 16384])
 def test_benchmark_sizes_d128(S):
     run_and_check(16384 // S, S, 16, 128, False, case=2, rows=sample_rows(S))
