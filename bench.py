@@ -65,7 +65,7 @@ def load_peaks():
 def kernel_source_sha():
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "exact_attention_46_gb300", "csrc")
-    for name in ("attn_kernel.cuh", "ptx.cuh", "hadamard_quant.cu"):
+    for name in ("attn_kernel.cuh", "ptx.cuh", "attn_bf16.cu"):
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -330,6 +330,41 @@ def cpu_baseline_sample(budget_s=12.0):
             "kind": "oracle", "sample": smp.describe(n, dt)}
 
 
+def rope_fusion(dev, n=30):
+    """Rotary embedding fused into the rotation + quantiser vs the rotation + quantiser alone,
+    at the benchmark size (device time per launch, microseconds).  Launches cycle through three
+    64 MB tensors, so each reads input last touched two launches (128 MB) earlier."""
+    from exact_attention_46_gb300 import ops
+    B, S = TOKENS // HEADLINE_S, HEADLINE_S
+    g = torch.Generator(device=dev).manual_seed(7)
+    xs = [torch.randn((B, S, H, D), generator=g, device=dev, dtype=torch.float32).to(torch.bfloat16)
+          for _ in range(3)]
+    s = torch.where(torch.rand(D, generator=g, device=dev) < 0.5, -1.0, 1.0)
+    cs = ops.rope_cos_sin_table(S, D)
+    out = torch.empty(xs[0].shape, dtype=torch.uint8, device=dev)
+    sc = torch.empty((B, H, (S + 127) // 128), dtype=torch.float32, device=dev)
+    res = {}
+    for name, fn in (("rotate_quant_us", lambda x: ops.hadamard_rotate_quant_fp8(x, s, out=out, scale=sc)),
+                     ("rope_rotate_quant_us", lambda x: ops.rope_hadamard_rotate_quant_fp8(x, cs, s, out=out, scale=sc))):
+        for i in range(6):
+            fn(xs[i % 3])
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record()
+        for i in range(n):
+            fn(xs[i % 3])
+        e1.record()
+        torch.cuda.synchronize()
+        res[name] = round(e0.elapsed_time(e1) / n * 1e3, 2)
+    ops.check()
+    qb = quant_bytes(B, S, H, D)
+    res["rope_table_bytes"] = S * D * 4
+    res["fused_gbs"] = round((qb + S * D * 4) / res["rope_rotate_quant_us"] / 1e3, 1)
+    res["extra_time_frac"] = round(res["rope_rotate_quant_us"] / res["rotate_quant_us"] - 1, 4)
+    res["workload"] = f"B={B} S={S} H={H} D={D} bf16 -> E4M3, random-sign rotation, RoPE base 1e4"
+    return res
+
+
 def run_ours(args):
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -382,6 +417,7 @@ def run_ours(args):
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / n_e2e, dist_on, dev)
 
     sw = sweep(dev) if (args.sweep and rank == 0) else None
+    rf = rope_fusion(dev) if (args.sweep and rank == 0) else None
     peaks, peak_src = load_peaks()
     cpu = cpu_baseline_sample() if (rank == 0 and world == 1 and args.cpu_baseline) else None
 
@@ -432,6 +468,7 @@ def run_ours(args):
             "clocks": clk,
             "cpu_baseline": cpu,
             "sweep": sw,
+            "rope_fusion": rf,
         }
         print(json.dumps(line), flush=True)
     if dist_on:

@@ -15,10 +15,13 @@ _P = ctypes.c_void_p
 _I = ctypes.c_int
 _F = ctypes.c_float
 _LL = ctypes.c_longlong
+_D = ctypes.c_double
 SIGNATURES = {
     "attn_fwd": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P]),
     "attn_fwd_fp8": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _P]),
     "hadamard_rotate_quant_fp8": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _P]),
+    "rope_cos_sin_table": (_I, [_P, _I, _I, _D, _P]),
+    "rope_hadamard_rotate_quant_fp8": (_I, [_P, _P, _I, _P, _P, _P, _I, _I, _I, _I, _P]),
     "attn_get_last_error": (ctypes.c_char_p, []),
     "attn_check": (_I, [_P]),
     "attn_set_spin_limit": (None, [_LL]),

@@ -222,6 +222,48 @@ __global__ void selftest_wait_kernel(long long limit, int* err) {
   __syncthreads();
 }
 
+int run_quant(const void* x, const float* rope_cs, int n_pos, void* out, float* scale, const float* signs,
+              int B, int H, int S, int D, void* stream) {
+  if (x == nullptr || out == nullptr || scale == nullptr)
+    return fail(ATTN_ERR_INVALID_ARG, "x, out and scale must be non-null device pointers");
+  if (B < 1 || H < 1 || S < 1)
+    return fail(ATTN_ERR_INVALID_ARG, "B, H, S must be >= 1 (got %d, %d, %d)", B, H, S);
+  if (D != 64 && D != 128 && D != 256)
+    return fail(D > 0 ? ATTN_ERR_UNSUPPORTED : ATTN_ERR_INVALID_ARG,
+                "head dimension D = %d not supported (64, 128, 256)", D);
+  if (!aligned16(x) || !aligned16(out) || (signs != nullptr && !aligned16(signs)) ||
+      (rope_cs != nullptr && !aligned16(rope_cs)) || (reinterpret_cast<uintptr_t>(scale) & 3u))
+    return fail(ATTN_ERR_INVALID_ARG, "x, out, signs, rope_cs must be 16-byte and scale 4-byte aligned");
+  const unsigned long long n = 1ull * B * S * H * D;
+  const int nblk = (S + 127) / 128;
+  if (n > (1ull << 40) / 2 || nblk > 0x7fffffff || H > 65535 || B > 65535)
+    return fail(ATTN_ERR_INVALID_ARG, "tensor too large for the grid");
+  if (rope_cs != nullptr && n_pos < 128 * nblk)
+    return fail(ATTN_ERR_INVALID_ARG,
+                "the rotary table needs rows for every position of the last 128-token block: "
+                "n_pos = %d < %d", n_pos, 128 * nblk);
+  const size_t sbytes = 4ull * B * H * nblk;
+  if (overlap(out, n, x, 2 * n) || overlap(scale, sbytes, x, 2 * n) || overlap(scale, sbytes, out, n))
+    return fail(ATTN_ERR_INVALID_ARG, "outputs overlap the input or each other");
+  if (rope_cs != nullptr) {
+    const size_t tbytes = 4ull * n_pos * D;
+    if (overlap(out, n, rope_cs, tbytes) || overlap(scale, sbytes, rope_cs, tbytes))
+      return fail(ATTN_ERR_INVALID_ARG, "outputs overlap the rotary table");
+  }
+  int* err = nullptr;
+  int rc = err_words(&err);
+  if (rc != ATTN_OK) return rc;
+  CUtensorMap tx;
+  if ((rc = make_qkv_map(&tx, x, B, S, H, D, false)) != ATTN_OK) return rc;
+  QuantParams p{B, H, S, nblk, out, scale, signs, rope_cs, spin_limit(), err, err + 1};
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = D == 64    ? launch_hadamard_quant<64>(tx, p, st)
+                  : D == 128 ? launch_hadamard_quant<128>(tx, p, st)
+                             : launch_hadamard_quant<256>(tx, p, st);
+  if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "quantiser launch failed: %s", cudaGetErrorString(e));
+  return ok();
+}
+
 }  // namespace
 
 extern "C" {
@@ -248,34 +290,26 @@ int attn_fwd_fp8(const void* q8, const void* k8, const void* v8, const float* q_
 
 int hadamard_rotate_quant_fp8(const void* x, void* out, float* scale, const float* signs, int B,
                               int H, int S, int D, void* stream) {
-  if (x == nullptr || out == nullptr || scale == nullptr)
-    return fail(ATTN_ERR_INVALID_ARG, "x, out and scale must be non-null device pointers");
-  if (B < 1 || H < 1 || S < 1)
-    return fail(ATTN_ERR_INVALID_ARG, "B, H, S must be >= 1 (got %d, %d, %d)", B, H, S);
-  if (D != 64 && D != 128 && D != 256)
-    return fail(D > 0 ? ATTN_ERR_UNSUPPORTED : ATTN_ERR_INVALID_ARG,
-                "head dimension D = %d not supported (64, 128, 256)", D);
-  if (!aligned16(x) || !aligned16(out) || (signs != nullptr && !aligned16(signs)) ||
-      (reinterpret_cast<uintptr_t>(scale) & 3u))
-    return fail(ATTN_ERR_INVALID_ARG, "x, out, signs must be 16-byte and scale 4-byte aligned");
-  const unsigned long long n = 1ull * B * S * H * D;
-  const int nblk = (S + 127) / 128;
-  if (n > (1ull << 40) / 2 || nblk > 0x7fffffff || H > 65535 || B > 65535)
-    return fail(ATTN_ERR_INVALID_ARG, "tensor too large for the grid");
-  const size_t sbytes = 4ull * B * H * nblk;
-  if (overlap(out, n, x, 2 * n) || overlap(scale, sbytes, x, 2 * n) || overlap(scale, sbytes, out, n))
-    return fail(ATTN_ERR_INVALID_ARG, "outputs overlap the input or each other");
-  int* err = nullptr;
-  int rc = err_words(&err);
-  if (rc != ATTN_OK) return rc;
-  CUtensorMap tx;
-  if ((rc = make_qkv_map(&tx, x, B, S, H, D, false)) != ATTN_OK) return rc;
-  QuantParams p{B, H, S, nblk, out, scale, signs, spin_limit(), err, err + 1};
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  cudaError_t e = D == 64    ? launch_hadamard_quant<64>(tx, p, st)
-                  : D == 128 ? launch_hadamard_quant<128>(tx, p, st)
-                             : launch_hadamard_quant<256>(tx, p, st);
-  if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "quantiser launch failed: %s", cudaGetErrorString(e));
+  return run_quant(x, nullptr, 0, out, scale, signs, B, H, S, D, stream);
+}
+
+int rope_hadamard_rotate_quant_fp8(const void* x, const float* rope_cs, int n_pos, void* out, float* scale,
+                                   const float* signs, int B, int H, int S, int D, void* stream) {
+  if (rope_cs == nullptr) return fail(ATTN_ERR_INVALID_ARG, "rope_cs must be a non-null device pointer");
+  return run_quant(x, rope_cs, n_pos, out, scale, signs, B, H, S, D, stream);
+}
+
+int rope_cos_sin_table(float* cs, int n_pos, int D, double base, void* stream) {
+  if (cs == nullptr) return fail(ATTN_ERR_INVALID_ARG, "cs must be a non-null device pointer");
+  if (n_pos < 1 || n_pos > (1 << 26))
+    return fail(ATTN_ERR_INVALID_ARG, "n_pos must be in [1, 2^26] (got %d)", n_pos);
+  if (D < 2 || D % 2 != 0 || D > 4096)
+    return fail(ATTN_ERR_INVALID_ARG, "D must be even and in [2, 4096] (got %d)", D);
+  if (!(base > 0.0) || !std::isfinite(base))
+    return fail(ATTN_ERR_INVALID_ARG, "base must be finite and > 0");
+  if (reinterpret_cast<uintptr_t>(cs) & 7u) return fail(ATTN_ERR_INVALID_ARG, "cs must be 8-byte aligned");
+  cudaError_t e = launch_rope_table(cs, n_pos, D, base, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "rotary table launch failed: %s", cudaGetErrorString(e));
   return ok();
 }
 
@@ -313,6 +347,6 @@ int attn_selftest_bounded_wait(long long spin_cycles, void* stream) {
   return ok();
 }
 
-int attn_version(void) { return 100; }
+int attn_version(void) { return 101; }
 
 }  // extern "C"

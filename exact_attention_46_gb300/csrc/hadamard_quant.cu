@@ -19,6 +19,15 @@
 // random signs are applied as XOR masks on the packed bf16 words, read from a small
 // shared-memory table by broadcast.  Rows beyond S arrive zero-filled and are never stored.
 // Codes go straight to global memory, 16 bytes at a time.
+//
+// Rotary embedding fused in front (hada.io FA3 summary, same section: the transform is
+// bandwidth-bound and costs nothing extra when fused with a preceding bandwidth-bound op such
+// as rotary embedding).  RoPE as in RoFormer (Su et al. 2021, section 3.2): pair
+// (x[2i], x[2i+1]) of the row at position p turns by p * theta_i, before the signs and the
+// transform, with no rounding in between.  A 128-row block would need 128 table rows (4 D
+// bytes each, twice the block's own input), so the kernel rebuilds (cos, sin)(p theta_i) with
+// the angle-addition identity, as the complex product of table row 128 blk + 16 r1 (8 rows per
+// block, bulk-copied with the block) and table row r0 (16 rows, resident), r = 16 r1 + r0.
 #include <atomic>
 #include <cstdint>
 #include <cuda_bf16.h>
@@ -31,8 +40,10 @@ namespace ea46 {
 namespace {
 
 constexpr int QROWS = 128;            // tokens per scale block
+constexpr int NCOARSE = 8;            // rotary rows 128 blk + 16 r1 per block
+constexpr int NFINE = 16;             // rotary rows r0 = 0..15, resident
 
-template <int D>
+template <int D, bool ROPE>
 struct QCfg {
   static constexpr int TPR = D > 128 ? D / 128 : 1;                        // threads per row
   static constexpr int VPT = D / TPR;                                      // values per thread
@@ -41,18 +52,51 @@ struct QCfg {
   static constexpr int PANEL_BYTES = 128 * 128;                            // 128 rows x 128 B
   static constexpr int NPANEL = ROW_BYTES / 128;                           // 1, 2, 4
   static constexpr int STAGE_BYTES = QROWS * ROW_BYTES;
-  static constexpr int CTAS_PER_SM = D == 64 ? 4 : (D == 128 ? 3 : 1);
-  static constexpr int NSTAGE = D == 256 ? 3 : 2;
+  static constexpr int CTAS_PER_SM = D == 64 ? 4 : (D == 128 ? (ROPE ? 2 : 3) : 1);
+  static constexpr int NSTAGE = D == 256 && !ROPE ? 3 : 2;
   static constexpr int NWARPS = THREADS / 32;
-  static constexpr int SMEM_BYTES =
-      NSTAGE * STAGE_BYTES + 1024 + 8 * NSTAGE + 4 * (D / 2) + 2 * NWARPS * 4 + 16;
-  static_assert(SMEM_BYTES * CTAS_PER_SM <= 227 * 1024, "shared memory budget");
+  // rotary table rows in shared memory: each thread's VPT/2 pairs (8 bytes each) form one
+  // segment, padded by 16 bytes so that the rows of one warp's reads fall in distinct banks
+  static constexpr int SEG_BYTES = 4 * VPT;
+  static constexpr int SEG_STRIDE = SEG_BYTES + 16;
+  static constexpr int TROW = TPR * SEG_STRIDE;
+  static constexpr int NCSLOT = NSTAGE + 1;                                // coarse-row slots
+  static constexpr int OFF_COARSE = NSTAGE * STAGE_BYTES;
+  static constexpr int OFF_FINE = OFF_COARSE + (ROPE ? NCSLOT * NCOARSE * TROW : 0);
+  static constexpr int OFF_SIGN = OFF_FINE + (ROPE ? NFINE * TROW : 0);
+  // signs: packed-bf16 XOR masks [D/2] without RoPE, fp32 sign-bit masks [D] with it
+  static constexpr int SIGN_BYTES = ROPE ? 4 * D : 2 * D;
+  static constexpr int OFF_BAR = OFF_SIGN + SIGN_BYTES;
+  static constexpr int OFF_WMAX = OFF_BAR + 8 * NSTAGE;
+  static constexpr int OFF_ABORT = OFF_WMAX + 2 * NWARPS * 4;
+  static constexpr int SMEM_BYTES = 1024 + OFF_ABORT + 16;
+  static constexpr uint32_t TX_BYTES = STAGE_BYTES + (ROPE ? NCOARSE * TPR * SEG_BYTES : 0);
+  static_assert(SMEM_BYTES * CTAS_PER_SM + 1024 * CTAS_PER_SM <= 228 * 1024, "shared memory budget");
+  static_assert(OFF_COARSE % 16 == 0 && OFF_FINE % 16 == 0 && OFF_SIGN % 16 == 0 && OFF_BAR % 8 == 0,
+                "alignment");
 };
 
-template <int D, bool ROTATE>
-__global__ void __launch_bounds__(QCfg<D>::THREADS, QCfg<D>::CTAS_PER_SM)
+__device__ __forceinline__ float4 lds128(uint32_t addr) {
+  float4 f;
+  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(f.x), "=f"(f.y), "=f"(f.z), "=f"(f.w) : "r"(addr));
+  return f;
+}
+
+// Pair (v0, v1) turned by the angle whose (cos, sin) is the complex product of (ac, as)
+// and (fc, fs).
+__device__ __forceinline__ void rotary_pair(float& v0, float& v1, float ac, float as, float fc, float fs) {
+  const float c = ac * fc - as * fs;
+  const float s = as * fc + ac * fs;
+  const float x0 = v0, x1 = v1;
+  v0 = x0 * c - x1 * s;
+  v1 = x0 * s + x1 * c;
+}
+
+template <int D, bool ROTATE, bool ROPE>
+__global__ void __launch_bounds__(QCfg<D, ROPE>::THREADS, QCfg<D, ROPE>::CTAS_PER_SM)
     hadamard_quant_kernel(const __grid_constant__ CUtensorMap tmX, const QuantParams p) {
-  using C = QCfg<D>;
+  using C = QCfg<D, ROPE>;
   constexpr int VPT = C::VPT;
   constexpr int NSTAGE = C::NSTAGE;
   constexpr int NW = VPT / 8;         // 16-byte input chunks per thread
@@ -61,12 +105,10 @@ __global__ void __launch_bounds__(QCfg<D>::THREADS, QCfg<D>::CTAS_PER_SM)
   const uint32_t raw_u32 = smem_u32(smem_raw);
   const uint32_t base_u32 = (raw_u32 + 1023u) & ~1023u;
   uint8_t* base = smem_raw + (base_u32 - raw_u32);
-  // layout: stages (1024-aligned) | sign masks [D/2] (16-byte vector reads) | barriers | warp maxima
-  uint32_t* sign_mask = reinterpret_cast<uint32_t*>(base + NSTAGE * C::STAGE_BYTES);                // [D/2]
-  const uint32_t bar0 = base_u32 + NSTAGE * C::STAGE_BYTES + 4 * (D / 2);
-  float* warp_max = reinterpret_cast<float*>(base + NSTAGE * C::STAGE_BYTES + 4 * (D / 2) + 8 * NSTAGE);  // [2][NWARPS]
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(warp_max + 2 * C::NWARPS);
-  static_assert((C::STAGE_BYTES * NSTAGE) % 16 == 0 && (4 * (D / 2)) % 8 == 0, "alignment");
+  uint32_t* sign_mask = reinterpret_cast<uint32_t*>(base + C::OFF_SIGN);
+  const uint32_t bar0 = base_u32 + C::OFF_BAR;
+  float* warp_max = reinterpret_cast<float*>(base + C::OFF_WMAX);          // [2][NWARPS]
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(base + C::OFF_ABORT);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // row and the part of it this thread owns (TPR = 2: adjacent lanes share a row)
@@ -80,11 +122,24 @@ __global__ void __launch_bounds__(QCfg<D>::THREADS, QCfg<D>::CTAS_PER_SM)
     fence_barrier_init();
     prefetch_tmap(&tmX);
   }
-  // bit 15 flips the even element of a packed bf16 pair, bit 31 the odd one
-  for (int w = static_cast<int>(threadIdx.x); w < D / 2; w += C::THREADS)
-    sign_mask[w] = ROTATE ? ((p.signs[2 * w] < 0.f ? 0x00008000u : 0u) |
-                             (p.signs[2 * w + 1] < 0.f ? 0x80000000u : 0u))
-                          : 0u;
+  if (!ROPE) {
+    // bit 15 flips the even element of a packed bf16 pair, bit 31 the odd one
+    for (int w = static_cast<int>(threadIdx.x); w < D / 2; w += C::THREADS)
+      sign_mask[w] = ROTATE ? ((p.signs[2 * w] < 0.f ? 0x00008000u : 0u) |
+                               (p.signs[2 * w + 1] < 0.f ? 0x80000000u : 0u))
+                            : 0u;
+  } else {
+    // signs act after the rotary step, on fp32 values: one sign-bit mask per element
+    for (int w = static_cast<int>(threadIdx.x); w < D; w += C::THREADS)
+      sign_mask[w] = ROTATE && p.signs[w] < 0.f ? 0x80000000u : 0u;
+    // resident rotary rows 0..15, in the padded per-thread segment layout
+    for (int idx = static_cast<int>(threadIdx.x); idx < NFINE * (D / 2); idx += C::THREADS) {
+      const int f = idx / (D / 2), i = idx % (D / 2);
+      const float2 cs = reinterpret_cast<const float2*>(p.rope_cs)[idx];
+      *reinterpret_cast<float2*>(base + C::OFF_FINE + f * C::TROW + (i / (VPT / 2)) * C::SEG_STRIDE +
+                                 8 * (i % (VPT / 2))) = cs;
+    }
+  }
   __syncthreads();
   const WaitCtl ctl{p.spin_limit, abort_flag, p.err_word, p.err_info};
 
@@ -94,11 +149,24 @@ __global__ void __launch_bounds__(QCfg<D>::THREADS, QCfg<D>::CTAS_PER_SM)
     const int h = bi % p.H, blk = (bi / p.H) % p.nblk, b = bi / (p.H * p.nblk);
     const uint32_t st = base_u32 + (k % NSTAGE) * C::STAGE_BYTES;
     const uint32_t bar = bar0 + 8u * (k % NSTAGE);
-    mbar_arrive_expect_tx(bar, C::STAGE_BYTES);
+    mbar_arrive_expect_tx(bar, C::TX_BYTES);
 #pragma unroll
     for (int pn = 0; pn < C::NPANEL; ++pn)
       tma_load_4d(st + pn * C::PANEL_BYTES, &tmX, bar, 64 * pn, h, blk * QROWS, b,
                   l2_policy_evict_first());
+    if (ROPE) {
+      // coarse rows 128 blk + 16 r1 into slot k % NCSLOT.  The slot last held block
+      // k - NSTAGE - 1; issue(k) runs after the CTA-wide barrier of block k - NSTAGE, which
+      // every thread reaches only after finishing block k - NSTAGE - 1.
+      const uint32_t slot = base_u32 + C::OFF_COARSE + (k % C::NCSLOT) * NCOARSE * C::TROW;
+#pragma unroll
+      for (int r1 = 0; r1 < NCOARSE; ++r1)
+#pragma unroll
+        for (int sg = 0; sg < C::TPR; ++sg)
+          bulk_load(slot + r1 * C::TROW + sg * C::SEG_STRIDE,
+                    p.rope_cs + static_cast<size_t>(blk * QROWS + 16 * r1) * D + sg * VPT, C::SEG_BYTES,
+                    bar, l2_policy_evict_last());
+    }
     n_issued = k + 1;
   };
   const int my_blocks = (nblocks - static_cast<int>(blockIdx.x) + static_cast<int>(gridDim.x) - 1) /
@@ -125,7 +193,7 @@ __global__ void __launch_bounds__(QCfg<D>::THREADS, QCfg<D>::CTAS_PER_SM)
       uint32_t w[4];
       asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
                    : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]) : "r"(addr));
-      if (ROTATE) {
+      if (ROTATE && !ROPE) {
         const uint4 m = reinterpret_cast<const uint4*>(sign_mask)[idx / 8];
         w[0] ^= m.x; w[1] ^= m.y; w[2] ^= m.z; w[3] ^= m.w;
       }
@@ -140,6 +208,28 @@ __global__ void __launch_bounds__(QCfg<D>::THREADS, QCfg<D>::CTAS_PER_SM)
     // flight while this one is transformed.
     if (__syncthreads_or(!ok)) break;
     if (threadIdx.x == 0 && k + NSTAGE < my_blocks) issue(k + NSTAGE);
+
+    if (ROPE) {
+      const uint32_t crow = base_u32 + C::OFF_COARSE + (k % C::NCSLOT) * NCOARSE * C::TROW +
+                            (r >> 4) * C::TROW + half * C::SEG_STRIDE;
+      const uint32_t frow = base_u32 + C::OFF_FINE + (r & 15) * C::TROW + half * C::SEG_STRIDE;
+#pragma unroll
+      for (int j = 0; j < VPT / 2; j += 2) {               // two pairs per 16-byte read
+        const float4 a = lds128(crow + 8 * j), f = lds128(frow + 8 * j);
+        rotary_pair(v[2 * j], v[2 * j + 1], a.x, a.y, f.x, f.y);
+        rotary_pair(v[2 * j + 2], v[2 * j + 3], a.z, a.w, f.z, f.w);
+      }
+      if (ROTATE) {
+#pragma unroll
+        for (int e = 0; e < VPT; e += 4) {
+          const uint4 m = reinterpret_cast<const uint4*>(sign_mask)[(half * VPT + e) / 4];
+          v[e] = __uint_as_float(__float_as_uint(v[e]) ^ m.x);
+          v[e + 1] = __uint_as_float(__float_as_uint(v[e + 1]) ^ m.y);
+          v[e + 2] = __uint_as_float(__float_as_uint(v[e + 2]) ^ m.z);
+          v[e + 3] = __uint_as_float(__float_as_uint(v[e + 3]) ^ m.w);
+        }
+      }
+    }
 
     if (ROTATE) {
       // butterflies over the index bits held by this thread: bit 0 pairs the two halves of a
@@ -225,11 +315,26 @@ __global__ void __launch_bounds__(QCfg<D>::THREADS, QCfg<D>::CTAS_PER_SM)
   }
 }
 
+template <int D, bool ROTATE, bool ROPE>
+cudaError_t launch_variant(const CUtensorMap& tx, const QuantParams& p, int sm_count, cudaStream_t stream) {
+  using C = QCfg<D, ROPE>;
+  const long long nblocks = static_cast<long long>(p.nblk) * p.H * p.B;
+  const long long cap = static_cast<long long>(sm_count) * C::CTAS_PER_SM;
+  const unsigned grid = static_cast<unsigned>(nblocks < cap ? nblocks : cap);
+  hadamard_quant_kernel<D, ROTATE, ROPE><<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(tx, p);
+  return cudaGetLastError();
+}
+
+template <int D, bool ROTATE, bool ROPE>
+cudaError_t set_smem() {
+  return cudaFuncSetAttribute(hadamard_quant_kernel<D, ROTATE, ROPE>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, QCfg<D, ROPE>::SMEM_BYTES);
+}
+
 }  // namespace
 
 template <int D>
 cudaError_t launch_hadamard_quant(const CUtensorMap& tx, const QuantParams& p, cudaStream_t stream) {
-  using C = QCfg<D>;
   static std::atomic<unsigned long long> configured{0};
   static int sm_count[64] = {0};
   int dev = 0;
@@ -237,24 +342,21 @@ cudaError_t launch_hadamard_quant(const CUtensorMap& tx, const QuantParams& p, c
   if (e != cudaSuccess) return e;
   const unsigned long long bit = 1ull << (dev & 63);
   if ((configured.load() & bit) == 0) {
-    e = cudaFuncSetAttribute(hadamard_quant_kernel<D, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(hadamard_quant_kernel<D, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
-    if (e != cudaSuccess) return e;
+    if ((e = set_smem<D, true, false>()) != cudaSuccess) return e;
+    if ((e = set_smem<D, false, false>()) != cudaSuccess) return e;
+    if ((e = set_smem<D, true, true>()) != cudaSuccess) return e;
+    if ((e = set_smem<D, false, true>()) != cudaSuccess) return e;
     int n = 0;
     e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
     sm_count[dev & 63] = n;
     configured.fetch_or(bit);
   }
-  const long long nblocks = static_cast<long long>(p.nblk) * p.H * p.B;
-  const long long cap = static_cast<long long>(sm_count[dev & 63]) * C::CTAS_PER_SM;
-  const unsigned grid = static_cast<unsigned>(nblocks < cap ? nblocks : cap);
-  if (p.signs != nullptr)
-    hadamard_quant_kernel<D, true><<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(tx, p);
-  else
-    hadamard_quant_kernel<D, false><<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(tx, p);
-  return cudaGetLastError();
+  const int sms = sm_count[dev & 63];
+  const bool rot = p.signs != nullptr, rope = p.rope_cs != nullptr;
+  if (rope)
+    return rot ? launch_variant<D, true, true>(tx, p, sms, stream) : launch_variant<D, false, true>(tx, p, sms, stream);
+  return rot ? launch_variant<D, true, false>(tx, p, sms, stream) : launch_variant<D, false, false>(tx, p, sms, stream);
 }
 
 template cudaError_t launch_hadamard_quant<64>(const CUtensorMap&, const QuantParams&, cudaStream_t);

@@ -37,6 +37,7 @@ struct QuantParams {
   void* out;            // [B, S, H, D] E4M3
   float* scale;         // [B, H, nblk]
   const float* signs;   // [D] or nullptr
+  const float* rope_cs; // [>= 128 * nblk, D/2, 2] rotary table (cos, sin of p * theta_i) or nullptr
   long long spin_limit; // cycles a bounded wait may spin
   int* err_word;        // device error word
   int* err_info;
@@ -45,5 +46,8 @@ struct QuantParams {
 // x is read through `tx`, the same [B, S, H, D] bf16 tensor map the attention kernel uses.
 template <int D>
 cudaError_t launch_hadamard_quant(const CUtensorMap& tx, const QuantParams& p, cudaStream_t stream);
+
+// cs[p, i] = (cos, sin)(p * base^(-2i/D)) for p < n_pos, i < D/2, in fp64 rounded to fp32.
+cudaError_t launch_rope_table(float* cs, int n_pos, int D, double base, cudaStream_t stream);
 
 }  // namespace ea46

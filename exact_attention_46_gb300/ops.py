@@ -9,7 +9,8 @@ import torch
 
 from . import _lib
 
-__all__ = ["attn_fwd", "attn_fwd_fp8", "hadamard_rotate_quant_fp8", "check",
+__all__ = ["attn_fwd", "attn_fwd_fp8", "hadamard_rotate_quant_fp8", "rope_cos_sin_table",
+           "rope_hadamard_rotate_quant_fp8", "check",
            "set_spin_limit", "selftest_bounded_wait", "block_count", "ATTN_BF16", "ATTN_FP8_E4M3"]
 
 ATTN_BF16 = 0
@@ -82,6 +83,30 @@ def hadamard_rotate_quant_fp8(x, signs=None, out=None, scale=None, stream=None):
         scale = torch.empty((B, H, block_count(S)), dtype=torch.float32, device=x.device)
     _lib.call("hadamard_rotate_quant_fp8", _ptr(x), _ptr(out), _ptr(scale), _ptr(signs), B, H, S,
               D, _stream(stream))
+    return out, scale
+
+
+def rope_cos_sin_table(n_pos, D, base=10000.0, device="cuda", out=None, stream=None):
+    """Rotary table fp32 [n_pos, D/2, 2]: (cos, sin) of p * base^(-2i/D), built on the GPU."""
+    if out is None:
+        out = torch.empty((n_pos, D // 2, 2), dtype=torch.float32, device=device)
+    _lib.call("rope_cos_sin_table", _ptr(out), int(n_pos), int(D), float(base), _stream(stream))
+    return out
+
+
+def rope_hadamard_rotate_quant_fp8(x, rope_cs, signs=None, out=None, scale=None, stream=None):
+    """Rotary embedding, then ``hadamard_rotate_quant_fp8``, in one kernel.
+
+    ``rope_cs``: the table from ``rope_cos_sin_table`` with at least 128 * ceil(S/128) rows.
+    """
+    _check4(x)
+    B, S, H, D = x.shape
+    if out is None:
+        out = torch.empty((B, S, H, D), dtype=torch.uint8, device=x.device)
+    if scale is None:
+        scale = torch.empty((B, H, block_count(S)), dtype=torch.float32, device=x.device)
+    _lib.call("rope_hadamard_rotate_quant_fp8", _ptr(x), _ptr(rope_cs), int(rope_cs.shape[0]), _ptr(out),
+              _ptr(scale), _ptr(signs), B, H, S, D, _stream(stream))
     return out, scale
 
 

@@ -110,6 +110,41 @@ int attn_fwd_fp8(const void* q8, const void* k8, const void* v8,
 int hadamard_rotate_quant_fp8(const void* x, void* out, float* scale, const float* signs,
                               int B, int H, int S, int D, void* stream);
 
+/*
+ * rope_cos_sin_table -- the rotary-embedding table.
+ *   [HADA] "Niedrige FP8-Präzision und incoherent processing" names rotary
+ *   embedding as the bandwidth-bound op to fuse the rotation with but does
+ *   not define it; the reading is RoFormer's (Su et al. 2021, section 3.2):
+ *   pair (x[2i], x[2i+1]) of the row at position p turns by p * theta_i,
+ *   theta_i = base^(-2i/D).
+ *   cs     : device output, [n_pos, D/2, 2] fp32, cs[p][i] = (cos, sin) of
+ *            p * theta_i, evaluated in fp64 and rounded to nearest fp32;
+ *            8-byte aligned.
+ *   n_pos  : positions 0 .. n_pos-1, 1 <= n_pos <= 2^26.
+ *   D      : even, 2 .. 4096.  base: finite, > 0 (10000 in RoFormer).
+ *   Enqueued on `stream`; the caller owns cs and normally builds it once.
+ */
+int rope_cos_sin_table(float* cs, int n_pos, int D, double base, void* stream);
+
+/*
+ * rope_hadamard_rotate_quant_fp8 -- rotary embedding fused into the
+ * rotation + quantiser (the fusion [HADA] says makes the rotation free).
+ *   Each row x of token s (position p = s) becomes
+ *   x' = (rope_p(x) * signs) H_D / sqrt(D), in fp32 with no rounding in
+ *   between, then is quantised exactly as by hadamard_rotate_quant_fp8
+ *   (signs may be NULL: RoPE + quantiser only).  Apply to Q and K, not V.
+ *   rope_cs: the table written by rope_cos_sin_table for this D and base,
+ *            16-byte aligned, with n_pos >= 128 * ceil(S/128) rows.  The
+ *            kernel reads rows 0..15 and the rows at multiples of 16 and
+ *            rebuilds the others with the angle-addition identity, so the
+ *            table must be a rotary table of that form.
+ *   Other arguments, layouts and errors as hadamard_rotate_quant_fp8;
+ *   ATTN_ERR_INVALID_ARG also for a null or short table.
+ */
+int rope_hadamard_rotate_quant_fp8(const void* x, const float* rope_cs, int n_pos, void* out,
+                                   float* scale, const float* signs, int B, int H, int S, int D,
+                                   void* stream);
+
 /* Message for the last non-OK status returned on the calling host thread ("" if none). */
 const char* attn_get_last_error(void);
 

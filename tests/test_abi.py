@@ -40,7 +40,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_version(lib):
-    assert lib.attn_version() == 100
+    assert lib.attn_version() == 101
 
 
 FAKE = 1 << 20   # 16-byte aligned non-null fake device addresses: never dereferenced
@@ -71,3 +71,20 @@ def test_quantiser_and_fp8_reject_bad_arguments(lib):
     assert lib.attn_fwd_fp8(FAKE, FAKE * 2, FAKE * 3, None, FAKE * 5, FAKE * 6, FAKE * 7, None,
                             1, 1, 128, 128, 0, 0.0, None) == 1
     assert lib.attn_selftest_bounded_wait(0, None) == 1
+
+
+def test_rotary_entry_points_reject_bad_arguments(lib):
+    f = lib.rope_hadamard_rotate_quant_fp8
+    assert f(FAKE, None, 256, FAKE * 8, FAKE * 16, None, 1, 1, 128, 128, None) == 1      # no table
+    assert f(FAKE, FAKE * 32, 127, FAKE * 8, FAKE * 16, None, 1, 1, 100, 128, None) == 1  # short table
+    assert f(FAKE, FAKE * 32, 255, FAKE * 8, FAKE * 16, None, 1, 1, 129, 128, None) == 1  # needs 256 rows
+    assert f(FAKE, FAKE * 32 + 8, 256, FAKE * 8, FAKE * 16, None, 1, 1, 128, 128, None) == 1  # misaligned
+    assert f(FAKE, FAKE * 32, 256, FAKE * 8, FAKE * 16, None, 1, 1, 128, 96, None) == 2   # D = 96
+    assert f(FAKE, FAKE * 8, 256, FAKE * 8, FAKE * 16, None, 1, 1, 128, 128, None) == 1   # out on table
+    t = lib.rope_cos_sin_table
+    assert t(None, 16, 128, 10000.0, None) == 1
+    assert t(FAKE, 0, 128, 10000.0, None) == 1
+    assert t(FAKE, 16, 63, 10000.0, None) == 1
+    assert t(FAKE, 16, 128, 0.0, None) == 1
+    assert t(FAKE, 16, 128, float("inf"), None) == 1
+    assert t(FAKE + 4, 16, 128, 10000.0, None) == 1

@@ -20,6 +20,7 @@ import torch
 from exact_attention_46_gb300 import ops, synth
 from oracle import attention as oracle_attention
 from oracle import e4m3, fp8_path, quantise
+from tests import helpers
 from tests.helpers import inputs, sample_rows, stats, to64
 
 pytestmark = pytest.mark.gpu
@@ -33,20 +34,7 @@ def signs_for(case, D):
 
 
 def check_codes(gpu_codes, ref):
-    diff = gpu_codes != ref["codes"]
-    n_diff = int(diff.sum())
-    if n_diff:
-        pre = ref["pre"][diff]
-        a = e4m3.decode(gpu_codes[diff])
-        b = e4m3.decode(ref["codes"][diff])
-        mid = (a + b) / 2
-        assert np.all(np.abs(pre - mid) <= TIE_RTOL * np.abs(pre) + 1e-12), "non-tie code mismatch"
-        # neighbours on the grid: nothing representable strictly between them
-        lo, hi = np.minimum(a, b), np.maximum(a, b)
-        assert np.all(e4m3.round_e4m3((lo + mid) / 2) == lo) and np.all(e4m3.round_e4m3((hi + mid) / 2) == hi)
-    assert n_diff <= max(3, 1e-5 * gpu_codes.size), n_diff
-    assert not np.any((gpu_codes & 0x7F) == 0x7F), "NaN code produced"
-    return n_diff
+    return helpers.check_codes(gpu_codes, ref, TIE_RTOL, 1e-12, 1e-5)
 
 
 @pytest.mark.parametrize("D", [64, 128, 256])
