@@ -253,13 +253,14 @@ int run_quant(const void* x, const float* rope_cs, int n_pos, void* out, float* 
   int* err = nullptr;
   int rc = err_words(&err);
   if (rc != ATTN_OK) return rc;
-  CUtensorMap tx;
+  CUtensorMap tx, tout;
   if ((rc = make_qkv_map(&tx, x, B, S, H, D, false)) != ATTN_OK) return rc;
+  if ((rc = make_qkv_map(&tout, out, B, S, H, D, true)) != ATTN_OK) return rc;
   QuantParams p{B, H, S, nblk, out, scale, signs, rope_cs, spin_limit(), err, err + 1};
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  cudaError_t e = D == 64    ? launch_hadamard_quant<64>(tx, p, st)
-                  : D == 128 ? launch_hadamard_quant<128>(tx, p, st)
-                             : launch_hadamard_quant<256>(tx, p, st);
+  cudaError_t e = D == 64    ? launch_hadamard_quant<64>(tx, tout, p, st)
+                  : D == 128 ? launch_hadamard_quant<128>(tx, tout, p, st)
+                             : launch_hadamard_quant<256>(tx, tout, p, st);
   if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "quantiser launch failed: %s", cudaGetErrorString(e));
   return ok();
 }

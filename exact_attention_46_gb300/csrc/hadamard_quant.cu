@@ -13,12 +13,14 @@
 // on the FP32 pipes: no tensor cores.  Persistent CTAs stream blocks of 128 rows through a
 // ring of shared-memory stages filled by TMA (the same 128-byte-swizzled box the attention
 // kernel uses), so the loads of the next blocks are in flight while a block is transformed.
-// A thread owns one row (two adjacent lanes share a row at D = 256), so every butterfly
-// stage runs in registers without shuffles (one shuffle stage at D = 256); the 32 lanes of
-// a warp read the same 16-byte chunk of 32 rows, which the swizzle makes conflict-free.  The
-// random signs are applied as XOR masks on the packed bf16 words, read from a small
-// shared-memory table by broadcast.  Rows beyond S arrive zero-filled and are never stored.
-// Codes go straight to global memory, 16 bytes at a time.
+// A thread owns a row (lanes l and l + 16 share one at D = 256), so the butterfly stages run
+// in registers (plus one lane-shuffle stage at D = 256); the 8 lanes of a 128-bit read phase
+// hold 8 rows and read the same 16-byte chunk of each, which the swizzle makes
+// conflict-free.  The random signs are applied as XOR masks on the packed bf16 words, read
+// from a small shared-memory table by broadcast.  Rows beyond S arrive zero-filled.  The
+// codes go back into the consumed stage in the swizzled layout of the E4M3 output map and
+// leave with one tensor store per panel (rows beyond S clipped), so L2 sees whole lines; the
+// stage is refilled once the store has read it.
 //
 // Rotary embedding fused in front (hada.io FA3 summary, same section: the transform is
 // bandwidth-bound and costs nothing extra when fused with a preceding bandwidth-bound op such
@@ -45,8 +47,9 @@ constexpr int NFINE = 16;             // rotary rows r0 = 0..15, resident
 
 template <int D, bool ROPE>
 struct QCfg {
-  static constexpr int TPR = D > 128 ? D / 128 : 1;                        // threads per row
-  static constexpr int VPT = D / TPR;                                      // values per thread
+  static constexpr int VPT = D < 128 ? D : 128;                            // values per thread
+  static constexpr int TPR = D / VPT;                                      // threads per row
+  static constexpr int RPW = 32 / TPR;                                     // rows per warp
   static constexpr int THREADS = QROWS * TPR;
   static constexpr int ROW_BYTES = D * 2;                                  // bf16 row
   static constexpr int PANEL_BYTES = 128 * 128;                            // 128 rows x 128 B
@@ -55,22 +58,29 @@ struct QCfg {
   static constexpr int CTAS_PER_SM = D == 64 ? 4 : (D == 128 ? (ROPE ? 2 : 3) : 1);
   static constexpr int NSTAGE = D == 256 && !ROPE ? 3 : 2;
   static constexpr int NWARPS = THREADS / 32;
-  // rotary table rows in shared memory: each thread's VPT/2 pairs (8 bytes each) form one
-  // segment, padded by 16 bytes so that the rows of one warp's reads fall in distinct banks
+  // rotary table rows in shared memory: (cos, sin) pairs, 8 bytes each, a thread's VPT/2 pairs
+  // at part * SEG_BYTES; rows padded by 16 bytes so that the 8 rows of one 128-bit read phase
+  // fall in distinct banks
   static constexpr int SEG_BYTES = 4 * VPT;
-  static constexpr int SEG_STRIDE = SEG_BYTES + 16;
-  static constexpr int TROW = TPR * SEG_STRIDE;
+  static constexpr int TROW = 4 * D + 16;
   static constexpr int NCSLOT = NSTAGE + 1;                                // coarse-row slots
   static constexpr int OFF_COARSE = NSTAGE * STAGE_BYTES;
   static constexpr int OFF_FINE = OFF_COARSE + (ROPE ? NCSLOT * NCOARSE * TROW : 0);
   static constexpr int OFF_SIGN = OFF_FINE + (ROPE ? NFINE * TROW : 0);
-  // signs: packed-bf16 XOR masks [D/2] without RoPE, fp32 sign-bit masks [D] with it
-  static constexpr int SIGN_BYTES = ROPE ? 4 * D : 2 * D;
+  // packed-bf16 sign XOR masks [D/2] without RoPE; per-pair masks sign(2i) != sign(2i+1) [D/2]
+  // with it (the even element's sign is folded into the resident rotary rows)
+  static constexpr int SIGN_BYTES = 2 * D;
   static constexpr int OFF_BAR = OFF_SIGN + SIGN_BYTES;
   static constexpr int OFF_WMAX = OFF_BAR + 8 * NSTAGE;
   static constexpr int OFF_ABORT = OFF_WMAX + 2 * NWARPS * 4;
   static constexpr int SMEM_BYTES = 1024 + OFF_ABORT + 16;
-  static constexpr uint32_t TX_BYTES = STAGE_BYTES + (ROPE ? NCOARSE * TPR * SEG_BYTES : 0);
+  static constexpr uint32_t TX_BYTES = STAGE_BYTES + (ROPE ? NCOARSE * 4 * D : 0);
+  // E4M3 codes of a block, staged in the consumed input stage for one tensor store per
+  // 128-byte panel (64-byte rows, 64-byte swizzle at D = 64)
+  static constexpr int CODE_PANEL = D < 128 ? D : 128;                     // bytes per code row
+  static constexpr int NCPANEL = D / CODE_PANEL;
+  static_assert(TPR >= 1 && TPR <= 2 && D % VPT == 0, "row split");
+  static_assert(QROWS * D <= STAGE_BYTES, "codes fit the stage");
   static_assert(SMEM_BYTES * CTAS_PER_SM + 1024 * CTAS_PER_SM <= 228 * 1024, "shared memory budget");
   static_assert(OFF_COARSE % 16 == 0 && OFF_FINE % 16 == 0 && OFF_SIGN % 16 == 0 && OFF_BAR % 8 == 0,
                 "alignment");
@@ -95,7 +105,8 @@ __device__ __forceinline__ void rotary_pair(float& v0, float& v1, float ac, floa
 
 template <int D, bool ROTATE, bool ROPE>
 __global__ void __launch_bounds__(QCfg<D, ROPE>::THREADS, QCfg<D, ROPE>::CTAS_PER_SM)
-    hadamard_quant_kernel(const __grid_constant__ CUtensorMap tmX, const QuantParams p) {
+    hadamard_quant_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmOut,
+                          const QuantParams p) {
   using C = QCfg<D, ROPE>;
   constexpr int VPT = C::VPT;
   constexpr int NSTAGE = C::NSTAGE;
@@ -111,9 +122,10 @@ __global__ void __launch_bounds__(QCfg<D, ROPE>::THREADS, QCfg<D, ROPE>::CTAS_PE
   volatile int* abort_flag = reinterpret_cast<volatile int*>(base + C::OFF_ABORT);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // row and the part of it this thread owns (TPR = 2: adjacent lanes share a row)
-  const int r = static_cast<int>(threadIdx.x) / C::TPR;
-  const int half = static_cast<int>(threadIdx.x) % C::TPR;
+  // row and the part of it this thread owns: a warp holds RPW rows, lanes l, l + RPW, ... share
+  // a row, so the 8 lanes of one 128-bit shared-memory read phase hold 8 different rows
+  const int r = warp * C::RPW + lane % C::RPW;
+  const int part = lane / C::RPW;
   const int nblocks = p.nblk * p.H * p.B;
 
   if (threadIdx.x == 0) {
@@ -121,6 +133,7 @@ __global__ void __launch_bounds__(QCfg<D, ROPE>::THREADS, QCfg<D, ROPE>::CTAS_PE
     *abort_flag = 0;
     fence_barrier_init();
     prefetch_tmap(&tmX);
+    prefetch_tmap(&tmOut);
   }
   if (!ROPE) {
     // bit 15 flips the even element of a packed bf16 pair, bit 31 the odd one
@@ -129,15 +142,16 @@ __global__ void __launch_bounds__(QCfg<D, ROPE>::THREADS, QCfg<D, ROPE>::CTAS_PE
                                (p.signs[2 * w + 1] < 0.f ? 0x80000000u : 0u))
                             : 0u;
   } else {
-    // signs act after the rotary step, on fp32 values: one sign-bit mask per element
-    for (int w = static_cast<int>(threadIdx.x); w < D; w += C::THREADS)
-      sign_mask[w] = ROTATE && p.signs[w] < 0.f ? 0x80000000u : 0u;
-    // resident rotary rows 0..15, in the padded per-thread segment layout
+    // The rotary step comes before the signs: the even element's sign is folded into the
+    // resident rows below, the odd element then needs sign(2i) * sign(2i+1).
+    for (int w = static_cast<int>(threadIdx.x); w < D / 2; w += C::THREADS)
+      sign_mask[w] = ROTATE && ((p.signs[2 * w] < 0.f) != (p.signs[2 * w + 1] < 0.f)) ? 0x80000000u : 0u;
+    // resident rotary rows 0..15, times the even element's sign
     for (int idx = static_cast<int>(threadIdx.x); idx < NFINE * (D / 2); idx += C::THREADS) {
       const int f = idx / (D / 2), i = idx % (D / 2);
-      const float2 cs = reinterpret_cast<const float2*>(p.rope_cs)[idx];
-      *reinterpret_cast<float2*>(base + C::OFF_FINE + f * C::TROW + (i / (VPT / 2)) * C::SEG_STRIDE +
-                                 8 * (i % (VPT / 2))) = cs;
+      float2 cs = reinterpret_cast<const float2*>(p.rope_cs)[idx];
+      if (ROTATE && p.signs[2 * i] < 0.f) cs = make_float2(-cs.x, -cs.y);
+      *reinterpret_cast<float2*>(base + C::OFF_FINE + f * C::TROW + 8 * i) = cs;
     }
   }
   __syncthreads();
@@ -161,11 +175,8 @@ __global__ void __launch_bounds__(QCfg<D, ROPE>::THREADS, QCfg<D, ROPE>::CTAS_PE
       const uint32_t slot = base_u32 + C::OFF_COARSE + (k % C::NCSLOT) * NCOARSE * C::TROW;
 #pragma unroll
       for (int r1 = 0; r1 < NCOARSE; ++r1)
-#pragma unroll
-        for (int sg = 0; sg < C::TPR; ++sg)
-          bulk_load(slot + r1 * C::TROW + sg * C::SEG_STRIDE,
-                    p.rope_cs + static_cast<size_t>(blk * QROWS + 16 * r1) * D + sg * VPT, C::SEG_BYTES,
-                    bar, l2_policy_evict_last());
+        bulk_load(slot + r1 * C::TROW, p.rope_cs + static_cast<size_t>(blk * QROWS + 16 * r1) * D, 4 * D, bar,
+                  l2_policy_evict_last());
     }
     n_issued = k + 1;
   };
@@ -187,7 +198,7 @@ __global__ void __launch_bounds__(QCfg<D, ROPE>::THREADS, QCfg<D, ROPE>::CTAS_PE
     float v[VPT];
 #pragma unroll
     for (int c = 0; c < NW; ++c) {
-      const int idx = half * VPT + 8 * c;                  // first element of the chunk
+      const int idx = part * VPT + 8 * c;                  // first element of the chunk
       const int pn = idx / 64, cc = (idx % 64) / 8;        // panel, 16-byte chunk in the row
       const uint32_t addr = st + pn * C::PANEL_BYTES + r * 128 + ((cc ^ (r & 7)) << 4);
       uint32_t w[4];
@@ -204,15 +215,13 @@ __global__ void __launch_bounds__(QCfg<D, ROPE>::THREADS, QCfg<D, ROPE>::CTAS_PE
       }
     }
 
-    // The values are in registers: refill the stage now, so the next blocks' loads stay in
-    // flight while this one is transformed.
+    // Every thread has its values in registers; the stage now takes this block's codes.
     if (__syncthreads_or(!ok)) break;
-    if (threadIdx.x == 0 && k + NSTAGE < my_blocks) issue(k + NSTAGE);
 
     if (ROPE) {
       const uint32_t crow = base_u32 + C::OFF_COARSE + (k % C::NCSLOT) * NCOARSE * C::TROW +
-                            (r >> 4) * C::TROW + half * C::SEG_STRIDE;
-      const uint32_t frow = base_u32 + C::OFF_FINE + (r & 15) * C::TROW + half * C::SEG_STRIDE;
+                            (r >> 4) * C::TROW + part * C::SEG_BYTES;
+      const uint32_t frow = base_u32 + C::OFF_FINE + (r & 15) * C::TROW + part * C::SEG_BYTES;
 #pragma unroll
       for (int j = 0; j < VPT / 2; j += 2) {               // two pairs per 16-byte read
         const float4 a = lds128(crow + 8 * j), f = lds128(frow + 8 * j);
@@ -221,12 +230,12 @@ __global__ void __launch_bounds__(QCfg<D, ROPE>::THREADS, QCfg<D, ROPE>::CTAS_PE
       }
       if (ROTATE) {
 #pragma unroll
-        for (int e = 0; e < VPT; e += 4) {
-          const uint4 m = reinterpret_cast<const uint4*>(sign_mask)[(half * VPT + e) / 4];
-          v[e] = __uint_as_float(__float_as_uint(v[e]) ^ m.x);
-          v[e + 1] = __uint_as_float(__float_as_uint(v[e + 1]) ^ m.y);
-          v[e + 2] = __uint_as_float(__float_as_uint(v[e + 2]) ^ m.z);
-          v[e + 3] = __uint_as_float(__float_as_uint(v[e + 3]) ^ m.w);
+        for (int j = 0; j < VPT / 2; j += 4) {
+          const uint4 m = reinterpret_cast<const uint4*>(sign_mask)[(part * VPT / 2 + j) / 4];
+          v[2 * j + 1] = __uint_as_float(__float_as_uint(v[2 * j + 1]) ^ m.x);
+          v[2 * j + 3] = __uint_as_float(__float_as_uint(v[2 * j + 3]) ^ m.y);
+          v[2 * j + 5] = __uint_as_float(__float_as_uint(v[2 * j + 5]) ^ m.z);
+          v[2 * j + 7] = __uint_as_float(__float_as_uint(v[2 * j + 7]) ^ m.w);
         }
       }
     }
@@ -249,13 +258,15 @@ __global__ void __launch_bounds__(QCfg<D, ROPE>::THREADS, QCfg<D, ROPE>::CTAS_PE
             f2_unpack(f2_add(a2, b2), v[e], v[e + 1]);
             f2_unpack(f2_sub(a2, b2), v[e + hs], v[e + hs + 1]);
           }
-      if (C::TPR == 2) {
-        // the top index bit lives in the adjacent lane: lower half a+b, upper half a-b
-        const float sgn = half ? -1.f : 1.f;
+      // the index bits above VPT live in the lanes RPW, 2 RPW apart: the lower part keeps
+      // a + b, the upper part a - b
+#pragma unroll
+      for (int pb = 1; pb < C::TPR; pb <<= 1) {
+        const float sgn = (part & pb) ? -1.f : 1.f;
 #pragma unroll
         for (int e = 0; e < VPT; e += 2) {
-          const float o0 = __shfl_xor_sync(0xffffffffu, v[e], 1);
-          const float o1 = __shfl_xor_sync(0xffffffffu, v[e + 1], 1);
+          const float o0 = __shfl_xor_sync(0xffffffffu, v[e], pb * C::RPW);
+          const float o1 = __shfl_xor_sync(0xffffffffu, v[e + 1], pb * C::RPW);
           const uint64_t r2 = f2_fma(f2_pack(v[e], v[e + 1]), f2_pack(sgn, sgn), f2_pack(o0, o1));
           f2_unpack(r2, v[e], v[e + 1]);
         }
@@ -279,11 +290,10 @@ __global__ void __launch_bounds__(QCfg<D, ROPE>::THREADS, QCfg<D, ROPE>::CTAS_PE
       const float norm = ROTATE ? rsqrtf(static_cast<float>(D)) : 1.f;
       p.scale[static_cast<size_t>(hb) * p.nblk + blk] = amax > 0.f ? (amax * norm) / 448.f : 1.f;
     }
-    const int tok = blk * QROWS + r;
-    if (tok < p.S) {
-      uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(p.out) +
-                                            ((static_cast<size_t>(b) * p.S + tok) * p.H + h) * D +
-                                            half * VPT);
+    // Codes into the stage in the output map's swizzled layout, then one tensor store per
+    // panel: whole 128-byte lines reach L2 instead of 16-byte pieces of 32-byte sectors, and
+    // rows beyond S are clipped by the store.
+    {
       const uint64_t inv2 = f2_pack(inv, inv);
 #pragma unroll
       for (int c = 0; c < VPT / 16; ++c) {
@@ -296,10 +306,28 @@ __global__ void __launch_bounds__(QCfg<D, ROPE>::THREADS, QCfg<D, ROPE>::CTAS_PE
             f2_unpack(f2_mul(f2_pack(v[16 * c + 4 * q + e], v[16 * c + 4 * q + e + 1]), inv2), y[e], y[e + 1]);
           wq[q] = pack_e4m3x4(y[0], y[1], y[2], y[3]);
         }
-        dst[c] = make_uint4(wq[0], wq[1], wq[2], wq[3]);
+        const int idx = part * VPT + 16 * c;                          // byte in the code row
+        const int pn = idx / C::CODE_PANEL, cc = (idx % C::CODE_PANEL) / 16;
+        const int sw = C::CODE_PANEL == 128 ? (r & 7) : ((r >> 1) & 3);
+        const uint32_t addr = st + pn * (QROWS * C::CODE_PANEL) + r * C::CODE_PANEL + ((cc ^ sw) << 4);
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(wq[0]), "r"(wq[1]),
+                     "r"(wq[2]), "r"(wq[3])
+                     : "memory");
       }
     }
+    fence_proxy_async_smem();
+    __syncthreads();
+    if (threadIdx.x == 0) {
+#pragma unroll
+      for (int pn = 0; pn < C::NCPANEL; ++pn)
+        tma_store_4d(&tmOut, st + pn * (QROWS * C::CODE_PANEL), pn * C::CODE_PANEL, h, blk * QROWS, b);
+      bulk_commit_group();
+      // the stage is free once the store has read it: refill it for block k + NSTAGE
+      bulk_wait_read_all();
+      if (k + NSTAGE < my_blocks) issue(k + NSTAGE);
+    }
   }
+  if (threadIdx.x == 0) bulk_wait_all();
 
   // On an abort, copies still in flight must land before the CTA exits.
   if (threadIdx.x == 0 && *abort_flag) {
@@ -316,12 +344,13 @@ __global__ void __launch_bounds__(QCfg<D, ROPE>::THREADS, QCfg<D, ROPE>::CTAS_PE
 }
 
 template <int D, bool ROTATE, bool ROPE>
-cudaError_t launch_variant(const CUtensorMap& tx, const QuantParams& p, int sm_count, cudaStream_t stream) {
+cudaError_t launch_variant(const CUtensorMap& tx, const CUtensorMap& tout, const QuantParams& p, int sm_count,
+                           cudaStream_t stream) {
   using C = QCfg<D, ROPE>;
   const long long nblocks = static_cast<long long>(p.nblk) * p.H * p.B;
   const long long cap = static_cast<long long>(sm_count) * C::CTAS_PER_SM;
   const unsigned grid = static_cast<unsigned>(nblocks < cap ? nblocks : cap);
-  hadamard_quant_kernel<D, ROTATE, ROPE><<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(tx, p);
+  hadamard_quant_kernel<D, ROTATE, ROPE><<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(tx, tout, p);
   return cudaGetLastError();
 }
 
@@ -334,7 +363,8 @@ cudaError_t set_smem() {
 }  // namespace
 
 template <int D>
-cudaError_t launch_hadamard_quant(const CUtensorMap& tx, const QuantParams& p, cudaStream_t stream) {
+cudaError_t launch_hadamard_quant(const CUtensorMap& tx, const CUtensorMap& tout, const QuantParams& p,
+                                  cudaStream_t stream) {
   static std::atomic<unsigned long long> configured{0};
   static int sm_count[64] = {0};
   int dev = 0;
@@ -355,12 +385,17 @@ cudaError_t launch_hadamard_quant(const CUtensorMap& tx, const QuantParams& p, c
   const int sms = sm_count[dev & 63];
   const bool rot = p.signs != nullptr, rope = p.rope_cs != nullptr;
   if (rope)
-    return rot ? launch_variant<D, true, true>(tx, p, sms, stream) : launch_variant<D, false, true>(tx, p, sms, stream);
-  return rot ? launch_variant<D, true, false>(tx, p, sms, stream) : launch_variant<D, false, false>(tx, p, sms, stream);
+    return rot ? launch_variant<D, true, true>(tx, tout, p, sms, stream)
+               : launch_variant<D, false, true>(tx, tout, p, sms, stream);
+  return rot ? launch_variant<D, true, false>(tx, tout, p, sms, stream)
+             : launch_variant<D, false, false>(tx, tout, p, sms, stream);
 }
 
-template cudaError_t launch_hadamard_quant<64>(const CUtensorMap&, const QuantParams&, cudaStream_t);
-template cudaError_t launch_hadamard_quant<128>(const CUtensorMap&, const QuantParams&, cudaStream_t);
-template cudaError_t launch_hadamard_quant<256>(const CUtensorMap&, const QuantParams&, cudaStream_t);
+template cudaError_t launch_hadamard_quant<64>(const CUtensorMap&, const CUtensorMap&, const QuantParams&,
+                                               cudaStream_t);
+template cudaError_t launch_hadamard_quant<128>(const CUtensorMap&, const CUtensorMap&, const QuantParams&,
+                                                cudaStream_t);
+template cudaError_t launch_hadamard_quant<256>(const CUtensorMap&, const CUtensorMap&, const QuantParams&,
+                                                cudaStream_t);
 
 }  // namespace ea46

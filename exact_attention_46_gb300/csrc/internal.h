@@ -43,9 +43,11 @@ struct QuantParams {
   int* err_info;
 };
 
-// x is read through `tx`, the same [B, S, H, D] bf16 tensor map the attention kernel uses.
+// x is read through `tx`, the same [B, S, H, D] bf16 tensor map the attention kernel uses;
+// codes are written through `tout`, the E4M3 map of the attention kernel's FP8 inputs.
 template <int D>
-cudaError_t launch_hadamard_quant(const CUtensorMap& tx, const QuantParams& p, cudaStream_t stream);
+cudaError_t launch_hadamard_quant(const CUtensorMap& tx, const CUtensorMap& tout, const QuantParams& p,
+                                  cudaStream_t stream);
 
 // cs[p, i] = (cos, sin)(p * base^(-2i/D)) for p < n_pos, i < D/2, in fp64 rounded to fp32.
 cudaError_t launch_rope_table(float* cs, int n_pos, int D, double base, cudaStream_t stream);
