@@ -19,6 +19,7 @@ _D = ctypes.c_double
 SIGNATURES = {
     "attn_fwd": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P]),
     "attn_fwd_fp8": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _P]),
+    "attn_fwd_varlen": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P]),
     "hadamard_rotate_quant_fp8": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _P]),
     "rope_cos_sin_table": (_I, [_P, _I, _I, _D, _P]),
     "rope_hadamard_rotate_quant_fp8": (_I, [_P, _P, _I, _P, _P, _P, _I, _I, _I, _I, _P]),

@@ -205,6 +205,14 @@ int run_attn(const void* q, const void* k, const void* v, const float* qs, const
              : dispatch<false>(tq, tk, tv, p, D, causal, st);
 }
 
+template <bool CAUSAL>
+cudaError_t launch_varlen(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                          const AttnParams& p, int D, cudaStream_t st) {
+  return D == 64    ? launch_attn<64, false, CAUSAL, true>(tq, tk, tv, p, st)
+         : D == 128 ? launch_attn<128, false, CAUSAL, true>(tq, tk, tv, p, st)
+                    : launch_attn<256, false, CAUSAL, true>(tq, tk, tv, p, st);
+}
+
 // One thread waits on a barrier that nothing arrives at; the bounded wait records a timeout.
 __global__ void selftest_wait_kernel(long long limit, int* err) {
   __shared__ uint64_t bar;
@@ -314,6 +322,54 @@ int rope_cos_sin_table(float* cs, int n_pos, int D, double base, void* stream) {
   return ok();
 }
 
+int attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse, const int* cu_seqlens,
+                    int n_seq, int total, int max_seqlen, int H, int D, int causal, float scale, void* stream) {
+  if (cu_seqlens == nullptr || (reinterpret_cast<uintptr_t>(cu_seqlens) & 3u))
+    return fail(ATTN_ERR_INVALID_ARG, "cu_seqlens must be a non-null, 4-byte aligned device pointer");
+  if (n_seq < 1 || n_seq > VARLEN_MAX_SEQ)
+    return fail(ATTN_ERR_INVALID_ARG, "n_seq must be in [1, %d] (got %d)", VARLEN_MAX_SEQ, n_seq);
+  int rc = check_attn_args(q, k, v, o, lse, 1, H, total, D, causal, scale, 2);
+  if (rc != ATTN_OK) return rc;
+  const int rows_per_cta = 128 * attn_q_tiles(D);
+  if (max_seqlen < 1)
+    return fail(ATTN_ERR_INVALID_ARG, "max_seqlen must be >= 1 (got %d)", max_seqlen);
+  if (max_seqlen > VARLEN_MAX_LEVELS * rows_per_cta)
+    return fail(ATTN_ERR_UNSUPPORTED, "max_seqlen %d above the limit %d for D = %d", max_seqlen,
+                VARLEN_MAX_LEVELS * rows_per_cta, D);
+  if ((static_cast<long long>(total) / 128 + n_seq) * H >= (1ll << 31))
+    return fail(ATTN_ERR_INVALID_ARG, "too many work items (total / 128 + n_seq) * H");
+  const size_t lse_bytes = lse != nullptr ? 4ull * H * total : 0;
+  if (lse != nullptr && overlap(cu_seqlens, 4ull * (n_seq + 1), lse, lse_bytes))
+    return fail(ATTN_ERR_INVALID_ARG, "lse overlaps cu_seqlens");
+  if (overlap(cu_seqlens, 4ull * (n_seq + 1), o, 2ull * total * H * D))
+    return fail(ATTN_ERR_INVALID_ARG, "o overlaps cu_seqlens");
+  int* err = nullptr;
+  if ((rc = err_words(&err)) != ATTN_OK) return rc;
+  CUtensorMap tq, tk, tv;
+  if ((rc = make_qkv_map(&tq, q, 1, total, H, D, false)) != ATTN_OK) return rc;
+  if ((rc = make_qkv_map(&tk, k, 1, total, H, D, false)) != ATTN_OK) return rc;
+  if ((rc = make_qkv_map(&tv, v, 1, total, H, D, false)) != ATTN_OK) return rc;
+  AttnParams p{};
+  p.B = 1;
+  p.H = H;
+  p.S = total;
+  const float sc = scale > 0.f ? scale : 1.0f / std::sqrt(static_cast<float>(D));
+  p.c_log2 = sc * 1.4426950408889634f;
+  p.o = o;
+  p.lse = lse;
+  p.spin_limit = spin_limit();
+  p.err_word = err;
+  p.err_info = err + 1;
+  p.cu_seqlens = cu_seqlens;
+  p.n_seq = n_seq;
+  p.max_seqlen = max_seqlen;
+  p.n_levels = (max_seqlen + rows_per_cta - 1) / rows_per_cta;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const cudaError_t e = causal ? launch_varlen<true>(tq, tk, tv, p, D, st) : launch_varlen<false>(tq, tk, tv, p, D, st);
+  if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "kernel launch failed: %s", cudaGetErrorString(e));
+  return ok();
+}
+
 const char* attn_get_last_error(void) { return g_msg; }
 
 int attn_check(void* stream) {
@@ -330,6 +386,9 @@ int attn_check(void* stream) {
     if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "error word reset: %s", cudaGetErrorString(e));
     e = cudaDeviceSynchronize();
     if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "error word reset: %s", cudaGetErrorString(e));
+    if (host[0] == ATTN_ERR_INVALID_ARG)
+      return fail(host[0], "a kernel rejected its device-side input (site %d: cu_seqlens must run from 0 to "
+                  "total, non-decreasing, no sequence longer than max_seqlen)", host[1]);
     return fail(host[0], "a kernel's bounded wait ran out (code %d, site %d)", host[0], host[1]);
   }
   return ok();
@@ -348,6 +407,6 @@ int attn_selftest_bounded_wait(long long spin_cycles, void* stream) {
   return ok();
 }
 
-int attn_version(void) { return 101; }
+int attn_version(void) { return 102; }
 
 }  // extern "C"

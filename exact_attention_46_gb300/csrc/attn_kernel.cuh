@@ -39,6 +39,20 @@
 //   r_j = sv_j / max_j sv_j <= 1 folded into the exponent (p' = 2^(x - m + log2 r_j)), the row
 //   sum adds sum(p') / r_j, and the epilogue multiplies by max_j sv_j / l.
 //
+//   Packed variable-length batches (VARLEN; hada.io FA3 summary, "Weitere Optimierungen und
+//   künftige Integration", names variable-length sequences): Q, K, V are [total, H, D] with
+//   sequence offsets cu_seqlens.  Every CTA copies the offsets to shared memory and sorts the
+//   sequences by their number of query blocks (a stable counting sort, so every CTA derives
+//   the same order), and only non-empty work items exist.  Causal: items go level by level
+//   from the top query block down -- level L holds block L of every sequence longer than L
+//   blocks, a prefix of the sorted order, times H heads -- so the blocks with the most keys
+//   come first, as in the fixed-length order.  Otherwise: longest sequences first, and a
+//   head's query blocks adjacent (its K/V then comes from L2 after the first block).  Item n
+//   maps to its (sequence, head, block) by a binary search over per-level offsets.  A
+//   sequence's tiles are addressed from its first token; tiles that run into the next
+//   sequence are masked like the ragged tail of a fixed length, and rows past the sequence
+//   are never stored.
+//
 // Every mbarrier wait is bounded (ptx.cuh, wait_bounded): a wait that runs out records
 // ATTN_ERR_TIMEOUT in the device error word, raises the CTA's abort flag, and every role then
 // drains its in-flight copies / MMAs and leaves through the common exit, which frees Tensor
@@ -109,7 +123,11 @@ __device__ __forceinline__ void wait_drain(uint32_t bar, uint32_t parity, long l
   }
 }
 
-template <int D, bool FP8, bool CAUSAL>
+// Shared memory a VARLEN launch adds: offsets [n_seq + 1], two per-level arrays
+// [n_levels + 1], the item count, and the sorted sequence order (16-bit) [n_seq].
+constexpr int VARLEN_SMEM_BYTES = ((VARLEN_MAX_SEQ + 1) + 2 * (VARLEN_MAX_LEVELS + 1) + 4) * 4 + VARLEN_MAX_SEQ * 2;
+
+template <int D, bool FP8, bool CAUSAL, bool VARLEN>
 __global__ void __launch_bounds__(AttnCfg<D, FP8>::THREADS, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const AttnParams p) {
@@ -127,6 +145,12 @@ __global__ void __launch_bounds__(AttnCfg<D, FP8>::THREADS, 1)
   uint8_t* bar_ptr = base + (bar0 - base_u32);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_ptr + C::NBAR * 8);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  // VARLEN only: offsets; per level, #sequences longer than it (cnt) and its first item (off)
+  int* s_cu = reinterpret_cast<int*>(bar_ptr + C::NBAR * 8 + 16);
+  int* s_cnt = s_cu + VARLEN_MAX_SEQ + 1;
+  int* s_off = s_cnt + VARLEN_MAX_LEVELS + 1;
+  int* s_nitems = s_off + VARLEN_MAX_LEVELS + 1;
+  int16_t* s_perm = reinterpret_cast<int16_t*>(s_nitems + 4);
 
   auto BAR_Q_FULL = [&]() { return bar0; };
   auto BAR_Q_EMPTY = [&]() { return bar0 + 8u; };
@@ -158,6 +182,88 @@ __global__ void __launch_bounds__(AttnCfg<D, FP8>::THREADS, 1)
     *abort_flag = 0;
     fence_barrier_init();
   }
+  if constexpr (VARLEN) {
+    // Offsets and the length histogram (key = query blocks of a sequence) to shared memory.
+    // Offsets that are not 0 .. total, non-decreasing, with every length <= max_seqlen end
+    // the launch with ATTN_ERR_INVALID_ARG in the error word before any work is issued.
+    constexpr int QR = 128 * NT;                 // query rows per work item
+    const int ns = p.n_seq, L = p.n_levels;
+    const int tid = static_cast<int>(threadIdx.x);
+    int* s_hist = s_off;                         // the histogram, later the per-key counters
+    for (int i = tid; i <= ns; i += C::THREADS) s_cu[i] = p.cu_seqlens[i];
+    for (int i = tid; i <= L; i += C::THREADS) s_hist[i] = 0;
+    __syncthreads();
+    bool bad = false;
+    for (int sq = tid; sq < ns; sq += C::THREADS) {
+      const int len = s_cu[sq + 1] - s_cu[sq];
+      if (len < 0 || len > p.max_seqlen) bad = true;
+      else if (len > 0) atomicAdd(&s_hist[(len + QR - 1) / QR], 1);
+    }
+    if (tid == 0) bad |= s_cu[0] != 0 || s_cu[ns] != p.S;
+    if (__syncthreads_or(bad)) {
+      if (tid == 0 && atomicCAS(p.err_word, 0, 1 /* ATTN_ERR_INVALID_ARG */) == 0) atomicExch(p.err_info, 5);
+      return;
+    }
+    const uint32_t lt_mask = (1u << lane) - 1u;
+    if (warp == 0) {
+      // cnt[l] = #sequences with more than l query blocks: suffix sums of the histogram,
+      // 32 keys at a time from the top
+      int carry = 0;
+      for (int top = L; top >= 1; top -= 32) {
+        const int key = top - static_cast<int>(lane);
+        int x = key >= 1 ? s_hist[key] : 0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int y = __shfl_up_sync(0xffffffffu, x, o);
+          if (static_cast<int>(lane) >= o) x += y;
+        }
+        if (key >= 1) s_cnt[key - 1] = carry + x;
+        carry += __shfl_sync(0xffffffffu, x, 31);
+      }
+      if (lane == 0) s_cnt[L] = 0;
+      __syncwarp();
+      for (int i = static_cast<int>(lane); i <= L; i += 32) s_hist[i] = 0;
+      __syncwarp();
+      // stable counting sort by key, descending: position = cnt[key] + earlier equal keys
+      for (int base_s = 0; base_s < ns; base_s += 32) {
+        const int sq = base_s + static_cast<int>(lane);
+        const int len = sq < ns ? s_cu[sq + 1] - s_cu[sq] : 0;
+        const int key = (len + QR - 1) / QR;
+        const bool act = key > 0;
+        const uint32_t grp = __match_any_sync(0xffffffffu, act ? key : -1 - static_cast<int>(lane));
+        const int rank = __popc(grp & lt_mask);
+        int pos = 0;
+        if (act) pos = s_cnt[key] + s_hist[key] + rank;
+        __syncwarp();
+        if (act) {
+          s_perm[pos] = static_cast<int16_t>(sq);
+          if (rank == 0) s_hist[key] += __popc(grp);
+        }
+        __syncwarp();
+      }
+      // Item offsets, exclusive suffix sums from the top, and the item count.
+      //   causal: off[l] = H * #items of the levels above l, an item per (sequence, head) at a
+      //           level: x(l) = cnt[l];
+      //   else:   off[k] = H * #items of the sequences with more than k blocks, k blocks per
+      //           (sequence, head): x(k) = k * (cnt[k-1] - cnt[k]), k >= 1.
+      carry = 0;
+      const int lmin = CAUSAL ? 0 : 1, lmax = CAUSAL ? L - 1 : L;
+      for (int top = lmax; top >= lmin; top -= 32) {
+        const int l = top - static_cast<int>(lane);
+        const int own = l < lmin ? 0 : (CAUSAL ? s_cnt[l] : l * (s_cnt[l - 1] - s_cnt[l]));
+        int x = own;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int y = __shfl_up_sync(0xffffffffu, x, o);
+          if (static_cast<int>(lane) >= o) x += y;
+        }
+        if (l >= lmin) s_off[l] = (carry + x - own) * p.H;
+        carry += __shfl_sync(0xffffffffu, x, 31);
+      }
+      if (lane == 0) *s_nitems = carry * p.H;
+    }
+    __syncthreads();
+  }
   if (warp == C::MMA_WARP) tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
   if (warp == C::LOAD_WARP && lane == 0) {
     prefetch_tmap(&tmQ);
@@ -174,28 +280,68 @@ __global__ void __launch_bounds__(AttnCfg<D, FP8>::THREADS, 1)
   // are adjacent (a head's K/V is read from HBM once, then from L2).  CTA k takes item
   // n*G + k in even rounds n and n*G + G-1-k in odd rounds (zig-zag), G = gridDim.x.
   const int HB = p.H * p.B;
-  const int n_items = p.nQB * HB;
+  int n_items;
+  if constexpr (VARLEN) n_items = *s_nitems; else n_items = p.nQB * HB;
   const int G = static_cast<int>(gridDim.x);
   const int k_cta = static_cast<int>(blockIdx.x);
   auto item_of = [&](int n) { return n * G + ((n & 1) ? (G - 1 - k_cta) : k_cta); };
-  struct Item { int h, b, q0, hb, nmax; int n[NT]; };
+  // An item: query rows q0 .. q0 + 128 NT - 1 of sequence (b, h), positions counted from the
+  // sequence's first token.  VARLEN: the sequence is tokens s0 .. s0 + len - 1 of the packed
+  // axis; otherwise it is batch b and len = S (read from the parameters, not kept).
+  struct Item { int h, b, q0, hb, nmax, s0, len; int n[NT]; };
+  auto seq_len = [&](const Item& it) {
+    if constexpr (VARLEN) return it.len; else return p.S;
+  };
+  auto key_tiles = [&](const Item& it) {
+    if constexpr (VARLEN) return (it.len + 127) / 128; else return p.nK;
+  };
+  auto tma_row = [&](const Item& it, int r) {    // token coordinate of a tile row in the TMA view
+    if constexpr (VARLEN) return it.s0 + r; else return r;
+  };
   auto decode = [&](int item, Item& it) {
     int qb;
-    if (CAUSAL) {
-      qb = p.nQB - 1 - item / HB;
-      it.hb = item % HB;
+    if constexpr (VARLEN) {
+      // lowest level (causal) or block count (otherwise) whose first item is <= item
+      int lo = CAUSAL ? 0 : 1, hi = CAUSAL ? p.n_levels - 1 : p.n_levels;
+      while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (s_off[mid] <= item) hi = mid; else lo = mid + 1;
+      }
+      const int local = item - s_off[lo];
+      int sq;
+      if constexpr (CAUSAL) {
+        sq = s_perm[local / p.H];
+        it.h = local % p.H;
+        qb = lo;
+      } else {
+        // sequences with lo blocks occupy sorted ranks cnt[lo] .. cnt[lo-1]-1, H * lo items each
+        sq = s_perm[s_cnt[lo] + local / (p.H * lo)];
+        const int rem = local % (p.H * lo);
+        it.h = rem / lo;
+        qb = rem % lo;
+      }
+      const int s0 = s_cu[sq];
+      it.len = s_cu[sq + 1] - s0;
+      it.b = 0;
+      it.hb = it.h;
+      it.s0 = s0;
     } else {
-      qb = item % p.nQB;
-      it.hb = item / p.nQB;
+      if (CAUSAL) {
+        qb = p.nQB - 1 - item / HB;
+        it.hb = item % HB;
+      } else {
+        qb = item % p.nQB;
+        it.hb = item / p.nQB;
+      }
+      it.h = it.hb % p.H;
+      it.b = it.hb / p.H;
     }
-    it.h = it.hb % p.H;
-    it.b = it.hb / p.H;
     it.q0 = qb * 128 * NT;
     it.nmax = 0;
 #pragma unroll
     for (int t = 0; t < NT; ++t) {
       const int r0 = it.q0 + 128 * t;
-      it.n[t] = (r0 >= p.S) ? 0 : (CAUSAL ? (r0 / 128 + 1) : p.nK);
+      it.n[t] = (r0 >= seq_len(it)) ? 0 : (CAUSAL ? (r0 / 128 + 1) : key_tiles(it));
       it.nmax = it.n[t] > it.nmax ? it.n[t] : it.nmax;
     }
   };
@@ -225,7 +371,7 @@ __global__ void __launch_bounds__(AttnCfg<D, FP8>::THREADS, 1)
 #pragma unroll
           for (int pn = 0; pn < C::NPANEL; ++pn)
             tma_load_4d(sQ + t * C::TILE_BYTES + pn * C::PANEL_BYTES, &tmQ, BAR_Q_FULL(),
-                        pn * C::PANEL_ELEMS, it.h, it.q0 + 128 * t, it.b, pol_q);
+                        pn * C::PANEL_ELEMS, it.h, tma_row(it, it.q0 + 128 * t), it.b, pol_q);
         }
         ++q_issued;
         for (int j = 0; j < it.nmax && !*abort_flag; ++j) {
@@ -238,7 +384,7 @@ __global__ void __launch_bounds__(AttnCfg<D, FP8>::THREADS, 1)
 #pragma unroll
             for (int pn = 0; pn < C::NPANEL; ++pn)
               tma_load_4d(sKV + slot * C::TILE_BYTES + pn * C::PANEL_BYTES, m, BAR_KV_FULL(slot),
-                          pn * C::PANEL_ELEMS, it.h, 128 * j, it.b, pol_kv);
+                          pn * C::PANEL_ELEMS, it.h, tma_row(it, 128 * j), it.b, pol_kv);
             ++issued;
           }
         }
@@ -371,7 +517,7 @@ __global__ void __launch_bounds__(AttnCfg<D, FP8>::THREADS, 1)
       Item it;
       decode(item, it);
       const int r0 = it.q0 + 128 * t;
-      const int nt = (r0 >= p.S) ? 0 : (CAUSAL ? (r0 / 128 + 1) : p.nK);
+      const int nt = (r0 >= seq_len(it)) ? 0 : (CAUSAL ? (r0 / 128 + 1) : key_tiles(it));
       if (nt == 0) continue;
       const int row = it.q0 + 128 * t + row_local;
       const size_t blk_base = static_cast<size_t>(it.hb) * p.nK;   // (b*H + h) * nK
@@ -412,8 +558,8 @@ __global__ void __launch_bounds__(AttnCfg<D, FP8>::THREADS, 1)
           for (int i = 0; i < 32; ++i) reg_fence(sr[c][i]);
 
         // masks: causal diagonal tile, or the ragged last key tile
-        if (CAUSAL ? (j == nt - 1) : (j == p.nK - 1 && (p.S & 127) != 0)) {
-          const int lim = CAUSAL ? (row - 128 * j) : (p.S - 128 * j - 1);   // last visible column
+        if (CAUSAL ? (j == nt - 1) : (j == key_tiles(it) - 1 && (seq_len(it) & 127) != 0)) {
+          const int lim = CAUSAL ? (row - 128 * j) : (seq_len(it) - 128 * j - 1);   // last visible column
 #pragma unroll
           for (int c = 0; c < 4; ++c)
 #pragma unroll
@@ -523,9 +669,12 @@ __global__ void __launch_bounds__(AttnCfg<D, FP8>::THREADS, 1)
       ++ouse;
       tc_fence_after();
       const float inv_l = sv_max / l_run;
-      const bool valid = row < p.S;
-      __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(p.o) +
-                            ((static_cast<size_t>(it.b) * p.S + (valid ? row : 0)) * p.H + it.h) * D;
+      const bool valid = row < seq_len(it);
+      // token of this row on O's token axis (packed axis, or b * S + row)
+      size_t tok;
+      if constexpr (VARLEN) tok = static_cast<size_t>(it.s0) + (valid ? row : 0);
+      else tok = static_cast<size_t>(it.b) * p.S + (valid ? row : 0);
+      __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(p.o) + (tok * p.H + it.h) * D;
 #pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {
         uint32_t o[32];
@@ -549,7 +698,7 @@ __global__ void __launch_bounds__(AttnCfg<D, FP8>::THREADS, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(BAR_O_EMPTY(t));
       if (valid && p.lse != nullptr)
-        p.lse[static_cast<size_t>(it.hb) * p.S + row] = (m_run + __log2f(l_run)) * LN2;
+        p.lse[static_cast<size_t>(it.hb) * p.S + tma_row(it, row)] = (m_run + __log2f(l_run)) * LN2;
     }
   }
 
@@ -562,18 +711,21 @@ __global__ void __launch_bounds__(AttnCfg<D, FP8>::THREADS, 1)
   }
 }
 
-template <int D, bool FP8, bool CAUSAL>
+template <int D, bool FP8, bool CAUSAL, bool VARLEN>
 cudaError_t launch_attn(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                         const AttnParams& p, cudaStream_t stream) {
   using C = AttnCfg<D, FP8>;
+  constexpr int SMEM = C::SMEM_BYTES + (VARLEN ? VARLEN_SMEM_BYTES : 0);
+  static_assert(SMEM <= 227 * 1024, "shared memory budget");
+  static_assert(!(VARLEN && FP8), "variable-length batches are BF16 only");
   static std::atomic<unsigned long long> configured{0};   // one bit per device
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   const unsigned long long bit = 1ull << (dev & 63);
   if ((configured.load() & bit) == 0) {
-    e = cudaFuncSetAttribute(attn_fwd_kernel<D, FP8, CAUSAL>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+    e = cudaFuncSetAttribute(attn_fwd_kernel<D, FP8, CAUSAL, VARLEN>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
     if (e != cudaSuccess) return e;
     configured.fetch_or(bit);
   }
@@ -584,10 +736,12 @@ cudaError_t launch_attn(const CUtensorMap& tq, const CUtensorMap& tk, const CUte
     if (e != cudaSuccess) return e;
     sm_count[dev & 63] = n;
   }
-  const long long items = static_cast<long long>(p.nQB) * p.H * p.B;
+  // VARLEN: an upper bound (every sequence adds at most one partial query block per head)
+  const long long items = VARLEN ? (static_cast<long long>(p.S) / (128 * C::NT) + p.n_seq) * p.H
+                                 : static_cast<long long>(p.nQB) * p.H * p.B;
   const long long grid = items < sm_count[dev & 63] ? items : sm_count[dev & 63];   // persistent
-  attn_fwd_kernel<D, FP8, CAUSAL>
-      <<<static_cast<unsigned>(grid), C::THREADS, C::SMEM_BYTES, stream>>>(tq, tk, tv, p);
+  attn_fwd_kernel<D, FP8, CAUSAL, VARLEN>
+      <<<static_cast<unsigned>(grid), C::THREADS, SMEM, stream>>>(tq, tk, tv, p);
   return cudaGetLastError();
 }
 

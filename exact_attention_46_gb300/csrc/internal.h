@@ -21,10 +21,20 @@ struct AttnParams {
   long long spin_limit; // cycles a bounded wait may spin
   int* err_word;        // device error word (first error code)
   int* err_info;        // where it happened
+  // packed variable-length batch (the VARLEN kernels): S = total tokens, B = 1
+  const int* cu_seqlens; // [n_seq + 1] token offsets of the sequences
+  int n_seq;
+  int max_seqlen;        // bound on every sequence's length (checked by the kernel)
+  int n_levels;          // ceil(max_seqlen / query rows per CTA)
 };
 
+// Sequences and query-block levels a variable-length launch may hold: each CTA keeps the
+// offsets, the sequences sorted by length and per-level counts in shared memory.
+constexpr int VARLEN_MAX_SEQ = 4096;
+constexpr int VARLEN_MAX_LEVELS = 1024;
+
 // Launch one attention forward.  Returns the cudaError_t of the launch.
-template <int D, bool FP8, bool CAUSAL>
+template <int D, bool FP8, bool CAUSAL, bool VARLEN = false>
 cudaError_t launch_attn(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                         const AttnParams& p, cudaStream_t stream);
 

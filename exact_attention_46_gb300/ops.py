@@ -9,7 +9,7 @@ import torch
 
 from . import _lib
 
-__all__ = ["attn_fwd", "attn_fwd_fp8", "hadamard_rotate_quant_fp8", "rope_cos_sin_table",
+__all__ = ["attn_fwd", "attn_fwd_fp8", "attn_fwd_varlen", "hadamard_rotate_quant_fp8", "rope_cos_sin_table",
            "rope_hadamard_rotate_quant_fp8", "check",
            "set_spin_limit", "selftest_bounded_wait", "block_count", "ATTN_BF16", "ATTN_FP8_E4M3"]
 
@@ -66,6 +66,30 @@ def attn_fwd_fp8(q8, k8, v8, q_scale, k_scale, v_scale, causal=False, scale=0.0,
         lse = torch.empty((B, H, S), dtype=torch.float32, device=q8.device)
     _lib.call("attn_fwd_fp8", _ptr(q8), _ptr(k8), _ptr(v8), _ptr(q_scale), _ptr(k_scale),
               _ptr(v_scale), _ptr(out), _ptr(lse), B, H, S, D, int(bool(causal)), float(scale),
+              _stream(stream))
+    return out, lse
+
+
+def attn_fwd_varlen(q, k, v, cu_seqlens, max_seqlen=None, causal=False, scale=0.0, out=None, lse=None,
+                    want_lse=True, stream=None):
+    """Attention over a packed batch: q, k, v bf16 [total, H, D]; cu_seqlens int32 CUDA
+    tensor [n_seq + 1]; max_seqlen bounds every sequence's length (None: read it from
+    cu_seqlens, which synchronises).  Returns (o [total, H, D] bf16, lse [H, total] fp32 or
+    None)."""
+    for t in (q, k, v):
+        if t.dim() != 3 or not t.is_cuda or not t.is_contiguous() or t.dtype != torch.bfloat16:
+            raise ValueError("q, k, v must be contiguous bf16 CUDA tensors [total, H, D]")
+    if cu_seqlens.dtype != torch.int32 or not cu_seqlens.is_cuda or cu_seqlens.dim() != 1:
+        raise ValueError("cu_seqlens must be a 1-D int32 CUDA tensor")
+    total, H, D = q.shape
+    if max_seqlen is None:
+        max_seqlen = max(1, int((cu_seqlens[1:] - cu_seqlens[:-1]).max().item()))
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and want_lse:
+        lse = torch.empty((H, total), dtype=torch.float32, device=q.device)
+    _lib.call("attn_fwd_varlen", _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(cu_seqlens),
+              int(cu_seqlens.numel() - 1), total, int(max_seqlen), H, D, int(bool(causal)), float(scale),
               _stream(stream))
     return out, lse
 

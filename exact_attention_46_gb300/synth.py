@@ -17,7 +17,7 @@ magnitude to simulate outliers):
 
 Seeds: ``seed_for(case, stream)`` = 0xA77E000 + 16 * case + stream, with
 streams 0 = Q, 1 = K, 2 = V, 3 = Hadamard signs, 4 = outlier mask,
-5 = outlier values.
+5 = outlier values, 6 = sequence lengths of a packed batch.
 """
 
 import os
@@ -26,10 +26,10 @@ from concurrent.futures import ThreadPoolExecutor
 import numpy as np
 import torch
 
-__all__ = ["seed_for", "uniform", "normal", "normal_with_outliers", "signs",
+__all__ = ["seed_for", "uniform", "normal", "normal_with_outliers", "signs", "seqlens",
            "make_qkv", "STREAM_Q", "STREAM_K", "STREAM_V", "STREAM_SIGNS"]
 
-STREAM_Q, STREAM_K, STREAM_V, STREAM_SIGNS, STREAM_OUT_MASK, STREAM_OUT_VAL = range(6)
+STREAM_Q, STREAM_K, STREAM_V, STREAM_SIGNS, STREAM_OUT_MASK, STREAM_OUT_VAL, STREAM_LENGTHS = range(7)
 _GOLDEN = np.uint64(0x9E3779B97F4A7C15)
 _M1 = np.uint64(0xBF58476D1CE4E5B9)
 _M2 = np.uint64(0x94D049BB133111EB)
@@ -107,6 +107,19 @@ def normal_with_outliers(shape, seed_base, prob=1e-3, sigma=10.0, case_streams=N
 def signs(D, seed):
     """fp32 vector of D random signs (+1 / -1)."""
     return np.where(uniform((D,), seed) < 0.5, 1.0, -1.0).astype(np.float32)
+
+
+def seqlens(total, lo, hi, seed):
+    """Sequence lengths drawn uniformly from the integers lo .. hi until they sum to ``total``
+    (the last one cut short); returns (lengths, cu_seqlens) as int32 numpy arrays."""
+    u = uniform((total // max(lo, 1) + 1,), seed)
+    lens, acc = [], 0
+    while acc < total:
+        n = min(lo + int(u[len(lens)] * (hi - lo + 1)), total - acc)
+        lens.append(n)
+        acc += n
+    lens = np.array(lens, dtype=np.int32)
+    return lens, np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
 
 
 def make_qkv(B, S, H, D, case, dist="normal", dtype=torch.bfloat16):

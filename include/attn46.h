@@ -91,6 +91,34 @@ int attn_fwd_fp8(const void* q8, const void* k8, const void* v8,
                  float scale, void* stream);
 
 /*
+ * attn_fwd_varlen -- attn_fwd over a packed batch of variable-length sequences.
+ *   [HADA] "Weitere Optimierungen und künftige Integration" lists variable-
+ *   length sequences among the paper's optimisations; the pages define
+ *   nothing further.  Reading: the sequences are concatenated along one token
+ *   axis and each attends only to itself (causal: to its own keys j <= i,
+ *   positions counted from its first token).
+ *   q, k, v, o : [total, H, D] bf16, contiguous, 16-byte aligned.
+ *   lse        : [H, total] fp32, natural log, or NULL.
+ *   cu_seqlens : device int32 [n_seq + 1]: cu_seqlens[0] = 0, non-decreasing,
+ *                cu_seqlens[n_seq] = total; sequence s is tokens
+ *                cu_seqlens[s] .. cu_seqlens[s+1]-1 (empty sequences allowed).
+ *   n_seq      : 1 .. 4096.  total >= 1.  D in {64, 128, 256}.
+ *   max_seqlen : a bound on every sequence's length, 1 .. 262144 (131072 at
+ *                D = 256; larger is ATTN_ERR_UNSUPPORTED); it sizes the
+ *                kernel's per-level work lists.
+ *   Work is ordered heaviest first (the query blocks with the most keys, and
+ *   the longest sequences), as in attn_fwd.
+ *   Host-side checks as attn_fwd (ATTN_ERR_INVALID_ARG / _UNSUPPORTED, no
+ *   launch).  cu_seqlens lives on the device, so its contents are checked by
+ *   the kernel: offsets that break the rules above, or a sequence longer than
+ *   max_seqlen, make the launch write nothing and leave ATTN_ERR_INVALID_ARG
+ *   in the device error word, which attn_check() reports.
+ */
+int attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
+                    const int* cu_seqlens, int n_seq, int total, int max_seqlen, int H, int D,
+                    int causal, float scale, void* stream);
+
+/*
  * hadamard_rotate_quant_fp8 -- random-sign Hadamard rotation + blockwise E4M3 quantisation.
  *   [NL] "Technische innovaties", item 3, steps 1-3: multiply by a random
  *   orthogonal matrix, which spreads outliers over the coordinates, then
@@ -151,7 +179,9 @@ const char* attn_get_last_error(void);
 /*
  * attn_check -- synchronise `stream`, then read and clear the current
  * device's error word.  Returns ATTN_OK, ATTN_ERR_TIMEOUT (a kernel's bounded
- * wait ran out; its outputs are undefined) or ATTN_ERR_CUDA.
+ * wait ran out; its outputs are undefined), ATTN_ERR_INVALID_ARG (a
+ * variable-length launch found bad cu_seqlens; it wrote nothing) or
+ * ATTN_ERR_CUDA.
  */
 int attn_check(void* stream);
 

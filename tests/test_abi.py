@@ -40,7 +40,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_version(lib):
-    assert lib.attn_version() == 101
+    assert lib.attn_version() == 102
 
 
 FAKE = 1 << 20   # 16-byte aligned non-null fake device addresses: never dereferenced
@@ -88,3 +88,23 @@ def test_rotary_entry_points_reject_bad_arguments(lib):
     assert t(FAKE, 16, 128, 0.0, None) == 1
     assert t(FAKE, 16, 128, float("inf"), None) == 1
     assert t(FAKE + 4, 16, 128, 10000.0, None) == 1
+
+
+def test_varlen_rejects_bad_arguments(lib):
+    f = lib.attn_fwd_varlen
+    ok = (FAKE, FAKE * 2, FAKE * 3, FAKE * 4, None, FAKE * 8, 2, 300, 200, 2, 128, 0, 0.0, None)
+    def bad(i, val, code=1):
+        a = list(ok)
+        a[i] = val
+        assert f(*a) == code, (i, val)
+    bad(5, None)                  # no cu_seqlens
+    bad(5, FAKE * 8 + 2)          # misaligned cu_seqlens
+    bad(6, 0)                     # n_seq = 0
+    bad(6, 4097)                  # too many sequences
+    bad(7, 0)                     # total = 0
+    bad(8, 0)                     # max_seqlen = 0
+    bad(8, 262145, 2)             # max_seqlen above the level limit (D = 128)
+    bad(10, 96, 2)                # D = 96
+    bad(11, 3)                    # causal = 3
+    bad(3, FAKE * 2)              # o aliases k
+    bad(5, FAKE * 4)              # cu_seqlens inside o
