@@ -330,6 +330,37 @@ def cpu_baseline_sample(budget_s=12.0):
             "kind": "oracle", "sample": smp.describe(n, dt)}
 
 
+def varlen_mix(dev, n=20):
+    """Packed variable-length batch at the headline token count: lengths drawn uniformly from
+    128 .. 4096 (seeded) until 16384 tokens, H=16, D=128; TFLOPS = sum over sequences of
+    4 * len^2 * H * D (halved under the causal mask) / device time."""
+    from exact_attention_46_gb300 import ops, synth
+    lens, cu_np = synth.seqlens(TOKENS, 128, 4096, synth.seed_for(2, synth.STREAM_LENGTHS))
+    g = torch.Generator(device=dev).manual_seed(11)
+    q, k, v = (torch.randn((TOKENS, H, D), generator=g, device=dev).to(torch.bfloat16) for _ in range(3))
+    cu = torch.from_numpy(cu_np).to(dev)
+    o = torch.empty_like(q)
+    lse = torch.empty((H, TOKENS), dtype=torch.float32, device=dev)
+    res = {"workload": f"{len(lens)} sequences, lengths U[128, 4096] summing to {TOKENS}, H={H} D={D}",
+           "lengths": [int(x) for x in lens]}
+    for causal in (False, True):
+        fn = lambda: ops.attn_fwd_varlen(q, k, v, cu, int(lens.max()), causal=causal, out=o, lse=lse)
+        for _ in range(3):
+            fn()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record()
+        for _ in range(n):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / n
+        flops = sum(4 * int(x) * int(x) * H * D for x in lens) / (2 if causal else 1)
+        res["causal_tflops" if causal else "tflops"] = round(flops / ms / 1e9, 1)
+    ops.check()
+    return res
+
+
 def rope_fusion(dev, n=30):
     """Rotary embedding fused into the rotation + quantiser vs the rotation + quantiser alone,
     at the benchmark size (device time per launch, microseconds).  Launches cycle through three
@@ -418,6 +449,7 @@ def run_ours(args):
 
     sw = sweep(dev) if (args.sweep and rank == 0) else None
     rf = rope_fusion(dev) if (args.sweep and rank == 0) else None
+    vl = varlen_mix(dev) if (args.sweep and rank == 0) else None
     peaks, peak_src = load_peaks()
     cpu = cpu_baseline_sample() if (rank == 0 and world == 1 and args.cpu_baseline) else None
 
@@ -469,6 +501,7 @@ def run_ours(args):
             "cpu_baseline": cpu,
             "sweep": sw,
             "rope_fusion": rf,
+            "varlen": vl,
         }
         print(json.dumps(line), flush=True)
     if dist_on:
