@@ -16,10 +16,13 @@ _I = ctypes.c_int
 _F = ctypes.c_float
 _LL = ctypes.c_longlong
 _D = ctypes.c_double
+_SZ = ctypes.c_size_t
 SIGNATURES = {
     "attn_fwd": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P]),
     "attn_fwd_fp8": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _P]),
     "attn_fwd_varlen": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P]),
+    "attn_bwd_workspace_bytes": (_SZ, [_I, _I, _I]),
+    "attn_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _I, _I, _I, _I, _I, _F, _P]),
     "hadamard_rotate_quant_fp8": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _P]),
     "rope_cos_sin_table": (_I, [_P, _I, _I, _D, _P]),
     "rope_hadamard_rotate_quant_fp8": (_I, [_P, _P, _I, _P, _P, _P, _I, _I, _I, _I, _P]),

@@ -370,6 +370,67 @@ int attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float*
   return ok();
 }
 
+size_t attn_bwd_workspace_bytes(int B, int H, int S) {
+  if (B < 1 || H < 1 || S < 1) return 0;
+  return 8ull * B * H * ((static_cast<size_t>(S) + 127) / 128 * 128);
+}
+
+int attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
+             void* dq, void* dk, void* dv, float* workspace, size_t workspace_bytes, int B, int H, int S, int D,
+             int causal, float scale, void* stream) {
+  if (o == nullptr || dout == nullptr || lse == nullptr || dq == nullptr || dk == nullptr || dv == nullptr ||
+      workspace == nullptr)
+    return fail(ATTN_ERR_INVALID_ARG, "o, dout, lse, dq, dk, dv and workspace must be non-null device pointers");
+  if (D == 256) return fail(ATTN_ERR_UNSUPPORTED, "the backward pass supports D = 64 and 128 (got 256)");
+  int rc = check_attn_args(q, k, v, dq, nullptr, B, H, S, D, causal, scale, 2);
+  if (rc != ATTN_OK) return rc;
+  if (!aligned16(o) || !aligned16(dout) || !aligned16(dk) || !aligned16(dv) || !aligned16(workspace) ||
+      (reinterpret_cast<uintptr_t>(lse) & 3u))
+    return fail(ATTN_ERR_INVALID_ARG, "tensors and workspace must be 16-byte aligned (lse 4-byte)");
+  const size_t need = attn_bwd_workspace_bytes(B, H, S);
+  if (workspace_bytes < need)
+    return fail(ATTN_ERR_INVALID_ARG, "workspace of %zu bytes is smaller than the %zu needed", workspace_bytes, need);
+  const size_t n = 2ull * B * S * H * D, nl = 4ull * B * H * S;
+  const void* ins[6] = {q, k, v, o, dout, lse};
+  const size_t in_bytes[6] = {n, n, n, n, n, nl};
+  void* outs[4] = {dq, dk, dv, workspace};
+  const size_t out_bytes[4] = {n, n, n, need};
+  for (int a = 0; a < 4; ++a) {
+    for (int i = 0; i < 6; ++i)
+      if (overlap(outs[a], out_bytes[a], ins[i], in_bytes[i]))
+        return fail(ATTN_ERR_INVALID_ARG, "an output or the workspace overlaps an input");
+    for (int c = a + 1; c < 4; ++c)
+      if (overlap(outs[a], out_bytes[a], outs[c], out_bytes[c]))
+        return fail(ATTN_ERR_INVALID_ARG, "outputs overlap each other or the workspace");
+  }
+  int* err = nullptr;
+  if ((rc = err_words(&err)) != ATTN_OK) return rc;
+  CUtensorMap maps[4];
+  const void* srcs[4] = {q, k, v, dout};
+  for (int i = 0; i < 4; ++i)
+    if ((rc = make_qkv_map(&maps[i], srcs[i], B, S, H, D, false)) != ATTN_OK) return rc;
+  BwdParams p{};
+  p.B = B;
+  p.H = H;
+  p.S = S;
+  p.Sp = (S + 127) / 128 * 128;
+  p.scale = scale > 0.f ? scale : 1.0f / std::sqrt(static_cast<float>(D));
+  p.c_log2 = p.scale * 1.4426950408889634f;
+  p.o = o;
+  p.dout = dout;
+  p.lse = lse;
+  p.ws = workspace;
+  p.dq = dq;
+  p.dk = dk;
+  p.dv = dv;
+  p.spin_limit = spin_limit();
+  p.err_word = err;
+  p.err_info = err + 1;
+  const cudaError_t e = launch_attn_bwd(maps, p, D, causal != 0, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "backward launch failed: %s", cudaGetErrorString(e));
+  return ok();
+}
+
 const char* attn_get_last_error(void) { return g_msg; }
 
 int attn_check(void* stream) {
@@ -407,6 +468,6 @@ int attn_selftest_bounded_wait(long long spin_cycles, void* stream) {
   return ok();
 }
 
-int attn_version(void) { return 102; }
+int attn_version(void) { return 103; }
 
 }  // extern "C"

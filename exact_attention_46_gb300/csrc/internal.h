@@ -42,6 +42,27 @@ cudaError_t launch_attn(const CUtensorMap& tq, const CUtensorMap& tk, const CUte
 // two tiles' S and O would not fit the 512 Tensor-Memory columns).
 constexpr int attn_q_tiles(int D) { return D == 256 ? 1 : 2; }
 
+// Backward pass (attn_bwd.cu).
+struct BwdParams {
+  int B, H, S;
+  int Sp;               // S rounded up to 128: row stride of the workspace
+  float c_log2;         // softmax scale * log2(e)
+  float scale;          // softmax scale
+  const void* o;        // [B, S, H, D] bf16, the forward output
+  const void* dout;     // [B, S, H, D] bf16
+  const float* lse;     // [B, H, S] fp32, the forward's log-sum-exp
+  float* ws;            // [B*H][2][Sp] fp32: Delta, lse*log2(e)
+  void* dq;             // [B, S, H, D] bf16 outputs
+  void* dk;
+  void* dv;
+  long long spin_limit;
+  int* err_word;
+  int* err_info;
+};
+
+// Delta kernel, dK/dV kernel, dQ kernel on `st`.  maps = Q, K, V, dO ([B, S, H, D] bf16 maps).
+cudaError_t launch_attn_bwd(const CUtensorMap* maps, const BwdParams& p, int D, bool causal, cudaStream_t st);
+
 struct QuantParams {
   int B, H, S, nblk;
   void* out;            // [B, S, H, D] E4M3

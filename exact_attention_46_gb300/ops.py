@@ -9,7 +9,7 @@ import torch
 
 from . import _lib
 
-__all__ = ["attn_fwd", "attn_fwd_fp8", "attn_fwd_varlen", "hadamard_rotate_quant_fp8", "rope_cos_sin_table",
+__all__ = ["attn_fwd", "attn_fwd_fp8", "attn_fwd_varlen", "attn_bwd", "hadamard_rotate_quant_fp8", "rope_cos_sin_table",
            "rope_hadamard_rotate_quant_fp8", "check",
            "set_spin_limit", "selftest_bounded_wait", "block_count", "ATTN_BF16", "ATTN_FP8_E4M3"]
 
@@ -92,6 +92,23 @@ def attn_fwd_varlen(q, k, v, cu_seqlens, max_seqlen=None, causal=False, scale=0.
               int(cu_seqlens.numel() - 1), total, int(max_seqlen), H, D, int(bool(causal)), float(scale),
               _stream(stream))
     return out, lse
+
+
+def attn_bwd(q, k, v, o, lse, dout, causal=False, scale=0.0, dq=None, dk=None, dv=None, workspace=None,
+             stream=None):
+    """Gradients (dq, dk, dv) bf16 [B, S, H, D] of attn_fwd from its output o and lse."""
+    _check4(q, k, v, o, dout)
+    B, S, H, D = q.shape
+    nbytes = _lib.load().attn_bwd_workspace_bytes(B, H, S)
+    if workspace is None:
+        workspace = torch.empty(max(nbytes // 4, 1), dtype=torch.float32, device=q.device)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    _lib.call("attn_bwd", _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv),
+              _ptr(workspace), workspace.numel() * workspace.element_size(), B, H, S, D, int(bool(causal)),
+              float(scale), _stream(stream))
+    return dq, dk, dv
 
 
 def hadamard_rotate_quant_fp8(x, signs=None, out=None, scale=None, stream=None):

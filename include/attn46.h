@@ -119,6 +119,32 @@ int attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float*
                     int causal, float scale, void* stream);
 
 /*
+ * attn_bwd -- gradients dQ, dK, dV of attn_fwd (BF16), recomputed from the saved
+ * log-sum-exp.
+ *   The pages describe FlashAttention as tiling plus recomputation ([HADA]
+ *   "Rückblick auf den FlashAttention-Ansatz"): the score matrix is never
+ *   stored; the backward recomputes it tile by tile.  With
+ *   P = exp(scale * Q K^T - lse) (masked): dV = P^T dO, dP = dO V^T,
+ *   Delta_i = sum_d dO_id O_id, dS = P * (dP - Delta), dQ = scale * dS K,
+ *   dK = scale * dS^T Q.
+ *   q, k, v, o, dout : [B, S, H, D] bf16 inputs (o = attn_fwd's output).
+ *   lse              : [B, H, S] fp32, attn_fwd's log-sum-exp for the same
+ *                      q, k, v, causal flag and scale.
+ *   dq, dk, dv       : [B, S, H, D] bf16 outputs.
+ *   workspace        : device scratch of workspace_bytes >= attn_bwd_workspace_bytes(B, H, S)
+ *                      (per row: Delta and lse * log2(e)); owned by the
+ *                      caller, contents overwritten.
+ *   D in {64, 128} (256: ATTN_ERR_UNSUPPORTED).  causal, scale as attn_fwd.
+ *   Three kernels on `stream`: Delta, then dK/dV, then dQ.  Alignment 16 bytes
+ *   (lse 4); outputs and workspace must not overlap inputs or each other.
+ */
+size_t attn_bwd_workspace_bytes(int B, int H, int S);
+int attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
+             const float* lse, void* dq, void* dk, void* dv, float* workspace,
+             size_t workspace_bytes, int B, int H, int S, int D, int causal, float scale,
+             void* stream);
+
+/*
  * hadamard_rotate_quant_fp8 -- random-sign Hadamard rotation + blockwise E4M3 quantisation.
  *   [NL] "Technische innovaties", item 3, steps 1-3: multiply by a random
  *   orthogonal matrix, which spreads outliers over the coordinates, then

@@ -40,7 +40,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_version(lib):
-    assert lib.attn_version() == 102
+    assert lib.attn_version() == 103
 
 
 FAKE = 1 << 20   # 16-byte aligned non-null fake device addresses: never dereferenced
@@ -108,3 +108,25 @@ def test_varlen_rejects_bad_arguments(lib):
     bad(11, 3)                    # causal = 3
     bad(3, FAKE * 2)              # o aliases k
     bad(5, FAKE * 4)              # cu_seqlens inside o
+
+
+def test_backward_rejects_bad_arguments(lib):
+    f = lib.attn_bwd
+    ws = lib.attn_bwd_workspace_bytes(1, 2, 300)
+    assert ws == 8 * 2 * 384
+    assert lib.attn_bwd_workspace_bytes(0, 2, 300) == 0
+    ok = [FAKE, FAKE * 2, FAKE * 3, FAKE * 4, FAKE * 5, FAKE * 6, FAKE * 7, FAKE * 8, FAKE * 9, FAKE * 10, ws,
+          1, 2, 300, 128, 0, 0.0, None]
+    def bad(i, val, code=1):
+        a = list(ok)
+        a[i] = val
+        assert f(*a) == code, (i, val)
+    bad(5, None)                  # no lse
+    bad(9, None)                  # no workspace
+    bad(10, ws - 1)               # workspace too small
+    bad(14, 256, 2)               # D = 256 unsupported here
+    bad(14, 96, 2)                # D = 96
+    bad(15, 2)                    # causal = 2
+    bad(6, FAKE * 3)              # dq aliases v
+    bad(9, FAKE * 8)              # workspace on dk
+    bad(4, FAKE * 5 + 8)          # misaligned dout
