@@ -330,6 +330,39 @@ def cpu_baseline_sample(budget_s=12.0):
             "kind": "oracle", "sample": smp.describe(n, dt)}
 
 
+def backward_leg(dev, n=10):
+    """attn_bwd at the benchmark size (B=2, S=8192, H=16, D=128), non-causal and causal.
+    TFLOPS by the usual convention for the backward pass: 2.5x the forward's FLOPs (five
+    S x S x D GEMMs against two); the kernels execute seven (S and dP are recomputed in both
+    the dK/dV and the dQ kernel)."""
+    from exact_attention_46_gb300 import ops
+    B, S = TOKENS // HEADLINE_S, HEADLINE_S
+    g = torch.Generator(device=dev).manual_seed(13)
+    q, k, v, do = (torch.randn((B, S, H, D), generator=g, device=dev).to(torch.bfloat16) for _ in range(4))
+    ws = torch.empty(ops._lib.load().attn_bwd_workspace_bytes(B, H, S) // 4, dtype=torch.float32, device=dev)
+    dq, dk, dv = (torch.empty_like(q) for _ in range(3))
+    res = {"workload": f"B={B} S={S} H={H} D={D} bf16, inputs from attn_fwd", "flop_convention": "2.5 x forward"}
+    for causal in (False, True):
+        o, lse = ops.attn_fwd(q, k, v, causal=causal)
+        fn = lambda: ops.attn_bwd(q, k, v, o, lse, do, causal=causal, dq=dq, dk=dk, dv=dv, workspace=ws)
+        for _ in range(3):
+            fn()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record()
+        for _ in range(n):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / n
+        flops = 2.5 * attention_flops(B, H, S, D, causal)
+        key = "causal" if causal else "non_causal"
+        res[key + "_ms"] = round(ms, 4)
+        res[key + "_tflops"] = round(flops / ms / 1e9, 1)
+    ops.check()
+    return res
+
+
 def varlen_mix(dev, n=20):
     """Packed variable-length batch at the headline token count: lengths drawn uniformly from
     128 .. 4096 (seeded) until 16384 tokens, H=16, D=128; TFLOPS = sum over sequences of
@@ -450,6 +483,7 @@ def run_ours(args):
     sw = sweep(dev) if (args.sweep and rank == 0) else None
     rf = rope_fusion(dev) if (args.sweep and rank == 0) else None
     vl = varlen_mix(dev) if (args.sweep and rank == 0) else None
+    bw = backward_leg(dev) if (args.sweep and rank == 0) else None
     peaks, peak_src = load_peaks()
     cpu = cpu_baseline_sample() if (rank == 0 and world == 1 and args.cpu_baseline) else None
 
@@ -502,6 +536,7 @@ def run_ours(args):
             "sweep": sw,
             "rope_fusion": rf,
             "varlen": vl,
+            "backward": bw,
         }
         print(json.dumps(line), flush=True)
     if dist_on:
