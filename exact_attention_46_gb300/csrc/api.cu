@@ -431,6 +431,23 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const v
   return ok();
 }
 
+int attn_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                     const float* lse, void* dq, void* dk, void* dv, int B, int H, int S, int D, int causal,
+                     float scale, void* stream) {
+  const size_t need = attn_bwd_workspace_bytes(B, H, S);
+  if (need == 0) return fail(ATTN_ERR_INVALID_ARG, "B, H, S must be >= 1 (got %d, %d, %d)", B, H, S);
+  if (need > NOALLOC_BWD_SCRATCH_BYTES)
+    return fail(ATTN_ERR_INVALID_ARG,
+                "this problem needs %zu bytes of backward workspace but the built-in scratch holds %zu "
+                "(B * H * S, with S rounded up to 128, must be <= %zu); call attn_bwd with a workspace instead",
+                need, NOALLOC_BWD_SCRATCH_BYTES, NOALLOC_BWD_SCRATCH_BYTES / 8);
+  float* ws = nullptr;
+  const cudaError_t e = noalloc_bwd_scratch(&ws);
+  if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "built-in scratch address: %s", cudaGetErrorString(e));
+  return attn_bwd(q, k, v, o, dout, lse, dq, dk, dv, ws, NOALLOC_BWD_SCRATCH_BYTES, B, H, S, D, causal, scale,
+                  stream);
+}
+
 const char* attn_get_last_error(void) { return g_msg; }
 
 int attn_check(void* stream) {

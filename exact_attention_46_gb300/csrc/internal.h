@@ -60,6 +60,11 @@ struct BwdParams {
   int* err_info;
 };
 
+// Size of the fixed per-GPU scratch used by attn_bwd_noalloc, and its device address on the
+// current GPU (looked up once per device; attn_bwd_noalloc.cu).
+constexpr size_t NOALLOC_BWD_SCRATCH_BYTES = size_t(16) << 20;
+cudaError_t noalloc_bwd_scratch(float** out);
+
 // Delta kernel, dK/dV kernel, dQ kernel on `st`.  maps = Q, K, V, dO ([B, S, H, D] bf16 maps).
 cudaError_t launch_attn_bwd(const CUtensorMap* maps, const BwdParams& p, int D, bool causal, cudaStream_t st);
 

@@ -145,6 +145,30 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const v
              void* stream);
 
 /*
+ * attn_bwd_noalloc -- attn_bwd without a caller workspace.  The paper has no
+ *   counterpart; this is a convenience of this library.
+ *   For callers that cannot allocate device memory where they run the
+ *   backward pass: an engine that gave nearly all of the GPU's memory to its
+ *   own pool at start-up, or a host that forbids allocation inside per-step
+ *   calls, cannot get a fresh workspace buffer.  This entry point uses a
+ *   fixed 16 MiB scratch array that the library carries on every GPU that
+ *   loads it (held until the process exits); no call allocates or frees.
+ *   Arguments, layouts, results and errors as attn_bwd, minus the workspace.
+ *   Limit: attn_bwd_workspace_bytes(B, H, S) <= 16 MiB, i.e.
+ *   B * H * (S rounded up to 128) <= 2,097,152; larger problems are rejected
+ *   with ATTN_ERR_INVALID_ARG before anything runs.
+ *   The first call on a device looks up the scratch's device address
+ *   (cudaGetSymbolAddress) with that device current; make that first call
+ *   before any stream capture.  All calls on a device share the scratch and
+ *   it keeps the last call's contents (every call rewrites what it reads, so
+ *   nothing needs clearing); calls whose kernels overlap on the GPU race on
+ *   it and may give wrong gradients, so serialise them.
+ */
+int attn_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                     const float* lse, void* dq, void* dk, void* dv, int B, int H, int S, int D,
+                     int causal, float scale, void* stream);
+
+/*
  * hadamard_rotate_quant_fp8 -- random-sign Hadamard rotation + blockwise E4M3 quantisation.
  *   [NL] "Technische innovaties", item 3, steps 1-3: multiply by a random
  *   orthogonal matrix, which spreads outliers over the coordinates, then

@@ -130,3 +130,14 @@ def test_backward_rejects_bad_arguments(lib):
     bad(6, FAKE * 3)              # dq aliases v
     bad(9, FAKE * 8)              # workspace on dk
     bad(4, FAKE * 5 + 8)          # misaligned dout
+
+
+def test_backward_without_workspace_rejects_problems_beyond_its_scratch(lib):
+    # 2 * 16 * 65664 rows * 8 bytes > 16 MiB: rejected before any device work
+    f = lib.attn_bwd_noalloc
+    args = [FAKE, FAKE * 2, FAKE * 3, FAKE * 4, FAKE * 5, FAKE * 6, FAKE * 7, FAKE * 8, FAKE * 9,
+            2, 16, 65537, 128, 0, 0.0, None]
+    assert f(*args) == 1
+    assert b"built-in scratch" in lib.attn_get_last_error()
+    args[9] = 0
+    assert f(*args) == 1
