@@ -25,6 +25,8 @@ Modules:
 * ``fp8_path``   -- the FP8 path end to end: rotate, quantise, attend on
   the de-quantised values, with P rounded to E4M3.
 * ``backward``   -- gradients dQ, dK, dV of exact attention.
+* ``gqa``        -- grouped-query attention and decoding (S_q <= S_k, mask
+  aligned at the last key).
 * ``varlen``     -- attention over a packed batch of variable-length
   sequences (cu_seqlens offsets).
 * ``rope``       -- rotary position embedding (the pages' example of a
@@ -35,4 +37,4 @@ Every array is numpy float64 unless stated; inputs are the exact values the
 GPU sees (bf16 or E4M3 values widened to fp64).
 """
 
-from . import attention, backward, hadamard, e4m3, quantise, fp8_path, rope, varlen  # noqa: F401
+from . import attention, backward, gqa, hadamard, e4m3, quantise, fp8_path, rope, varlen  # noqa: F401
