@@ -200,6 +200,7 @@ int run_attn(const void* q, const void* k, const void* v, const float* qs, const
   p.spin_limit = spin_limit();
   p.err_word = err;
   p.err_info = err + 1;
+  p.kv_group = 1;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   return fp8 ? dispatch<true>(tq, tk, tv, p, D, causal, st)
              : dispatch<false>(tq, tk, tv, p, D, causal, st);
@@ -271,6 +272,69 @@ int run_quant(const void* x, const float* rope_cs, int n_pos, void* out, float* 
                              : launch_hadamard_quant<256>(tx, tout, p, st);
   if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "quantiser launch failed: %s", cudaGetErrorString(e));
   return ok();
+}
+
+// Key splits for decoding.  Each CTA pays a fixed start-up (barriers, Tensor Memory, the query
+// tile, filling the K/V ring, the epilogue) worth about three 128-key tiles, then streams its
+// tiles at the SM's share of HBM bandwidth; the split count minimises
+// waves * (3 + tiles per split), waves = ceil(B * Hkv * splits / SMs), fewest splits on ties.
+void decode_plan(int B, int Hkv, int Sk, int* n_split, int* tps) {
+  int dev = 0, sms = 152;
+  if (cudaGetDevice(&dev) == cudaSuccess) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && n > 0) sms = n;
+  }
+  const long long base = 1ll * B * Hkv;
+  const int nk = (Sk + 127) / 128;
+  int best_t = nk;
+  long long best = -1;
+  for (int n = 1; n <= 64 && n <= nk; ++n) {
+    const int t = (nk + n - 1) / n;
+    const int eff_n = (nk + t - 1) / t;       // splits that actually hold tiles
+    const long long waves = (base * eff_n + sms - 1) / sms;
+    const long long cost = waves * (3 + t);
+    if (best < 0 || cost < best) {
+      best = cost;
+      best_t = t;
+    }
+  }
+  *tps = best_t;
+  *n_split = (nk + best_t - 1) / best_t;
+}
+
+int make_q_group_map(CUtensorMap* m, const void* q, int B, int Sq, int Hkv, int G, int D) {
+  EncodeTiledFn enc = encode_fn();
+  if (enc == nullptr) return fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled entry point unavailable");
+  const cuuint64_t dims[5] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(G), static_cast<cuuint64_t>(Hkv),
+                              static_cast<cuuint64_t>(Sq), static_cast<cuuint64_t>(B)};
+  const cuuint64_t row = static_cast<cuuint64_t>(D) * 2;
+  const cuuint64_t strides[4] = {row, row * G, row * G * Hkv, row * G * Hkv * Sq};
+  const cuuint32_t box[5] = {64, static_cast<cuuint32_t>(G), 1, static_cast<cuuint32_t>(Sq), 1};
+  const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(q), dims, strides, box, estr,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled (grouped Q) failed (%d)", int(r));
+  return ATTN_OK;
+}
+
+// Pointer / shape checks of the grouped-head entry points: q and o carry Hq heads over Sq
+// tokens, k and v Hkv heads over Sk tokens.
+int check_gqa_args(const void* q, const void* k, const void* v, const void* o, const float* lse, int B, int Hq,
+                   int Hkv, int Sq, int Sk, int D, int causal, float scale, bool d256_ok) {
+  if (Hkv < 1 || Hq < 1 || Hq % Hkv != 0)
+    return fail(ATTN_ERR_INVALID_ARG, "Hq (%d) must be a positive multiple of Hkv (%d)", Hq, Hkv);
+  if (Sk < 1 || Sq < 1 || Sq > Sk) return fail(ATTN_ERR_INVALID_ARG, "need 1 <= Sq <= Sk (got %d, %d)", Sq, Sk);
+  if (D == 256 && !d256_ok) return fail(ATTN_ERR_UNSUPPORTED, "D = 256 is not supported here (64, 128)");
+  int rc = check_attn_args(q, q, q, o, lse, B, Hq, Sq, D, causal, scale, 2);   // q, o, lse
+  if (rc != ATTN_OK) return rc;
+  if (k == nullptr || v == nullptr || !aligned16(k) || !aligned16(v))
+    return fail(ATTN_ERR_INVALID_ARG, "k and v must be non-null, 16-byte aligned device pointers");
+  const size_t kvb = 2ull * B * Sk * Hkv * D, ob = 2ull * B * Sq * Hq * D, lb = 4ull * B * Hq * Sq;
+  if (overlap(o, ob, k, kvb) || overlap(o, ob, v, kvb) ||
+      (lse != nullptr && (overlap(lse, lb, k, kvb) || overlap(lse, lb, v, kvb))))
+    return fail(ATTN_ERR_INVALID_ARG, "an output overlaps k or v");
+  return ATTN_OK;
 }
 
 }  // namespace
@@ -362,6 +426,7 @@ int attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float*
   p.err_info = err + 1;
   p.cu_seqlens = cu_seqlens;
   p.n_seq = n_seq;
+  p.kv_group = 1;
   p.max_seqlen = max_seqlen;
   p.n_levels = (max_seqlen + rows_per_cta - 1) / rows_per_cta;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -448,6 +513,93 @@ int attn_bwd_noalloc(const void* q, const void* k, const void* v, const void* o,
                   stream);
 }
 
+int attn_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int S,
+                 int D, int causal, float scale, void* stream) {
+  int rc = check_gqa_args(q, k, v, o, lse, B, Hq, Hkv, S, S, D, causal, scale, true);
+  if (rc != ATTN_OK) return rc;
+  int* err = nullptr;
+  if ((rc = err_words(&err)) != ATTN_OK) return rc;
+  CUtensorMap tq, tk, tv;
+  if ((rc = make_qkv_map(&tq, q, B, S, Hq, D, false)) != ATTN_OK) return rc;
+  if ((rc = make_qkv_map(&tk, k, B, S, Hkv, D, false)) != ATTN_OK) return rc;
+  if ((rc = make_qkv_map(&tv, v, B, S, Hkv, D, false)) != ATTN_OK) return rc;
+  AttnParams p{};
+  p.B = B;
+  p.H = Hq;
+  p.S = S;
+  const int rows_per_cta = 128 * attn_q_tiles(D);
+  p.nQB = (S + rows_per_cta - 1) / rows_per_cta;
+  p.nK = (S + 127) / 128;
+  const float sc = scale > 0.f ? scale : 1.0f / std::sqrt(static_cast<float>(D));
+  p.c_log2 = sc * 1.4426950408889634f;
+  p.o = o;
+  p.lse = lse;
+  p.spin_limit = spin_limit();
+  p.err_word = err;
+  p.err_info = err + 1;
+  p.kv_group = Hq / Hkv;
+  return dispatch<false>(tq, tk, tv, p, D, causal, static_cast<cudaStream_t>(stream));
+}
+
+size_t attn_decode_workspace_bytes(int B, int Hq, int Hkv, int Sq, int Sk, int D) {
+  if (B < 1 || Hq < 1 || Hkv < 1 || Sq < 1 || Sk < 1 || D < 1) return 0;
+  int n_split = 1, tps = 1;
+  decode_plan(B, Hkv, Sk, &n_split, &tps);
+  if (n_split == 1) return 0;
+  return 4ull * n_split * B * Hq * Sq * (static_cast<size_t>(D) + 1);
+}
+
+int attn_decode(const void* q, const void* k, const void* v, void* o, float* lse, float* workspace,
+                size_t workspace_bytes, int B, int Hq, int Hkv, int Sq, int Sk, int D, int causal, float scale,
+                void* stream) {
+  int rc = check_gqa_args(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, D, causal, scale, false);
+  if (rc != ATTN_OK) return rc;
+  const int G = Hq / Hkv;
+  if (G * Sq > 128)
+    return fail(ATTN_ERR_UNSUPPORTED, "decoding packs (Hq / Hkv) * Sq = %d query rows into one 128-row tile; "
+                "use attn_fwd_gqa for longer query blocks", G * Sq);
+  int n_split = 1, tps = 1;
+  decode_plan(B, Hkv, Sk, &n_split, &tps);
+  const size_t need = n_split == 1 ? 0 : 4ull * n_split * B * Hq * Sq * (static_cast<size_t>(D) + 1);
+  if (need > 0) {
+    if (workspace == nullptr || workspace_bytes < need)
+      return fail(ATTN_ERR_INVALID_ARG, "decoding needs a workspace of %zu bytes (attn_decode_workspace_bytes)", need);
+    if (!aligned16(workspace)) return fail(ATTN_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
+    const size_t qb = 2ull * B * Sq * Hq * D, kvb = 2ull * B * Sk * Hkv * D;
+    if (overlap(workspace, need, q, qb) || overlap(workspace, need, k, kvb) || overlap(workspace, need, v, kvb) ||
+        overlap(workspace, need, o, qb) || (lse != nullptr && overlap(workspace, need, lse, 4ull * B * Hq * Sq)))
+      return fail(ATTN_ERR_INVALID_ARG, "the workspace overlaps a tensor");
+  }
+  int* err = nullptr;
+  if ((rc = err_words(&err)) != ATTN_OK) return rc;
+  CUtensorMap tq, tk, tv;
+  if ((rc = make_q_group_map(&tq, q, B, Sq, Hkv, G, D)) != ATTN_OK) return rc;
+  if ((rc = make_qkv_map(&tk, k, B, Sk, Hkv, D, false)) != ATTN_OK) return rc;
+  if ((rc = make_qkv_map(&tv, v, B, Sk, Hkv, D, false)) != ATTN_OK) return rc;
+  DecodeParams p{};
+  p.B = B;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.G = G;
+  p.Sq = Sq;
+  p.Sk = Sk;
+  const float sc = scale > 0.f ? scale : 1.0f / std::sqrt(static_cast<float>(D));
+  p.c_log2 = sc * 1.4426950408889634f;
+  p.o = o;
+  p.lse = lse;
+  p.n_split = n_split;
+  p.tiles_per_split = tps;
+  p.rows_total = 1ll * B * Hq * Sq;
+  p.ws_o = need > 0 ? workspace : nullptr;
+  p.ws_l = need > 0 ? workspace + static_cast<size_t>(n_split) * p.rows_total * D : nullptr;
+  p.spin_limit = spin_limit();
+  p.err_word = err;
+  p.err_info = err + 1;
+  const cudaError_t e = launch_attn_decode(tq, tk, tv, p, D, causal != 0, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "decode launch failed: %s", cudaGetErrorString(e));
+  return ok();
+}
+
 const char* attn_get_last_error(void) { return g_msg; }
 
 int attn_check(void* stream) {
@@ -485,6 +637,6 @@ int attn_selftest_bounded_wait(long long spin_cycles, void* stream) {
   return ok();
 }
 
-int attn_version(void) { return 103; }
+int attn_version(void) { return 104; }
 
 }  // extern "C"

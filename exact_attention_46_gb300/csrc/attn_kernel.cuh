@@ -359,6 +359,7 @@ __global__ void __launch_bounds__(AttnCfg<D, FP8>::THREADS, 1)
         if (item >= n_items) break;
         Item it;
         decode(item, it);
+        const int kvh = it.h / p.kv_group;     // grouped-query attention: the shared K/V head
         // The Q buffer is released by the MMA warp after the previous item's last S MMA.
         if (!wait_bounded(BAR_Q_EMPTY(), (q_issued & 1) ^ 1u, ctl, WHERE_LOAD)) break;
         uint32_t qbytes = 0;
@@ -384,7 +385,7 @@ __global__ void __launch_bounds__(AttnCfg<D, FP8>::THREADS, 1)
 #pragma unroll
             for (int pn = 0; pn < C::NPANEL; ++pn)
               tma_load_4d(sKV + slot * C::TILE_BYTES + pn * C::PANEL_BYTES, m, BAR_KV_FULL(slot),
-                          pn * C::PANEL_ELEMS, it.h, tma_row(it, 128 * j), it.b, pol_kv);
+                          pn * C::PANEL_ELEMS, kvh, tma_row(it, 128 * j), it.b, pol_kv);
             ++issued;
           }
         }

@@ -26,6 +26,8 @@ struct AttnParams {
   int n_seq;
   int max_seqlen;        // bound on every sequence's length (checked by the kernel)
   int n_levels;          // ceil(max_seqlen / query rows per CTA)
+  // grouped-query attention: query head h reads key/value head h / kv_group (1 = plain)
+  int kv_group;
 };
 
 // Sequences and query-block levels a variable-length launch may hold: each CTA keeps the
@@ -41,6 +43,26 @@ cudaError_t launch_attn(const CUtensorMap& tq, const CUtensorMap& tk, const CUte
 // Query-tile count per CTA (two Q tiles share K/V loads; one at D = 256 where
 // two tiles' S and O would not fit the 512 Tensor-Memory columns).
 constexpr int attn_q_tiles(int D) { return D == 256 ? 1 : 2; }
+
+// Decoding with grouped key/value heads (attn_decode.cu).
+struct DecodeParams {
+  int B, Hq, Hkv, G, Sq, Sk;
+  float c_log2;         // softmax scale * log2(e)
+  void* o;              // [B, Sq, Hq, D] bf16
+  float* lse;           // [B, Hq, Sq] fp32 or nullptr
+  float* ws_o;          // [n_split][rows_total][D] fp32 partial outputs (n_split > 1)
+  float* ws_l;          // [n_split][rows_total] fp32 partial lse
+  int n_split;          // key splits per (b, key/value head)
+  int tiles_per_split;  // 128-key tiles per split
+  long long rows_total; // B * Hq * Sq
+  long long spin_limit;
+  int* err_word;
+  int* err_info;
+};
+
+// tq: the 5-D [B, Sq, Hkv, G, D] view of Q (box {64, G, 1, Sq, 1}); tk, tv: [B, Sk, Hkv, D].
+cudaError_t launch_attn_decode(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                               const DecodeParams& p, int D, bool causal, cudaStream_t st);
 
 // Backward pass (attn_bwd.cu).
 struct BwdParams {

@@ -9,7 +9,7 @@ import torch
 
 from . import _lib
 
-__all__ = ["attn_fwd", "attn_fwd_fp8", "attn_fwd_varlen", "attn_bwd", "hadamard_rotate_quant_fp8", "rope_cos_sin_table",
+__all__ = ["attn_fwd", "attn_fwd_fp8", "attn_fwd_varlen", "attn_bwd", "attn_fwd_gqa", "attn_decode", "hadamard_rotate_quant_fp8", "rope_cos_sin_table",
            "rope_hadamard_rotate_quant_fp8", "check",
            "set_spin_limit", "selftest_bounded_wait", "block_count", "ATTN_BF16", "ATTN_FP8_E4M3"]
 
@@ -91,6 +91,38 @@ def attn_fwd_varlen(q, k, v, cu_seqlens, max_seqlen=None, causal=False, scale=0.
     _lib.call("attn_fwd_varlen", _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(cu_seqlens),
               int(cu_seqlens.numel() - 1), total, int(max_seqlen), H, D, int(bool(causal)), float(scale),
               _stream(stream))
+    return out, lse
+
+
+def attn_fwd_gqa(q, k, v, causal=False, scale=0.0, out=None, lse=None, want_lse=True, stream=None):
+    """Grouped-query attention: q [B, S, Hq, D], k, v [B, S, Hkv, D] bf16 -> (o, lse [B, Hq, S])."""
+    _check4(q, k, v)
+    B, S, Hq, D = q.shape
+    Hkv = k.shape[2]
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and want_lse:
+        lse = torch.empty((B, Hq, S), dtype=torch.float32, device=q.device)
+    _lib.call("attn_fwd_gqa", _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, Hq, Hkv, S, D,
+              int(bool(causal)), float(scale), _stream(stream))
+    return out, lse
+
+
+def attn_decode(q, k, v, causal=False, scale=0.0, out=None, lse=None, want_lse=True, workspace=None, stream=None):
+    """Decoding: q [B, Sq, Hq, D] against k, v [B, Sk, Hkv, D] bf16 -> (o, lse [B, Hq, Sq])."""
+    _check4(q, k, v)
+    B, Sq, Hq, D = q.shape
+    Sk, Hkv = k.shape[1], k.shape[2]
+    nbytes = _lib.load().attn_decode_workspace_bytes(B, Hq, Hkv, Sq, Sk, D)
+    if workspace is None and nbytes > 0:
+        workspace = torch.empty(nbytes // 4, dtype=torch.float32, device=q.device)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and want_lse:
+        lse = torch.empty((B, Hq, Sq), dtype=torch.float32, device=q.device)
+    wsb = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _lib.call("attn_decode", _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(workspace), wsb, B, Hq, Hkv,
+              Sq, Sk, D, int(bool(causal)), float(scale), _stream(stream))
     return out, lse
 
 

@@ -119,6 +119,39 @@ int attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float*
                     int causal, float scale, void* stream);
 
 /*
+ * attn_fwd_gqa -- attn_fwd (BF16) with grouped key/value heads.
+ *   The pages name LLM inference as future work ([HADA] "Weitere
+ *   Optimierungen und künftige Integration"); grouped-query attention is
+ *   the reading: Hq query heads share Hkv key/value heads, query head h reads
+ *   key/value head h / (Hq / Hkv).
+ *   q, o : [B, S, Hq, D] bf16.   k, v : [B, S, Hkv, D] bf16.   lse [B, Hq, S].
+ *   Hq a positive multiple of Hkv; other arguments and errors as attn_fwd.
+ */
+int attn_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                 int Hq, int Hkv, int S, int D, int causal, float scale, void* stream);
+
+/*
+ * attn_decode -- attention of Sq query tokens against Sk >= Sq keys with
+ *   grouped key/value heads: decoding (Sq = 1) and short query blocks.
+ *   The queries are the last Sq positions: under the causal mask query i sees
+ *   keys j <= Sk - Sq + i.  Query head h reads key/value head h / G, G = Hq / Hkv.
+ *   q, o : [B, Sq, Hq, D] bf16.   k, v : [B, Sk, Hkv, D] bf16.
+ *   lse  : [B, Hq, Sq] fp32 or NULL.
+ *   D in {64, 128}; G * Sq <= 128 (the G heads x Sq tokens of one key/value
+ *   head share one 128-row tile; ATTN_ERR_UNSUPPORTED otherwise).
+ *   The keys are split over CTAs to fill the GPU; with more than one split
+ *   the partial results go to `workspace` (caller-owned device scratch of
+ *   attn_decode_workspace_bytes(...) bytes, 16-byte aligned, overwritten; it
+ *   may be NULL when that function returns 0) and a second kernel merges
+ *   them.  The split count depends on the shape and the current device's SM
+ *   count only.
+ */
+size_t attn_decode_workspace_bytes(int B, int Hq, int Hkv, int Sq, int Sk, int D);
+int attn_decode(const void* q, const void* k, const void* v, void* o, float* lse, float* workspace,
+                size_t workspace_bytes, int B, int Hq, int Hkv, int Sq, int Sk, int D, int causal,
+                float scale, void* stream);
+
+/*
  * attn_bwd -- gradients dQ, dK, dV of attn_fwd (BF16), recomputed from the saved
  * log-sum-exp.
  *   The pages describe FlashAttention as tiling plus recomputation ([HADA]

@@ -40,7 +40,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_version(lib):
-    assert lib.attn_version() == 103
+    assert lib.attn_version() == 104
 
 
 FAKE = 1 << 20   # 16-byte aligned non-null fake device addresses: never dereferenced
@@ -141,3 +141,22 @@ def test_backward_without_workspace_rejects_problems_beyond_its_scratch(lib):
     assert b"built-in scratch" in lib.attn_get_last_error()
     args[9] = 0
     assert f(*args) == 1
+
+
+def test_gqa_and_decode_reject_bad_arguments(lib):
+    g = lib.attn_fwd_gqa
+    ok = [FAKE, FAKE * 2, FAKE * 3, FAKE * 4, None, 1, 8, 2, 256, 128, 0, 0.0, None]
+    for i, val, code in ((6, 3, 1), (7, 0, 1), (9, 96, 2), (0, None, 1), (1, FAKE * 2 + 8, 1), (3, FAKE * 2, 1)):
+        a = list(ok)
+        a[i] = val
+        assert g(*a) == code, (i, val)
+    d = lib.attn_decode
+    ok = [FAKE, FAKE * 8, FAKE * 16, FAKE * 24, None, None, 0, 1, 8, 2, 1, 4096, 128, 0, 0.0, None]
+    for i, val, code in ((10, 5000, 1),      # Sq > Sk
+                         (10, 33, 2),        # G * Sq = 4 * 33 > 128
+                         (12, 256, 2),       # D = 256
+                         (8, 6, 1)):         # Hq not a multiple of Hkv
+        a = list(ok)
+        a[i] = val
+        assert d(*a) == code, (i, val)
+    assert lib.attn_decode_workspace_bytes(0, 8, 2, 1, 4096, 128) == 0
