@@ -330,6 +330,39 @@ def cpu_baseline_sample(budget_s=12.0):
             "kind": "oracle", "sample": smp.describe(n, dt)}
 
 
+def decode_leg(dev, n=20):
+    """attn_decode, one query token per sequence, grouped heads: B=16, Hq=32, Hkv=8, D=128,
+    Sk=8192, causal (the token sees every key).  Bandwidth-bound: GB/s = the K and V bytes
+    (2 * B * Sk * Hkv * D * 2) per launch / device time."""
+    from exact_attention_46_gb300 import ops
+    B, Hq, Hkv, Sq, Sk, Dd = 16, 32, 8, 1, 8192, 128
+    g = torch.Generator(device=dev).manual_seed(17)
+    q = torch.randn((B, Sq, Hq, Dd), generator=g, device=dev).to(torch.bfloat16)
+    k, v = (torch.randn((B, Sk, Hkv, Dd), generator=g, device=dev).to(torch.bfloat16) for _ in range(2))
+    nb = ops._lib.load().attn_decode_workspace_bytes(B, Hq, Hkv, Sq, Sk, Dd)
+    ws = torch.empty(max(nb // 4, 1), dtype=torch.float32, device=dev)
+    o = torch.empty_like(q)
+    lse = torch.empty((B, Hq, Sq), dtype=torch.float32, device=dev)
+    fn = lambda: ops.attn_decode(q, k, v, causal=True, out=o, lse=lse, workspace=ws)
+    for _ in range(3):
+        fn()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record()
+    for _ in range(n):
+        fn()
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / n
+    ops.check()
+    kv_bytes = 2 * B * Sk * Hkv * Dd * 2
+    peaks, _ = load_peaks()
+    return {"workload": f"B={B} Hq={Hq} Hkv={Hkv} Sq={Sq} Sk={Sk} D={Dd} bf16, causal",
+            "us": round(ms * 1e3, 2), "gbs": round(kv_bytes / ms / 1e6, 1),
+            "frac_of_hbm": round(kv_bytes / ms / 1e6 / peaks["hbm_gbs"], 4),
+            "note": "K and V (537 MB) exceed L2; each launch streams them from HBM"}
+
+
 def backward_leg(dev, n=10):
     """attn_bwd at the benchmark size (B=2, S=8192, H=16, D=128), non-causal and causal.
     TFLOPS by the usual convention for the backward pass: 2.5x the forward's FLOPs (five
@@ -484,6 +517,7 @@ def run_ours(args):
     rf = rope_fusion(dev) if (args.sweep and rank == 0) else None
     vl = varlen_mix(dev) if (args.sweep and rank == 0) else None
     bw = backward_leg(dev) if (args.sweep and rank == 0) else None
+    dc = decode_leg(dev) if (args.sweep and rank == 0) else None
     peaks, peak_src = load_peaks()
     cpu = cpu_baseline_sample() if (rank == 0 and world == 1 and args.cpu_baseline) else None
 
@@ -537,6 +571,7 @@ def run_ours(args):
             "rope_fusion": rf,
             "varlen": vl,
             "backward": bw,
+            "decode": dc,
         }
         print(json.dumps(line), flush=True)
     if dist_on:
