@@ -260,6 +260,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       if (!wait_bounded(BAR_FULL(s), (i / NSTAGE) & 1, ctl, WHERE_BWD_COMPUTE)) { ok = false; break; }
       if (!wait_bounded(BAR_S, i & 1, ctl, WHERE_BWD_COMPUTE)) { ok = false; break; }
       tc_fence_after();
+      // masks are needed only on the diagonal tile (causal) and the ragged last query tile
+      const bool masked = (CAUSAL && j0 + i == kt) || q0 + 128 > p.S;
 #pragma unroll 1
       for (int c = 0; c < 4; ++c) {
         uint32_t sv[32], pv[32];
@@ -268,21 +270,28 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
         tmem_wait_ld();
         uint32_t pk[16], dk[16];
 #pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          float pp[2], dd[2];
+        for (int e = 0; e < 32; e += 4) {
+          // the columns' Delta and lse*log2e, four at a time (broadcast reads)
+          const float4 l4 = *reinterpret_cast<const float4*>(l2 + 32 * c + e);
+          const float4 d4 = *reinterpret_cast<const float4*>(dlt + 32 * c + e);
+          const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, dv4[4] = {d4.x, d4.y, d4.z, d4.w};
+          float pp[4], dd[4];
 #pragma unroll
-          for (int u = 0; u < 2; ++u) {
+          for (int u = 0; u < 4; ++u) {
             reg_fence(sv[e + u]);
             reg_fence(pv[e + u]);
-            const int col = 32 * c + e + u;
-            const int q = q0 + col;
-            const bool vis = q < p.S && (!CAUSAL || key <= q);
-            const float x = vis ? fmaf(__uint_as_float(sv[e + u]), p.c_log2, -l2[col]) : -INFINITY;
+            float x = fmaf(__uint_as_float(sv[e + u]), p.c_log2, -lv[u]);
+            if (masked) {
+              const int q = q0 + 32 * c + e + u;
+              if (!(q < p.S && (!CAUSAL || key <= q))) x = -INFINITY;
+            }
             pp[u] = ex2(x);
-            dd[u] = pp[u] * (__uint_as_float(pv[e + u]) - dlt[col]);
+            dd[u] = pp[u] * (__uint_as_float(pv[e + u]) - dv4[u]);
           }
           pk[e / 2] = pack_bf16x2(pp[0], pp[1]);
+          pk[e / 2 + 1] = pack_bf16x2(pp[2], pp[3]);
           dk[e / 2] = pack_bf16x2(dd[0], dd[1]);
+          dk[e / 2 + 1] = pack_bf16x2(dd[2], dd[3]);
         }
         tmem_st16(tl + 16u * c, pk);
         tmem_st16(tl + 128u + 16u * c, dk);
@@ -457,6 +466,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     bool ok = true;
     for (int i = 0; ok && i < ntile; ++i) {
       const int kb = 128 * i;
+      const bool masked = (CAUSAL && i == qt) || kb + 128 > p.S;
       if (!wait_bounded(BAR_S, i & 1, ctl, WHERE_BWD_COMPUTE)) { ok = false; break; }
       tc_fence_after();
 #pragma unroll 1
@@ -473,9 +483,11 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
           for (int u = 0; u < 2; ++u) {
             reg_fence(sv[e + u]);
             reg_fence(pv[e + u]);
-            const int kcol = kb + 32 * c + e + u;
-            const bool vis = kcol < p.S && (!CAUSAL || kcol <= qrow);
-            const float x = vis ? fmaf(__uint_as_float(sv[e + u]), p.c_log2, -l2) : -INFINITY;
+            float x = fmaf(__uint_as_float(sv[e + u]), p.c_log2, -l2);
+            if (masked) {
+              const int kcol = kb + 32 * c + e + u;
+              if (!(kcol < p.S && (!CAUSAL || kcol <= qrow))) x = -INFINITY;
+            }
             dd[u] = ex2(x) * (__uint_as_float(pv[e + u]) - dlt);
           }
           dk[e / 2] = pack_bf16x2(dd[0], dd[1]);
