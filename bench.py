@@ -609,6 +609,10 @@ def run_reference(args):
     }), flush=True)
 
 
+# auxiliary legs, by name (bench.py --profile-leg NAME runs one of them alone)
+LEGS = {"varlen": varlen_mix, "rope": rope_fusion, "backward": backward_leg, "decode": decode_leg}
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -617,10 +621,18 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-sweep", dest="sweep", action="store_false")
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
+    ap.add_argument("--profile-leg", choices=sorted(LEGS),
+                    help="run one auxiliary leg's workload once (for a profiler) and print its result")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
-    if args.impl == "reference":
+    if args.profile_leg:
+        import __graft_entry__
+        __graft_entry__.build()
+        dev = torch.device("cuda", 0)
+        torch.cuda.set_device(dev)
+        print(json.dumps({args.profile_leg: LEGS[args.profile_leg](dev, n=1)}), flush=True)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)
