@@ -85,7 +85,7 @@ struct AttnCfg {
   static constexpr int SMEM_TILES_BUDGET = 200 * 1024;
   static constexpr int NSLOT_RAW = (SMEM_TILES_BUDGET - NT * TILE_BYTES) / TILE_BYTES;
   static constexpr int NSLOT = NSLOT_RAW > 8 ? 8 : NSLOT_RAW;
-  static constexpr int NBAR = 2 + 2 * NSLOT + 4 * NT + 1;
+  static constexpr int NBAR = 2 + 2 * NSLOT + 5 * NT + 1;
   static constexpr int SMEM_BYTES_RAW = (NT + NSLOT) * TILE_BYTES + NBAR * 8 + 16;
   // Request at least ~120 KB so that one CTA (and its 512 TMEM columns) owns the SM.
   static constexpr int SMEM_BYTES =
@@ -134,6 +134,7 @@ __global__ void __launch_bounds__(AttnCfg<D, FP8>::THREADS, 1)
   using C = AttnCfg<D, FP8>;
   constexpr int NT = C::NT;
   constexpr int NSLOT = C::NSLOT;
+  constexpr bool SPLIT_P = NT == 1;    // hand P to the MMA warp in two halves (one query tile)
 
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_u32 = smem_u32(smem_raw);
@@ -161,6 +162,8 @@ __global__ void __launch_bounds__(AttnCfg<D, FP8>::THREADS, 1)
   auto BAR_O_FULL = [&](int t) { return bar0 + 8u * (2 + 2 * NSLOT + 2 * NT + t); };
   auto BAR_O_EMPTY = [&](int t) { return bar0 + 8u * (2 + 2 * NSLOT + 3 * NT + t); };
   auto BAR_MMA_DONE = [&]() { return bar0 + 8u * (2 + 2 * NSLOT + 4 * NT); };
+  // the first half of P_t (keys 0..63 of the tile) is in Tensor Memory
+  auto BAR_P_HALF = [&](int t) { return bar0 + 8u * (2 + 2 * NSLOT + 4 * NT + 1 + t); };
 
   const uint32_t warp = warp_id();
   const uint32_t lane = lane_id();
@@ -175,6 +178,7 @@ __global__ void __launch_bounds__(AttnCfg<D, FP8>::THREADS, 1)
     for (int t = 0; t < NT; ++t) {
       mbar_init(BAR_S_FULL(t), 1);
       mbar_init(BAR_P_FULL(t), 4);
+      mbar_init(BAR_P_HALF(t), 4);
       mbar_init(BAR_O_FULL(t), 1);
       mbar_init(BAR_O_EMPTY(t), 4);
     }
@@ -418,11 +422,12 @@ __global__ void __launch_bounds__(AttnCfg<D, FP8>::THREADS, 1)
           else     mma_f16_ss(d, a0 + off, b0 + off, C::IDESC_QK, kk > 0);
         }
       };
-      auto gemm_pv = [&](int t, int slot, bool acc) {
+      // O_t += P_t V over K-steps [k_begin, k_end) (each half of the keys follows its own arrival)
+      auto gemm_pv = [&](int t, int slot, bool acc, int k_begin, int k_end) {
         const uint32_t d = tmem + 128u * NT + static_cast<uint32_t>(D) * t;
         const uint64_t b0 = dv0 + ((slot * C::TILE_BYTES) >> 4);
 #pragma unroll
-        for (int kk = 0; kk < C::KSTEPS_PV; ++kk) {
+        for (int kk = k_begin; kk < k_end; ++kk) {
           const uint32_t a = tmem + 128u * t + 8u * kk;
           const uint32_t off = (kk * C::UMMA_K * C::PANEL_ROW) >> 4;
           if (FP8) mma_f8_ts(d, a, b0 + off, C::IDESC_PV, (acc || kk > 0) ? 1u : 0u);
@@ -471,10 +476,15 @@ __global__ void __launch_bounds__(AttnCfg<D, FP8>::THREADS, 1)
                 // O_t is free once the softmax warps have read the previous item's O_t.
                 if (!wait_bounded(BAR_O_EMPTY(t), (ouse[t] & 1) ^ 1, ctl, WHERE_MMA)) { ok = false; break; }
               }
+              if constexpr (SPLIT_P) {
+                if (!wait_bounded(BAR_P_HALF(t), pc[t] & 1, ctl, WHERE_MMA)) { ok = false; break; }
+                tc_fence_after();
+                gemm_pv(t, vs, j - 1 > 0, 0, C::KSTEPS_PV / 2);
+              }
               if (!wait_bounded(BAR_P_FULL(t), pc[t] & 1, ctl, WHERE_MMA)) { ok = false; break; }
               ++pc[t];
               tc_fence_after();
-              gemm_pv(t, vs, j - 1 > 0);
+              gemm_pv(t, vs, SPLIT_P || j - 1 > 0, SPLIT_P ? C::KSTEPS_PV / 2 : 0, C::KSTEPS_PV);
               if (j - 1 == it.n[t] - 1) {
                 mma_commit(BAR_O_FULL(t));
                 ++ouse[t];
@@ -598,6 +608,34 @@ __global__ void __launch_bounds__(AttnCfg<D, FP8>::THREADS, 1)
         uint64_t ls2[4];
 #pragma unroll
         for (int k = 0; k < 4; ++k) ls2[k] = f2_pack(0.f, 0.f);
+        // O_t holds PV_t(j-1) complete (it preceded S_t(j)) and PV_t(j) waits for this warp's
+        // arrival, so O_t is rescaled in place before that arrival.  With one query tile
+        // (SPLIT_P) the first 64 keys' numerators are handed over on their own, so PV over them
+        // overlaps the exponentials of the second half; with two tiles the other tile's MMAs
+        // already fill that time and the extra hand-off only costs.
+        auto rescale_o = [&]() {
+          if (__any_sync(0xffffffffu, rescale)) {
+#pragma unroll 1
+            for (int c = 0; c < D / 32; ++c) {
+              uint32_t o[32];
+              tmem_ld32(o_addr + 32u * c, o);
+              tmem_wait_ld();
+#pragma unroll
+              for (int i = 0; i < 32; ++i) {
+                reg_fence(o[i]);
+                o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+              }
+              tmem_st32(o_addr + 32u * c, o);
+            }
+          }
+        };
+        auto hand_off_first_half = [&]() {
+          rescale_o();
+          tmem_wait_st();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(BAR_P_HALF(t));
+        };
         if (!FP8) {
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
@@ -612,6 +650,7 @@ __global__ void __launch_bounds__(AttnCfg<D, FP8>::THREADS, 1)
               pk[i] = pack_bf16x2(p0, p1);
             }
             tmem_st16(s_addr + 16u * c, pk);
+            if (SPLIT_P && c == 1) hand_off_first_half();
           }
         } else {
 #pragma unroll
@@ -634,6 +673,7 @@ __global__ void __launch_bounds__(AttnCfg<D, FP8>::THREADS, 1)
               pk[i] = pack_e4m3x4(pv[0], pv[1], pv[2], pv[3]);
             }
             tmem_st16(s_addr + 16u * h2, pk);
+            if (SPLIT_P && h2 == 0) hand_off_first_half();
           }
         }
         {
@@ -642,22 +682,7 @@ __global__ void __launch_bounds__(AttnCfg<D, FP8>::THREADS, 1)
           f2_unpack(t2, a0, a1);
           l_run += (a0 + a1) * inv_r;
         }
-        if (__any_sync(0xffffffffu, rescale)) {
-          // O_t holds PV_t(j-1) complete (it preceded S_t(j)); PV_t(j) waits for this warp's
-          // arrival below, so O_t can be rescaled in place now (S_t's registers are dead here).
-#pragma unroll 1
-          for (int c = 0; c < D / 32; ++c) {
-            uint32_t o[32];
-            tmem_ld32(o_addr + 32u * c, o);
-            tmem_wait_ld();
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              reg_fence(o[i]);
-              o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-            }
-            tmem_st32(o_addr + 32u * c, o);
-          }
-        }
+        if (!SPLIT_P) rescale_o();
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
