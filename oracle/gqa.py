@@ -13,16 +13,21 @@ decoding.  Readings (the common ones):
   mask is aligned at the bottom-right); without the mask every query sees all S_k keys.
 
 Per query head this is the definition in ``attention`` with that key/value head and mask.
+
+For the FP8 path (inputs already de-quantised from E4M3) ``round_p`` rounds the softmax
+numerators exp(s - m) to E4M3 before the product with V, as in ``fp8_path``: relative to the
+exact row max, with the row sum taken over the unrounded numerators.
 """
 
 import numpy as np
 
 from .attention import default_scale
+from .e4m3 import round_e4m3
 
 __all__ = ["attention_gqa"]
 
 
-def attention_gqa(q, k, v, scale=None, causal=False):
+def attention_gqa(q, k, v, scale=None, causal=False, round_p=False):
     """q [B, Sq, Hq, D], k and v [B, Sk, Hkv, D] -> (O [B, Sq, Hq, D], lse [B, Hq, Sq])."""
     q = np.asarray(q, dtype=np.float64)
     k = np.asarray(k, dtype=np.float64)
@@ -46,6 +51,7 @@ def attention_gqa(q, k, v, scale=None, causal=False):
             m = s.max(axis=1)
             e = np.exp(s - m[:, None])
             l = e.sum(axis=1)
-            O[b, :, h] = (e / l[:, None]) @ v[b, :, h // G]
+            num = round_e4m3(e) if round_p else e
+            O[b, :, h] = (num / l[:, None]) @ v[b, :, h // G]
             lse[b, h] = m + np.log(l)
     return O, lse

@@ -74,3 +74,16 @@ def test_rejects_bad_shapes():
         gqa.attention_gqa(np.zeros((1, 2, 3, 4)), np.zeros((1, 2, 2, 4)), np.zeros((1, 2, 2, 4)))
     with pytest.raises(ValueError):
         gqa.attention_gqa(np.zeros((1, 5, 2, 4)), np.zeros((1, 4, 2, 4)), np.zeros((1, 4, 2, 4)))
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_rounded_numerators_match_the_fp8_path_at_one_group(causal):
+    # G = 1 and Sq = Sk: the same computation as fp8_path.attention_rounded_p
+    from oracle import fp8_path
+    q, k, v = (RNG.standard_normal((2, 50, 3, 16)) for _ in range(3))
+    a, la = gqa.attention_gqa(q, k, v, causal=causal, round_p=True)
+    b, lb = fp8_path.attention_rounded_p(q, k, v, 1 / math.sqrt(16), causal)
+    np.testing.assert_allclose(a, b, atol=1e-13)
+    np.testing.assert_allclose(la, lb, atol=1e-13)
+    c, _ = gqa.attention_gqa(q, k, v, causal=causal)
+    assert np.abs(a - c).max() > 1e-4          # the rounding does change O
