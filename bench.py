@@ -369,8 +369,9 @@ def cpu_baseline_sample(budget_s=12.0):
 def decode_leg(dev, n=20):
     """attn_decode, one query token per sequence, grouped heads: B=16, Hq=32, Hkv=8, D=128,
     Sk=8192, causal (the token sees every key).  Bandwidth-bound: GB/s = the K and V bytes
-    (2 * B * Sk * Hkv * D * 2) per launch / device time."""
-    from exact_attention_46_gb300 import ops
+    (2 * B * Sk * Hkv * D * element size) per launch / device time.  The same step on E4M3
+    (attn_decode_fp8, Q and K rotated, block scales from the quantiser) streams half the bytes."""
+    from exact_attention_46_gb300 import ops, synth
     B, Hq, Hkv, Sq, Sk, Dd = 16, 32, 8, 1, 8192, 128
     g = torch.Generator(device=dev).manual_seed(17)
     q = torch.randn((B, Sq, Hq, Dd), generator=g, device=dev).to(torch.bfloat16)
@@ -379,24 +380,37 @@ def decode_leg(dev, n=20):
     ws = torch.empty(max(nb // 4, 1), dtype=torch.float32, device=dev)
     o = torch.empty_like(q)
     lse = torch.empty((B, Hq, Sq), dtype=torch.float32, device=dev)
-    fn = lambda: ops.attn_decode(q, k, v, causal=True, out=o, lse=lse, workspace=ws)
-    for _ in range(3):
-        fn()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    torch.cuda.synchronize()
-    e0.record()
-    for _ in range(n):
-        fn()
-    e1.record()
-    torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1) / n
+
+    def timed(fn):
+        for _ in range(3):
+            fn()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record()
+        for _ in range(n):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / n
+
+    ms = timed(lambda: ops.attn_decode(q, k, v, causal=True, out=o, lse=lse, workspace=ws))
+    sg = torch.from_numpy(synth.signs(Dd, synth.seed_for(17, synth.STREAM_SIGNS))).to(dev)
+    q8, sq = ops.hadamard_rotate_quant_fp8(q, sg)
+    k8, sk = ops.hadamard_rotate_quant_fp8(k, sg)
+    v8, sv = ops.hadamard_rotate_quant_fp8(v, None)
+    del k, v
+    ms8 = timed(lambda: ops.attn_decode_fp8(q8, k8, v8, sq, sk, sv, causal=True, out=o, lse=lse, workspace=ws))
     ops.check()
     kv_bytes = 2 * B * Sk * Hkv * Dd * 2
+    kv8_bytes = kv_bytes // 2 + 2 * sk.numel() * 4
     peaks, _ = load_peaks()
-    return {"workload": f"B={B} Hq={Hq} Hkv={Hkv} Sq={Sq} Sk={Sk} D={Dd} bf16, causal",
+    return {"workload": f"B={B} Hq={Hq} Hkv={Hkv} Sq={Sq} Sk={Sk} D={Dd}, causal",
             "us": round(ms * 1e3, 2), "gbs": round(kv_bytes / ms / 1e6, 1),
             "frac_of_hbm": round(kv_bytes / ms / 1e6 / peaks["hbm_gbs"], 4),
-            "note": "K and V (537 MB) exceed L2; each launch streams them from HBM"}
+            "fp8_us": round(ms8 * 1e3, 2), "fp8_gbs": round(kv8_bytes / ms8 / 1e6, 1),
+            "fp8_frac_of_hbm": round(kv8_bytes / ms8 / 1e6 / peaks["hbm_gbs"], 4),
+            "fp8_speedup": round(ms / ms8, 3),
+            "note": "K and V (537 MB bf16, 268 MB E4M3) exceed L2; each launch streams them from HBM"}
 
 
 def backward_leg(dev, n=10):

@@ -90,6 +90,13 @@ EncodeTiledFn encode_fn() {
 
 // [B, S, H, D] tensor viewed as the 4-D box grid (D, H, S, B); one box = 128 tokens x one
 // swizzle panel of one head.
+// L2 promotion no wider than one row: a row of another head sits beside each row, and a wider
+// promotion would fetch it from HBM with this one.
+CUtensorMapL2promotion l2_promotion(int row_bytes) {
+  return row_bytes >= 256 ? CU_TENSOR_MAP_L2_PROMOTION_L2_256B
+                          : (row_bytes >= 128 ? CU_TENSOR_MAP_L2_PROMOTION_L2_128B : CU_TENSOR_MAP_L2_PROMOTION_L2_64B);
+}
+
 int make_qkv_map(CUtensorMap* m, const void* ptr, int B, int S, int H, int D, bool fp8) {
   EncodeTiledFn enc = encode_fn();
   if (enc == nullptr) return fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled entry point unavailable");
@@ -107,7 +114,7 @@ int make_qkv_map(CUtensorMap* m, const void* ptr, int B, int S, int H, int D, bo
                          4, const_cast<void*>(ptr), dims, strides, box, estr,
                          CU_TENSOR_MAP_INTERLEAVE_NONE,
                          panel_row == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
-                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                         l2_promotion(row_bytes), CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", int(r));
   return ATTN_OK;
 }
@@ -302,18 +309,22 @@ void decode_plan(int B, int Hkv, int Sk, int* n_split, int* tps) {
   *n_split = (nk + best_t - 1) / best_t;
 }
 
-int make_q_group_map(CUtensorMap* m, const void* q, int B, int Sq, int Hkv, int G, int D) {
+int make_q_group_map(CUtensorMap* m, const void* q, int B, int Sq, int Hkv, int G, int D, bool fp8) {
   EncodeTiledFn enc = encode_fn();
   if (enc == nullptr) return fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled entry point unavailable");
+  const int esz = fp8 ? 1 : 2;
+  const int panel_row = D * esz >= 128 ? 128 : D * esz;
   const cuuint64_t dims[5] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(G), static_cast<cuuint64_t>(Hkv),
                               static_cast<cuuint64_t>(Sq), static_cast<cuuint64_t>(B)};
-  const cuuint64_t row = static_cast<cuuint64_t>(D) * 2;
+  const cuuint64_t row = static_cast<cuuint64_t>(D) * esz;
   const cuuint64_t strides[4] = {row, row * G, row * G * Hkv, row * G * Hkv * Sq};
-  const cuuint32_t box[5] = {64, static_cast<cuuint32_t>(G), 1, static_cast<cuuint32_t>(Sq), 1};
+  const cuuint32_t box[5] = {static_cast<cuuint32_t>(panel_row / esz), static_cast<cuuint32_t>(G), 1,
+                             static_cast<cuuint32_t>(Sq), 1};
   const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
-  const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(q), dims, strides, box, estr,
-                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  const CUresult r = enc(m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5,
+                         const_cast<void*>(q), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                         panel_row == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                         l2_promotion(D * esz), CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled (grouped Q) failed (%d)", int(r));
   return ATTN_OK;
 }
@@ -321,16 +332,16 @@ int make_q_group_map(CUtensorMap* m, const void* q, int B, int Sq, int Hkv, int 
 // Pointer / shape checks of the grouped-head entry points: q and o carry Hq heads over Sq
 // tokens, k and v Hkv heads over Sk tokens.
 int check_gqa_args(const void* q, const void* k, const void* v, const void* o, const float* lse, int B, int Hq,
-                   int Hkv, int Sq, int Sk, int D, int causal, float scale, bool d256_ok) {
+                   int Hkv, int Sq, int Sk, int D, int causal, float scale, bool d256_ok, int esz = 2) {
   if (Hkv < 1 || Hq < 1 || Hq % Hkv != 0)
     return fail(ATTN_ERR_INVALID_ARG, "Hq (%d) must be a positive multiple of Hkv (%d)", Hq, Hkv);
   if (Sk < 1 || Sq < 1 || Sq > Sk) return fail(ATTN_ERR_INVALID_ARG, "need 1 <= Sq <= Sk (got %d, %d)", Sq, Sk);
   if (D == 256 && !d256_ok) return fail(ATTN_ERR_UNSUPPORTED, "D = 256 is not supported here (64, 128)");
-  int rc = check_attn_args(q, q, q, o, lse, B, Hq, Sq, D, causal, scale, 2);   // q, o, lse
+  int rc = check_attn_args(q, q, q, o, lse, B, Hq, Sq, D, causal, scale, esz);   // q, o, lse
   if (rc != ATTN_OK) return rc;
   if (k == nullptr || v == nullptr || !aligned16(k) || !aligned16(v))
     return fail(ATTN_ERR_INVALID_ARG, "k and v must be non-null, 16-byte aligned device pointers");
-  const size_t kvb = 2ull * B * Sk * Hkv * D, ob = 2ull * B * Sq * Hq * D, lb = 4ull * B * Hq * Sq;
+  const size_t kvb = 1ull * esz * B * Sk * Hkv * D, ob = 2ull * B * Sq * Hq * D, lb = 4ull * B * Hq * Sq;
   if (overlap(o, ob, k, kvb) || overlap(o, ob, v, kvb) ||
       (lse != nullptr && (overlap(lse, lb, k, kvb) || overlap(lse, lb, v, kvb))))
     return fail(ATTN_ERR_INVALID_ARG, "an output overlaps k or v");
@@ -549,10 +560,17 @@ size_t attn_decode_workspace_bytes(int B, int Hq, int Hkv, int Sq, int Sk, int D
   return 4ull * n_split * B * Hq * Sq * (static_cast<size_t>(D) + 1);
 }
 
-int attn_decode(const void* q, const void* k, const void* v, void* o, float* lse, float* workspace,
-                size_t workspace_bytes, int B, int Hq, int Hkv, int Sq, int Sk, int D, int causal, float scale,
-                void* stream) {
-  int rc = check_gqa_args(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, D, causal, scale, false);
+}  // extern "C"
+
+namespace {
+
+// The decoding entry points: bf16 inputs (qs = ks = vs = nullptr, fp8 = false) or E4M3 codes
+// with their block scales.
+int run_decode(const void* q, const void* k, const void* v, const float* qs, const float* ks, const float* vs,
+               void* o, float* lse, float* workspace, size_t workspace_bytes, int B, int Hq, int Hkv, int Sq,
+               int Sk, int D, int causal, float scale, bool fp8, void* stream) {
+  const int esz = fp8 ? 1 : 2;
+  int rc = check_gqa_args(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, D, causal, scale, false, esz);
   if (rc != ATTN_OK) return rc;
   const int G = Hq / Hkv;
   if (G * Sq > 128)
@@ -565,17 +583,17 @@ int attn_decode(const void* q, const void* k, const void* v, void* o, float* lse
     if (workspace == nullptr || workspace_bytes < need)
       return fail(ATTN_ERR_INVALID_ARG, "decoding needs a workspace of %zu bytes (attn_decode_workspace_bytes)", need);
     if (!aligned16(workspace)) return fail(ATTN_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
-    const size_t qb = 2ull * B * Sq * Hq * D, kvb = 2ull * B * Sk * Hkv * D;
+    const size_t qb = 1ull * esz * B * Sq * Hq * D, kvb = 1ull * esz * B * Sk * Hkv * D, ob = 2ull * B * Sq * Hq * D;
     if (overlap(workspace, need, q, qb) || overlap(workspace, need, k, kvb) || overlap(workspace, need, v, kvb) ||
-        overlap(workspace, need, o, qb) || (lse != nullptr && overlap(workspace, need, lse, 4ull * B * Hq * Sq)))
+        overlap(workspace, need, o, ob) || (lse != nullptr && overlap(workspace, need, lse, 4ull * B * Hq * Sq)))
       return fail(ATTN_ERR_INVALID_ARG, "the workspace overlaps a tensor");
   }
   int* err = nullptr;
   if ((rc = err_words(&err)) != ATTN_OK) return rc;
   CUtensorMap tq, tk, tv;
-  if ((rc = make_q_group_map(&tq, q, B, Sq, Hkv, G, D)) != ATTN_OK) return rc;
-  if ((rc = make_qkv_map(&tk, k, B, Sk, Hkv, D, false)) != ATTN_OK) return rc;
-  if ((rc = make_qkv_map(&tv, v, B, Sk, Hkv, D, false)) != ATTN_OK) return rc;
+  if ((rc = make_q_group_map(&tq, q, B, Sq, Hkv, G, D, fp8)) != ATTN_OK) return rc;
+  if ((rc = make_qkv_map(&tk, k, B, Sk, Hkv, D, fp8)) != ATTN_OK) return rc;
+  if ((rc = make_qkv_map(&tv, v, B, Sk, Hkv, D, fp8)) != ATTN_OK) return rc;
   DecodeParams p{};
   p.B = B;
   p.Hq = Hq;
@@ -595,9 +613,37 @@ int attn_decode(const void* q, const void* k, const void* v, void* o, float* lse
   p.spin_limit = spin_limit();
   p.err_word = err;
   p.err_info = err + 1;
-  const cudaError_t e = launch_attn_decode(tq, tk, tv, p, D, causal != 0, static_cast<cudaStream_t>(stream));
+  p.q_scale = qs;
+  p.k_scale = ks;
+  p.v_scale = vs;
+  p.nqb = (Sq + 127) / 128;
+  p.nkb = (Sk + 127) / 128;
+  const cudaError_t e = launch_attn_decode(tq, tk, tv, p, D, fp8, causal != 0, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "decode launch failed: %s", cudaGetErrorString(e));
   return ok();
+}
+
+}  // namespace
+
+extern "C" {
+
+int attn_decode(const void* q, const void* k, const void* v, void* o, float* lse, float* workspace,
+                size_t workspace_bytes, int B, int Hq, int Hkv, int Sq, int Sk, int D, int causal, float scale,
+                void* stream) {
+  return run_decode(q, k, v, nullptr, nullptr, nullptr, o, lse, workspace, workspace_bytes, B, Hq, Hkv, Sq, Sk, D,
+                    causal, scale, false, stream);
+}
+
+int attn_decode_fp8(const void* q8, const void* k8, const void* v8, const float* q_scale, const float* k_scale,
+                    const float* v_scale, void* o, float* lse, float* workspace, size_t workspace_bytes, int B,
+                    int Hq, int Hkv, int Sq, int Sk, int D, int causal, float scale, void* stream) {
+  if (q_scale == nullptr || k_scale == nullptr || v_scale == nullptr)
+    return fail(ATTN_ERR_INVALID_ARG, "q_scale, k_scale and v_scale must be non-null");
+  if ((reinterpret_cast<uintptr_t>(q_scale) | reinterpret_cast<uintptr_t>(k_scale) |
+       reinterpret_cast<uintptr_t>(v_scale)) & 3u)
+    return fail(ATTN_ERR_INVALID_ARG, "scale arrays must be 4-byte aligned");
+  return run_decode(q8, k8, v8, q_scale, k_scale, v_scale, o, lse, workspace, workspace_bytes, B, Hq, Hkv, Sq, Sk,
+                    D, causal, scale, true, stream);
 }
 
 const char* attn_get_last_error(void) { return g_msg; }
@@ -637,6 +683,6 @@ int attn_selftest_bounded_wait(long long spin_cycles, void* stream) {
   return ok();
 }
 
-int attn_version(void) { return 104; }
+int attn_version(void) { return 105; }
 
 }  // extern "C"

@@ -58,11 +58,16 @@ struct DecodeParams {
   long long spin_limit;
   int* err_word;
   int* err_info;
+  // FP8 (E4M3 inputs): block scales as the quantiser writes them, or nullptr = 1
+  const float* q_scale; // [B, Hq, nqb]
+  const float* k_scale; // [B, Hkv, nkb]
+  const float* v_scale; // [B, Hkv, nkb]
+  int nqb, nkb;         // ceil(Sq / 128), ceil(Sk / 128)
 };
 
-// tq: the 5-D [B, Sq, Hkv, G, D] view of Q (box {64, G, 1, Sq, 1}); tk, tv: [B, Sk, Hkv, D].
+// tq: the 5-D [B, Sq, Hkv, G, D] view of Q (box {one panel, G, 1, Sq, 1}); tk, tv: [B, Sk, Hkv, D].
 cudaError_t launch_attn_decode(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                               const DecodeParams& p, int D, bool causal, cudaStream_t st);
+                               const DecodeParams& p, int D, bool fp8, bool causal, cudaStream_t st);
 
 // Backward pass (attn_bwd.cu).
 struct BwdParams {

@@ -126,6 +126,27 @@ def attn_decode(q, k, v, causal=False, scale=0.0, out=None, lse=None, want_lse=T
     return out, lse
 
 
+def attn_decode_fp8(q8, k8, v8, q_scale, k_scale, v_scale, causal=False, scale=0.0, out=None, lse=None,
+                    want_lse=True, workspace=None, stream=None):
+    """Decoding on E4M3 codes: q8 [B, Sq, Hq, D], k8, v8 [B, Sk, Hkv, D] (uint8 or float8_e4m3fn)
+    with fp32 block scales [B, Hq, ceil(Sq/128)] and [B, Hkv, ceil(Sk/128)] -> (o bf16, lse)."""
+    _check4(q8, k8, v8)
+    B, Sq, Hq, D = q8.shape
+    Sk, Hkv = k8.shape[1], k8.shape[2]
+    nbytes = _lib.load().attn_decode_workspace_bytes(B, Hq, Hkv, Sq, Sk, D)
+    if workspace is None and nbytes > 0:
+        workspace = torch.empty(nbytes // 4, dtype=torch.float32, device=q8.device)
+    if out is None:
+        out = torch.empty((B, Sq, Hq, D), dtype=torch.bfloat16, device=q8.device)
+    if lse is None and want_lse:
+        lse = torch.empty((B, Hq, Sq), dtype=torch.float32, device=q8.device)
+    wsb = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _lib.call("attn_decode_fp8", _ptr(q8), _ptr(k8), _ptr(v8), _ptr(q_scale), _ptr(k_scale), _ptr(v_scale),
+              _ptr(out), _ptr(lse), _ptr(workspace), wsb, B, Hq, Hkv, Sq, Sk, D, int(bool(causal)), float(scale),
+              _stream(stream))
+    return out, lse
+
+
 def attn_bwd(q, k, v, o, lse, dout, causal=False, scale=0.0, dq=None, dk=None, dv=None, workspace=None,
              stream=None):
     """Gradients (dq, dk, dv) bf16 [B, S, H, D] of attn_fwd from its output o and lse."""

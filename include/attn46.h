@@ -152,6 +152,27 @@ int attn_decode(const void* q, const void* k, const void* v, void* o, float* lse
                 float scale, void* stream);
 
 /*
+ * attn_decode_fp8 -- attn_decode on E4M3 inputs with per-block scales: the
+ *   FP8 path of [HADA] "Niedrige FP8-Präzision und incoherent processing"
+ *   (block quantisation of the rotated Q and K) applied to a decoding step,
+ *   so that a step streams one byte per cached element instead of two.
+ *   q8   : [B, Sq, Hq, D] E4M3 bytes.   k8, v8 : [B, Sk, Hkv, D] E4M3 bytes.
+ *   q_scale : [B, Hq, ceil(Sq/128)] fp32; k_scale, v_scale : [B, Hkv,
+ *             ceil(Sk/128)] fp32; an element's value is code * its block's
+ *             scale -- the layout hadamard_rotate_quant_fp8 writes, so the
+ *             key/value cache is quantised by (b, key/value head, 128-token
+ *             block).  All three non-null, 4-byte aligned, device memory.
+ *   Q and K rotated by the same signs (or neither) give the same logits.
+ *   o, lse, workspace (attn_decode_workspace_bytes), shapes, the mask and the
+ *   errors as attn_decode.  The numerators of P reach the tensor core as E4M3,
+ *   as in attn_fwd_fp8.
+ */
+int attn_decode_fp8(const void* q8, const void* k8, const void* v8, const float* q_scale,
+                    const float* k_scale, const float* v_scale, void* o, float* lse, float* workspace,
+                    size_t workspace_bytes, int B, int Hq, int Hkv, int Sq, int Sk, int D, int causal,
+                    float scale, void* stream);
+
+/*
  * attn_bwd -- gradients dQ, dK, dV of attn_fwd (BF16), recomputed from the saved
  * log-sum-exp.
  *   The pages describe FlashAttention as tiling plus recomputation ([HADA]

@@ -40,7 +40,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_version(lib):
-    assert lib.attn_version() == 104
+    assert lib.attn_version() == 105
 
 
 FAKE = 1 << 20   # 16-byte aligned non-null fake device addresses: never dereferenced
@@ -160,3 +160,21 @@ def test_gqa_and_decode_reject_bad_arguments(lib):
         a[i] = val
         assert d(*a) == code, (i, val)
     assert lib.attn_decode_workspace_bytes(0, 8, 2, 1, 4096, 128) == 0
+
+
+def test_decode_fp8_rejects_bad_arguments(lib):
+    d = lib.attn_decode_fp8
+    ok = [FAKE, FAKE * 8, FAKE * 16, FAKE * 24, FAKE * 25, FAKE * 26, FAKE * 32, None, None, 0,
+          1, 8, 2, 1, 4096, 128, 0, 0.0, None]
+    for i, val, code in ((3, None, 1),           # q_scale missing
+                         (5, None, 1),           # v_scale missing
+                         (4, FAKE * 25 + 2, 1),  # k_scale misaligned
+                         (13, 5000, 1),          # Sq > Sk
+                         (13, 33, 2),            # G * Sq = 4 * 33 > 128
+                         (15, 256, 2),           # D = 256
+                         (15, 96, 2),            # D = 96
+                         (11, 6, 1),             # Hq not a multiple of Hkv
+                         (6, FAKE * 16, 1)):     # o aliases v
+        a = list(ok)
+        a[i] = val
+        assert d(*a) == code, (i, val)

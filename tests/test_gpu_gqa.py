@@ -1,9 +1,11 @@
 """Grouped-query attention (prefill) and decoding vs the fp64 oracle, through the C ABI (GPU).
 
 Same bounds as the BF16 forward tests (max error beyond half a bf16 ulp <= 1e-2, RMS <= 2e-3,
-lse <= 1e-3).  Decoding shapes cover one and several query tokens, group sizes 1 .. 16
-(G * Sq up to the 128-row tile), key counts below, at and above a tile, ragged tails, and
-enough keys for many key splits (the partial results then go through the merge kernel).
+lse <= 1e-3).  Decoding shapes cover one and several query tokens, group sizes 1 .. 32
+(G * Sq up to the 128-row tile; the kernel keeps 4, 2 or 1 copies of the packed rows for
+G * Sq <= 32, <= 64 and above, and 33 and 64 rows sit on those edges), key counts below, at and
+above a tile, ragged tails, and enough keys for many key splits (the partial results then go
+through the merge kernel).
 """
 
 import numpy as np
@@ -55,7 +57,8 @@ def test_gqa_with_one_group_per_head_is_attn_fwd():
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("B,Sq,Sk,Hq,Hkv", [
     (1, 1, 1, 8, 8), (2, 1, 100, 8, 2), (2, 1, 129, 32, 8), (1, 4, 1000, 16, 2), (3, 16, 300, 8, 1),
-    (2, 8, 4097, 16, 1), (1, 1, 65536, 4, 1), (4, 2, 20000, 32, 4), (1, 128, 2000, 1, 1)])
+    (2, 8, 4097, 16, 1), (1, 1, 65536, 4, 1), (4, 2, 20000, 32, 4), (1, 128, 2000, 1, 1),
+    (2, 6, 3000, 8, 1), (1, 2, 700, 32, 1), (1, 33, 500, 1, 1)])
 def test_decode(B, Sq, Sk, Hq, Hkv, D, causal):
     q, k, v = qkv(B, Sq, Sk, Hq, Hkv, D, case=72)
     dev = torch.device("cuda")
