@@ -348,6 +348,40 @@ int check_gqa_args(const void* q, const void* k, const void* v, const void* o, c
   return ATTN_OK;
 }
 
+// Grouped-query prefill: bf16 inputs (qs = ks = vs = nullptr) or E4M3 codes with block scales
+// (q_scale [B, Hq, nK], k_scale and v_scale [B, Hkv, nK]).
+int run_gqa(const void* q, const void* k, const void* v, const float* qs, const float* ks, const float* vs, void* o,
+            float* lse, int B, int Hq, int Hkv, int S, int D, int causal, float scale, bool fp8, void* stream) {
+  int rc = check_gqa_args(q, k, v, o, lse, B, Hq, Hkv, S, S, D, causal, scale, true, fp8 ? 1 : 2);
+  if (rc != ATTN_OK) return rc;
+  int* err = nullptr;
+  if ((rc = err_words(&err)) != ATTN_OK) return rc;
+  CUtensorMap tq, tk, tv;
+  if ((rc = make_qkv_map(&tq, q, B, S, Hq, D, fp8)) != ATTN_OK) return rc;
+  if ((rc = make_qkv_map(&tk, k, B, S, Hkv, D, fp8)) != ATTN_OK) return rc;
+  if ((rc = make_qkv_map(&tv, v, B, S, Hkv, D, fp8)) != ATTN_OK) return rc;
+  AttnParams p{};
+  p.B = B;
+  p.H = Hq;
+  p.S = S;
+  const int rows_per_cta = 128 * attn_q_tiles(D);
+  p.nQB = (S + rows_per_cta - 1) / rows_per_cta;
+  p.nK = (S + 127) / 128;
+  const float sc = scale > 0.f ? scale : 1.0f / std::sqrt(static_cast<float>(D));
+  p.c_log2 = sc * 1.4426950408889634f;
+  p.o = o;
+  p.lse = lse;
+  p.q_scale = qs;
+  p.k_scale = ks;
+  p.v_scale = vs;
+  p.spin_limit = spin_limit();
+  p.err_word = err;
+  p.err_info = err + 1;
+  p.kv_group = Hq / Hkv;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  return fp8 ? dispatch<true>(tq, tk, tv, p, D, causal, st) : dispatch<false>(tq, tk, tv, p, D, causal, st);
+}
+
 }  // namespace
 
 extern "C" {
@@ -526,30 +560,18 @@ int attn_bwd_noalloc(const void* q, const void* k, const void* v, const void* o,
 
 int attn_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int S,
                  int D, int causal, float scale, void* stream) {
-  int rc = check_gqa_args(q, k, v, o, lse, B, Hq, Hkv, S, S, D, causal, scale, true);
-  if (rc != ATTN_OK) return rc;
-  int* err = nullptr;
-  if ((rc = err_words(&err)) != ATTN_OK) return rc;
-  CUtensorMap tq, tk, tv;
-  if ((rc = make_qkv_map(&tq, q, B, S, Hq, D, false)) != ATTN_OK) return rc;
-  if ((rc = make_qkv_map(&tk, k, B, S, Hkv, D, false)) != ATTN_OK) return rc;
-  if ((rc = make_qkv_map(&tv, v, B, S, Hkv, D, false)) != ATTN_OK) return rc;
-  AttnParams p{};
-  p.B = B;
-  p.H = Hq;
-  p.S = S;
-  const int rows_per_cta = 128 * attn_q_tiles(D);
-  p.nQB = (S + rows_per_cta - 1) / rows_per_cta;
-  p.nK = (S + 127) / 128;
-  const float sc = scale > 0.f ? scale : 1.0f / std::sqrt(static_cast<float>(D));
-  p.c_log2 = sc * 1.4426950408889634f;
-  p.o = o;
-  p.lse = lse;
-  p.spin_limit = spin_limit();
-  p.err_word = err;
-  p.err_info = err + 1;
-  p.kv_group = Hq / Hkv;
-  return dispatch<false>(tq, tk, tv, p, D, causal, static_cast<cudaStream_t>(stream));
+  return run_gqa(q, k, v, nullptr, nullptr, nullptr, o, lse, B, Hq, Hkv, S, D, causal, scale, false, stream);
+}
+
+int attn_fwd_gqa_fp8(const void* q8, const void* k8, const void* v8, const float* q_scale, const float* k_scale,
+                     const float* v_scale, void* o, float* lse, int B, int Hq, int Hkv, int S, int D, int causal,
+                     float scale, void* stream) {
+  if (q_scale == nullptr || k_scale == nullptr || v_scale == nullptr)
+    return fail(ATTN_ERR_INVALID_ARG, "q_scale, k_scale and v_scale must be non-null");
+  if ((reinterpret_cast<uintptr_t>(q_scale) | reinterpret_cast<uintptr_t>(k_scale) |
+       reinterpret_cast<uintptr_t>(v_scale)) & 3u)
+    return fail(ATTN_ERR_INVALID_ARG, "scale arrays must be 4-byte aligned");
+  return run_gqa(q8, k8, v8, q_scale, k_scale, v_scale, o, lse, B, Hq, Hkv, S, D, causal, scale, true, stream);
 }
 
 size_t attn_decode_workspace_bytes(int B, int Hq, int Hkv, int Sq, int Sk, int D) {
@@ -683,6 +705,6 @@ int attn_selftest_bounded_wait(long long spin_cycles, void* stream) {
   return ok();
 }
 
-int attn_version(void) { return 105; }
+int attn_version(void) { return 106; }
 
 }  // extern "C"

@@ -290,12 +290,30 @@ __global__ void __launch_bounds__(DecCfg<D, FP8>::THREADS, 1)
         return x;
       }
     };
+    // FP8: the key and value scales of the split's tiles, 32 tiles at a time in the lanes'
+    // registers (lane i: tile 32 * n + i), the next 32 fetched a batch ahead, so that no global
+    // load sits between one tile's P hand-off and the next tile's S
+    float sk_cur = 1.f, sv_cur = 1.f, sk_nxt = 1.f, sv_nxt = 1.f;
+    auto fetch_scales = [&](int j0, float& skr, float& svr) {
+      const int jj = j0 + static_cast<int>(lane);
+      skr = (p.k_scale != nullptr && jj < ntile) ? p.k_scale[kv_blk + t0 + jj] : 1.f;
+      svr = (p.v_scale != nullptr && jj < ntile) ? p.v_scale[kv_blk + t0 + jj] : 1.f;
+    };
+    if (FP8) {
+      fetch_scales(0, sk_cur, sv_cur);
+      fetch_scales(32, sk_nxt, sv_nxt);
+    }
     for (int j = 0; j < ntile; ++j) {
       const int kb = 128 * (t0 + j);
       float cmul = p.c_log2, bias = 0.f, inv_r = 1.f;
       if (FP8) {
-        const float sk = p.k_scale != nullptr ? p.k_scale[kv_blk + t0 + j] : 1.f;
-        const float sv = p.v_scale != nullptr ? p.v_scale[kv_blk + t0 + j] : 1.f;
+        if (j > 0 && (j & 31) == 0) {
+          sk_cur = sk_nxt;
+          sv_cur = sv_nxt;
+          fetch_scales(j + 32, sk_nxt, sv_nxt);
+        }
+        const float sk = __shfl_sync(0xffffffffu, sk_cur, j & 31);
+        const float sv = __shfl_sync(0xffffffffu, sv_cur, j & 31);
         cmul = cq * sk;
         bias = __log2f(sv / sv_max);
         inv_r = sv_max / sv;

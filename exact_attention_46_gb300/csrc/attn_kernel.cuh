@@ -532,13 +532,15 @@ __global__ void __launch_bounds__(AttnCfg<D, FP8>::THREADS, 1)
       if (nt == 0) continue;
       const int row = it.q0 + 128 * t + row_local;
       const size_t blk_base = static_cast<size_t>(it.hb) * p.nK;   // (b*H + h) * nK
+      // the K/V block scales belong to the shared key/value head: (b * Hkv + h / G) * nK
+      const size_t kv_base = static_cast<size_t>(it.b * (p.H / p.kv_group) + it.h / p.kv_group) * p.nK;
 
       float sq = 1.f, sv_max = 1.f;
       if (FP8) {
         if (p.q_scale != nullptr) sq = p.q_scale[blk_base + (it.q0 + 128 * t) / 128];
         if (p.v_scale != nullptr) {
           sv_max = 0.f;
-          for (int j = static_cast<int>(lane); j < p.nK; j += 32) sv_max = fmaxf(sv_max, p.v_scale[blk_base + j]);
+          for (int j = static_cast<int>(lane); j < p.nK; j += 32) sv_max = fmaxf(sv_max, p.v_scale[kv_base + j]);
 #pragma unroll
           for (int o = 16; o > 0; o >>= 1) sv_max = fmaxf(sv_max, __shfl_xor_sync(0xffffffffu, sv_max, o));
         }
@@ -550,8 +552,8 @@ __global__ void __launch_bounds__(AttnCfg<D, FP8>::THREADS, 1)
         // Per-tile FP8 scales are read before waiting for S, so the loads overlap the wait.
         float cmul = p.c_log2, bias = 0.f, inv_r = 1.f;
         if (FP8) {
-          const float sk = p.k_scale != nullptr ? p.k_scale[blk_base + j] : 1.f;
-          const float sv = p.v_scale != nullptr ? p.v_scale[blk_base + j] : 1.f;
+          const float sk = p.k_scale != nullptr ? p.k_scale[kv_base + j] : 1.f;
+          const float sv = p.v_scale != nullptr ? p.v_scale[kv_base + j] : 1.f;
           cmul *= sq * sk;
           bias = __log2f(sv / sv_max);
           inv_r = sv_max / sv;

@@ -108,6 +108,22 @@ def attn_fwd_gqa(q, k, v, causal=False, scale=0.0, out=None, lse=None, want_lse=
     return out, lse
 
 
+def attn_fwd_gqa_fp8(q8, k8, v8, q_scale, k_scale, v_scale, causal=False, scale=0.0, out=None, lse=None,
+                     want_lse=True, stream=None):
+    """Grouped-query attention on E4M3 codes: q8 [B, S, Hq, D], k8, v8 [B, S, Hkv, D] with fp32
+    block scales [B, Hq, ceil(S/128)] and [B, Hkv, ceil(S/128)] -> (o bf16, lse [B, Hq, S])."""
+    _check4(q8, k8, v8)
+    B, S, Hq, D = q8.shape
+    Hkv = k8.shape[2]
+    if out is None:
+        out = torch.empty((B, S, Hq, D), dtype=torch.bfloat16, device=q8.device)
+    if lse is None and want_lse:
+        lse = torch.empty((B, Hq, S), dtype=torch.float32, device=q8.device)
+    _lib.call("attn_fwd_gqa_fp8", _ptr(q8), _ptr(k8), _ptr(v8), _ptr(q_scale), _ptr(k_scale), _ptr(v_scale),
+              _ptr(out), _ptr(lse), B, Hq, Hkv, S, D, int(bool(causal)), float(scale), _stream(stream))
+    return out, lse
+
+
 def attn_decode(q, k, v, causal=False, scale=0.0, out=None, lse=None, want_lse=True, workspace=None, stream=None):
     """Decoding: q [B, Sq, Hq, D] against k, v [B, Sk, Hkv, D] bf16 -> (o, lse [B, Hq, Sq])."""
     _check4(q, k, v)

@@ -131,6 +131,21 @@ int attn_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* ls
                  int Hq, int Hkv, int S, int D, int causal, float scale, void* stream);
 
 /*
+ * attn_fwd_gqa_fp8 -- attn_fwd_fp8 with grouped key/value heads: the FP8 path of
+ *   [HADA] "Niedrige FP8-Präzision und incoherent processing" with the grouping
+ *   of attn_fwd_gqa.
+ *   q8 : [B, S, Hq, D] E4M3 bytes, q_scale [B, Hq, ceil(S/128)] fp32.
+ *   k8, v8 : [B, S, Hkv, D] E4M3 bytes, k_scale, v_scale [B, Hkv, ceil(S/128)]
+ *   fp32 (the layout hadamard_rotate_quant_fp8 writes for each tensor).
+ *   o : [B, S, Hq, D] bf16.   lse : [B, Hq, S] fp32 or NULL.
+ *   Hq a positive multiple of Hkv; scales non-null and 4-byte aligned; other
+ *   arguments and errors as attn_fwd_fp8.
+ */
+int attn_fwd_gqa_fp8(const void* q8, const void* k8, const void* v8, const float* q_scale,
+                     const float* k_scale, const float* v_scale, void* o, float* lse, int B, int Hq,
+                     int Hkv, int S, int D, int causal, float scale, void* stream);
+
+/*
  * attn_decode -- attention of Sq query tokens against Sk >= Sq keys with
  *   grouped key/value heads: decoding (Sq = 1) and short query blocks.
  *   The queries are the last Sq positions: under the causal mask query i sees

@@ -40,7 +40,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_version(lib):
-    assert lib.attn_version() == 105
+    assert lib.attn_version() == 106
 
 
 FAKE = 1 << 20   # 16-byte aligned non-null fake device addresses: never dereferenced
@@ -160,6 +160,21 @@ def test_gqa_and_decode_reject_bad_arguments(lib):
         a[i] = val
         assert d(*a) == code, (i, val)
     assert lib.attn_decode_workspace_bytes(0, 8, 2, 1, 4096, 128) == 0
+
+
+def test_gqa_fp8_rejects_bad_arguments(lib):
+    g = lib.attn_fwd_gqa_fp8
+    ok = [FAKE, FAKE * 2, FAKE * 3, FAKE * 4, FAKE * 5, FAKE * 6, FAKE * 8, None, 1, 8, 2, 256, 128, 0, 0.0, None]
+    for i, val, code in ((3, None, 1),            # q_scale missing
+                         (5, FAKE * 6 + 1, 1),    # v_scale misaligned
+                         (9, 3, 1),               # Hq not a multiple of Hkv
+                         (10, 0, 1),              # Hkv = 0
+                         (12, 96, 2),             # D = 96
+                         (0, None, 1),            # q8 missing
+                         (6, FAKE * 2, 1)):       # o aliases k8
+        a = list(ok)
+        a[i] = val
+        assert g(*a) == code, (i, val)
 
 
 def test_decode_fp8_rejects_bad_arguments(lib):

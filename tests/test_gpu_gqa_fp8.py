@@ -1,6 +1,7 @@
-"""FP8 decoding vs the fp64 oracle, through the C ABI (GPU).
+"""FP8 grouped-query attention -- prefill (attn_fwd_gqa_fp8) and decoding (attn_decode_fp8) --
+vs the fp64 oracle, through the C ABI (GPU).
 
-The kernel gets the oracle's own E4M3 codes and block scales (Q and K rotated by the same
+The kernels get the oracle's own E4M3 codes and block scales (Q and K rotated by the same
 random signs, V not rotated), so both sides see the same inputs.  O_deq is exact grouped
 attention on the de-quantised values and O_emul the oracle's FP8 reading, which also rounds
 the softmax numerators to E4M3 (relative to the exact row max; the kernel rounds relative to
@@ -46,13 +47,13 @@ def quantised(x, signs):
     return r["codes"], sc32, quantise.dequantise(r["q"], sc32.astype(np.float64))
 
 
-def run(B, Sq, Sk, Hq, Hkv, D, causal, case, block_gain=False, rotate=True):
+def run(B, Sq, Sk, Hq, Hkv, D, causal, case, block_gain=False, rotate=True, fn=None):
     q, k, v = raw_inputs(B, Sq, Sk, Hq, Hkv, D, case, block_gain)
     s = synth.signs(D, synth.seed_for(case, synth.STREAM_SIGNS)).astype(np.float64) if rotate else None
     (q8, sq, qd), (k8, sk, kd), (v8, sv, vd) = quantised(q, s), quantised(k, s), quantised(v, None)
     dev = torch.device("cuda")
     t = [torch.from_numpy(np.ascontiguousarray(a)).to(dev) for a in (q8, k8, v8, sq, sk, sv)]
-    o, lse = ops.attn_decode_fp8(*t, causal=causal)
+    o, lse = (fn or ops.attn_decode_fp8)(*t, causal=causal)
     ops.check()
     O_deq, lse_deq = oracle_gqa.attention_gqa(qd, kd, vd, causal=causal)
     O_emul, _ = oracle_gqa.attention_gqa(qd, kd, vd, causal=causal, round_p=True)
@@ -70,6 +71,30 @@ def check(o, lse, O_deq, O_emul, lse_deq):
     assert e_gpu <= bound, (e_gpu, e_emul, bound)
     lse_err = float(np.abs(lse - lse_deq).max())
     assert lse_err <= LSE_TOL, lse_err
+
+
+@pytest.mark.parametrize("D", [64, 128, 256])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("S,Hkv", [(1, 1), (100, 1), (300, 2), (513, 8)])
+def test_gqa_fp8_prefill_matches_oracle(S, Hkv, D, causal):
+    check(*run(2, S, S, 8, Hkv, D, causal, case=85, fn=ops.attn_fwd_gqa_fp8))
+
+
+def test_gqa_fp8_prefill_block_scales_that_differ():
+    check(*run(1, 1000, 1000, 8, 2, 128, True, case=86, block_gain=True, fn=ops.attn_fwd_gqa_fp8))
+
+
+def test_gqa_fp8_with_one_group_per_head_is_attn_fwd_fp8():
+    B, S, H, D = 2, 700, 4, 128
+    q, k, v = raw_inputs(B, S, S, H, H, D, case=87)
+    dev = torch.device("cuda")
+    t = [torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+         for r in (quantised(q, None), quantised(k, None), quantised(v, None)) for a in r[:2]]
+    q8, sq, k8, sk, v8, sv = t
+    a, la = ops.attn_fwd_gqa_fp8(q8, k8, v8, sq, sk, sv, causal=True)
+    b, lb = ops.attn_fwd_fp8(q8, k8, v8, sq, sk, sv, causal=True)
+    ops.check()
+    assert torch.equal(a, b) and torch.equal(la, lb)
 
 
 @pytest.mark.parametrize("D", [64, 128])
