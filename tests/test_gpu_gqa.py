@@ -58,7 +58,8 @@ def test_gqa_with_one_group_per_head_is_attn_fwd():
 @pytest.mark.parametrize("B,Sq,Sk,Hq,Hkv", [
     (1, 1, 1, 8, 8), (2, 1, 100, 8, 2), (2, 1, 129, 32, 8), (1, 4, 1000, 16, 2), (3, 16, 300, 8, 1),
     (2, 8, 4097, 16, 1), (1, 1, 65536, 4, 1), (4, 2, 20000, 32, 4), (1, 128, 2000, 1, 1),
-    (2, 6, 3000, 8, 1), (1, 2, 700, 32, 1), (1, 33, 500, 1, 1)])
+    (2, 6, 3000, 8, 1), (1, 2, 700, 32, 1), (1, 33, 500, 1, 1),
+    (1, 17, 900, 1, 1), (2, 1, 3000, 16, 1)])
 def test_decode(B, Sq, Sk, Hq, Hkv, D, causal):
     q, k, v = qkv(B, Sq, Sk, Hq, Hkv, D, case=72)
     dev = torch.device("cuda")
