@@ -294,6 +294,43 @@ def sweep(dev):
     return out
 
 
+def long_context(dev, n=5):
+    """The long-context workload: B=1, H=16, D=128, S in {32K, 64K}, non-causal and causal,
+    BF16 and FP8 (Q and K rotated), TFLOPS by the same convention (causal counts half)."""
+    from exact_attention_46_gb300 import ops
+    out = []
+    for S in (32768, 65536):
+        g = torch.Generator(device=dev).manual_seed(S + 1)
+        q, k, v = (torch.randn((1, S, H, D), generator=g, device=dev, dtype=torch.float32).to(torch.bfloat16)
+                   for _ in range(3))
+        o = torch.empty_like(q)
+        lse = torch.empty((1, H, S), device=dev)
+        s = torch.where(torch.rand(D, generator=g, device=dev) < 0.5, -1.0, 1.0)
+        q8, sq = ops.hadamard_rotate_quant_fp8(q, s)
+        k8, sk = ops.hadamard_rotate_quant_fp8(k, s)
+        v8, sv = ops.hadamard_rotate_quant_fp8(v, None)
+        res = {"S": S, "B": 1}
+        for causal in (False, True):
+            for name, fn in (("bf16", lambda: ops.attn_fwd(q, k, v, causal=causal, out=o, lse=lse)),
+                             ("fp8", lambda: ops.attn_fwd_fp8(q8, k8, v8, sq, sk, sv, causal=causal, out=o,
+                                                             lse=lse))):
+                fn()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                torch.cuda.synchronize()
+                e0.record()
+                for _ in range(n):
+                    fn()
+                e1.record()
+                torch.cuda.synchronize()
+                ms = e0.elapsed_time(e1) / n
+                key = name + ("_causal" if causal else "") + "_tflops"
+                res[key] = round(attention_flops(1, H, S, D, causal) / ms / 1e9, 1)
+        ops.check()
+        out.append(res)
+        del q, k, v, o, q8, k8, v8
+    return out
+
+
 class OracleSample:
     """A bounded sample of the workload for the fp64 oracle: one head at the headline S.
 
@@ -562,6 +599,7 @@ def run_ours(args):
     vl = varlen_mix(dev) if (args.sweep and rank == 0) else None
     bw = backward_leg(dev) if (args.sweep and rank == 0) else None
     dc = decode_leg(dev) if (args.sweep and rank == 0) else None
+    lc = long_context(dev) if (args.sweep and rank == 0) else None
     peaks, peak_src = load_peaks()
     cpu = cpu_baseline_sample() if (rank == 0 and world == 1 and args.cpu_baseline) else None
 
@@ -619,6 +657,7 @@ def run_ours(args):
             "varlen": vl,
             "backward": bw,
             "decode": dc,
+            "long_context": lc,
         }
         print(json.dumps(line), flush=True)
     if dist_on:
@@ -657,7 +696,8 @@ def run_reference(args):
 
 
 # auxiliary legs, by name (bench.py --profile-leg NAME runs one of them alone)
-LEGS = {"varlen": varlen_mix, "rope": rope_fusion, "backward": backward_leg, "decode": decode_leg}
+LEGS = {"varlen": varlen_mix, "rope": rope_fusion, "backward": backward_leg, "decode": decode_leg,
+        "long": long_context}
 
 
 def main():

@@ -6,8 +6,9 @@ there the kernel's fp32 transform may land on either side, and the test checks t
 codes are the neighbouring grid values around that midpoint.
 
 FP8 attention: the only rounding the oracle's FP8 path has beyond the quantised inputs is the
-E4M3 rounding of the softmax numerators; the kernel rounds them relative to its running max
-rather than the exact row max, so the two roundings are independent draws of the same size.
+E4M3 rounding of the softmax numerators, with V's block ratios sv_j / max sv folded in as the
+kernel folds them (``fold_v``); the kernel rounds relative to its running max rather than the
+exact row max, so the two roundings are independent draws of the same size.
 The check: RMS(O_gpu - O_deq) <= 2 * RMS(O_emul - O_deq) + 1e-4, where O_deq is exact
 attention on the de-quantised inputs and O_emul the oracle's FP8 path; lse (which the
 rounding does not touch) within 1e-3 of the oracle's.
@@ -78,7 +79,7 @@ def run_fp8_path(q, k, v, s, causal):
 def oracle_fp8(q, k, v, s, causal, rows):
     s64 = None if s is None else s.astype(np.float64)
     O_emul, lse_emul, (Qq, Kq, Vq) = fp8_path.fp8_attention(to64(q), to64(k), to64(v), s64,
-                                                            causal=causal, rows=rows)
+                                                            causal=causal, rows=rows, fold_v=True)
     qd = quantise.dequantise(Qq["q"], Qq["scale"])
     kd = quantise.dequantise(Kq["q"], Kq["scale"])
     vd = quantise.dequantise(Vq["q"], Vq["scale"])
@@ -99,6 +100,37 @@ def test_fp8_attention_matches_oracle(B, S, H, D, rotate, causal):
     assert np.isfinite(to64(o)).all()
     assert e_gpu <= 2 * e_emul + 1e-4, (e_gpu, e_emul)
     assert np.abs(to64(lse) - lse_deq).max() <= 1e-3
+
+
+@pytest.mark.parametrize("S", [32768, 65536])
+def test_fp8_long_context(S):
+    # the long-context workload (B=1, H=16, D=128), non-causal and causal, checked on sampled
+    # query rows; each side quantises once and both masks use the result
+    B, H, D = 1, 16, 128
+    q, k, v = inputs(B, S, H, D, case=24)
+    s = signs_for(24, D)
+    dev = torch.device("cuda")
+    sd = torch.from_numpy(s).to(dev)
+    q8, sq = ops.hadamard_rotate_quant_fp8(q.to(dev), sd)
+    k8, sk = ops.hadamard_rotate_quant_fp8(k.to(dev), sd)
+    v8, sv = ops.hadamard_rotate_quant_fp8(v.to(dev), None)
+    Qq, Kq, Vq = fp8_path.quantise_qkv(to64(q), to64(k), to64(v), s.astype(np.float64))
+    qd = quantise.dequantise(Qq["q"], Qq["scale"])
+    kd = quantise.dequantise(Kq["q"], Kq["scale"])
+    vd = quantise.dequantise(Vq["q"], Vq["scale"])
+    rows = sample_rows(S, n_random=8)
+    ratio = fp8_path.v_block_ratio(Vq["scale"], S)
+    for causal in (False, True):
+        o, lse = ops.attn_fwd_fp8(q8, k8, v8, sq, sk, sv, causal=causal)
+        ops.check()
+        O_emul, _ = fp8_path.attention_rounded_p(qd, kd, vd, 1 / np.sqrt(D), causal, rows, v_ratio=ratio)
+        O_deq, lse_deq = fp8_path.attention_rounded_p(qd, kd, vd, 1 / np.sqrt(D), causal, rows, round_p=False)
+        og = to64(o)[:, rows]
+        _, e_gpu = stats(og, O_deq)
+        _, e_emul = stats(O_emul, O_deq)
+        assert np.isfinite(og).all()
+        assert e_gpu <= 2 * e_emul + 1e-4, (causal, e_gpu, e_emul)
+        assert np.abs(to64(lse)[:, :, rows] - lse_deq).max() <= 1e-3, causal
 
 
 def test_fp8_unit_scales_through_attn_fwd():
