@@ -496,8 +496,8 @@ def varlen_mix(dev, n=20):
     lse = torch.empty((H, TOKENS), dtype=torch.float32, device=dev)
     res = {"workload": f"{len(lens)} sequences, lengths U[128, 4096] summing to {TOKENS}, H={H} D={D}",
            "lengths": [int(x) for x in lens]}
-    for causal in (False, True):
-        fn = lambda: ops.attn_fwd_varlen(q, k, v, cu, int(lens.max()), causal=causal, out=o, lse=lse)
+
+    def timed(fn):
         for _ in range(3):
             fn()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -507,9 +507,20 @@ def varlen_mix(dev, n=20):
             fn()
         e1.record()
         torch.cuda.synchronize()
-        ms = e0.elapsed_time(e1) / n
+        return e0.elapsed_time(e1) / n
+
+    # the FP8 path: per-sequence blocks from the packed quantiser, Q and K rotated
+    sg = torch.from_numpy(synth.signs(D, synth.seed_for(2, synth.STREAM_SIGNS))).to(dev)
+    q8, sq = ops.hadamard_rotate_quant_fp8_varlen(q, cu, sg)
+    k8, sk = ops.hadamard_rotate_quant_fp8_varlen(k, cu, sg)
+    v8, sv = ops.hadamard_rotate_quant_fp8_varlen(v, cu, None)
+    for causal in (False, True):
         flops = sum(4 * int(x) * int(x) * H * D for x in lens) / (2 if causal else 1)
+        ms = timed(lambda: ops.attn_fwd_varlen(q, k, v, cu, int(lens.max()), causal=causal, out=o, lse=lse))
         res["causal_tflops" if causal else "tflops"] = round(flops / ms / 1e9, 1)
+        ms8 = timed(lambda: ops.attn_fwd_varlen_fp8(q8, k8, v8, sq, sk, sv, cu, int(lens.max()), causal=causal,
+                                                    out=o, lse=lse))
+        res["fp8_causal_tflops" if causal else "fp8_tflops"] = round(flops / ms8 / 1e9, 1)
     ops.check()
     return res
 

@@ -213,13 +213,16 @@ int run_attn(const void* q, const void* k, const void* v, const float* qs, const
              : dispatch<false>(tq, tk, tv, p, D, causal, st);
 }
 
-template <bool CAUSAL>
+template <bool FP8, bool CAUSAL>
 cudaError_t launch_varlen(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                           const AttnParams& p, int D, cudaStream_t st) {
-  return D == 64    ? launch_attn<64, false, CAUSAL, true>(tq, tk, tv, p, st)
-         : D == 128 ? launch_attn<128, false, CAUSAL, true>(tq, tk, tv, p, st)
-                    : launch_attn<256, false, CAUSAL, true>(tq, tk, tv, p, st);
+  return D == 64    ? launch_attn<64, FP8, CAUSAL, true>(tq, tk, tv, p, st)
+         : D == 128 ? launch_attn<128, FP8, CAUSAL, true>(tq, tk, tv, p, st)
+                    : launch_attn<256, FP8, CAUSAL, true>(tq, tk, tv, p, st);
 }
+
+// Scale entries per head of a packed batch's block scales.
+long long varlen_scale_blocks(long long total, long long n_seq) { return total / 128 + n_seq + 1; }
 
 // One thread waits on a barrier that nothing arrives at; the bounded wait records a timeout.
 __global__ void selftest_wait_kernel(long long limit, int* err) {
@@ -239,7 +242,7 @@ __global__ void selftest_wait_kernel(long long limit, int* err) {
 }
 
 int run_quant(const void* x, const float* rope_cs, int n_pos, void* out, float* scale, const float* signs,
-              int B, int H, int S, int D, void* stream) {
+              int B, int H, int S, int D, void* stream, const int* cu_seqlens = nullptr, int n_seq = 0) {
   if (x == nullptr || out == nullptr || scale == nullptr)
     return fail(ATTN_ERR_INVALID_ARG, "x, out and scale must be non-null device pointers");
   if (B < 1 || H < 1 || S < 1)
@@ -251,9 +254,10 @@ int run_quant(const void* x, const float* rope_cs, int n_pos, void* out, float* 
       (rope_cs != nullptr && !aligned16(rope_cs)) || (reinterpret_cast<uintptr_t>(scale) & 3u))
     return fail(ATTN_ERR_INVALID_ARG, "x, out, signs, rope_cs must be 16-byte and scale 4-byte aligned");
   const unsigned long long n = 1ull * B * S * H * D;
-  const int nblk = (S + 127) / 128;
-  if (n > (1ull << 40) / 2 || nblk > 0x7fffffff || H > 65535 || B > 65535)
+  const long long nblk_ll = cu_seqlens != nullptr ? varlen_scale_blocks(S, n_seq) : (S + 127) / 128;
+  if (n > (1ull << 40) / 2 || nblk_ll * H * B >= 0x7fffffffll || H > 65535 || B > 65535)
     return fail(ATTN_ERR_INVALID_ARG, "tensor too large for the grid");
+  const int nblk = static_cast<int>(nblk_ll);
   if (rope_cs != nullptr && n_pos < 128 * nblk)
     return fail(ATTN_ERR_INVALID_ARG,
                 "the rotary table needs rows for every position of the last 128-token block: "
@@ -261,6 +265,9 @@ int run_quant(const void* x, const float* rope_cs, int n_pos, void* out, float* 
   const size_t sbytes = 4ull * B * H * nblk;
   if (overlap(out, n, x, 2 * n) || overlap(scale, sbytes, x, 2 * n) || overlap(scale, sbytes, out, n))
     return fail(ATTN_ERR_INVALID_ARG, "outputs overlap the input or each other");
+  if (cu_seqlens != nullptr &&
+      (overlap(out, n, cu_seqlens, 4ull * (n_seq + 1)) || overlap(scale, sbytes, cu_seqlens, 4ull * (n_seq + 1))))
+    return fail(ATTN_ERR_INVALID_ARG, "outputs overlap cu_seqlens");
   if (rope_cs != nullptr) {
     const size_t tbytes = 4ull * n_pos * D;
     if (overlap(out, n, rope_cs, tbytes) || overlap(scale, sbytes, rope_cs, tbytes))
@@ -272,7 +279,7 @@ int run_quant(const void* x, const float* rope_cs, int n_pos, void* out, float* 
   CUtensorMap tx, tout;
   if ((rc = make_qkv_map(&tx, x, B, S, H, D, false)) != ATTN_OK) return rc;
   if ((rc = make_qkv_map(&tout, out, B, S, H, D, true)) != ATTN_OK) return rc;
-  QuantParams p{B, H, S, nblk, out, scale, signs, rope_cs, spin_limit(), err, err + 1};
+  QuantParams p{B, H, S, nblk, out, scale, signs, rope_cs, spin_limit(), err, err + 1, cu_seqlens, n_seq};
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e = D == 64    ? launch_hadamard_quant<64>(tx, tout, p, st)
                   : D == 128 ? launch_hadamard_quant<128>(tx, tout, p, st)
@@ -431,13 +438,20 @@ int rope_cos_sin_table(float* cs, int n_pos, int D, double base, void* stream) {
   return ok();
 }
 
-int attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse, const int* cu_seqlens,
-                    int n_seq, int total, int max_seqlen, int H, int D, int causal, float scale, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// Packed variable-length batches: bf16 inputs (qs = ks = vs = nullptr) or E4M3 codes with the
+// block scales of hadamard_rotate_quant_fp8_varlen ([H, varlen_scale_blocks(total, n_seq)]).
+int run_varlen(const void* q, const void* k, const void* v, const float* qs, const float* ks, const float* vs,
+               void* o, float* lse, const int* cu_seqlens, int n_seq, int total, int max_seqlen, int H, int D,
+               int causal, float scale, bool fp8, void* stream) {
   if (cu_seqlens == nullptr || (reinterpret_cast<uintptr_t>(cu_seqlens) & 3u))
     return fail(ATTN_ERR_INVALID_ARG, "cu_seqlens must be a non-null, 4-byte aligned device pointer");
   if (n_seq < 1 || n_seq > VARLEN_MAX_SEQ)
     return fail(ATTN_ERR_INVALID_ARG, "n_seq must be in [1, %d] (got %d)", VARLEN_MAX_SEQ, n_seq);
-  int rc = check_attn_args(q, k, v, o, lse, 1, H, total, D, causal, scale, 2);
+  int rc = check_attn_args(q, k, v, o, lse, 1, H, total, D, causal, scale, fp8 ? 1 : 2);
   if (rc != ATTN_OK) return rc;
   const int rows_per_cta = 128 * attn_q_tiles(D);
   if (max_seqlen < 1)
@@ -455,9 +469,9 @@ int attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float*
   int* err = nullptr;
   if ((rc = err_words(&err)) != ATTN_OK) return rc;
   CUtensorMap tq, tk, tv;
-  if ((rc = make_qkv_map(&tq, q, 1, total, H, D, false)) != ATTN_OK) return rc;
-  if ((rc = make_qkv_map(&tk, k, 1, total, H, D, false)) != ATTN_OK) return rc;
-  if ((rc = make_qkv_map(&tv, v, 1, total, H, D, false)) != ATTN_OK) return rc;
+  if ((rc = make_qkv_map(&tq, q, 1, total, H, D, fp8)) != ATTN_OK) return rc;
+  if ((rc = make_qkv_map(&tk, k, 1, total, H, D, fp8)) != ATTN_OK) return rc;
+  if ((rc = make_qkv_map(&tv, v, 1, total, H, D, fp8)) != ATTN_OK) return rc;
   AttnParams p{};
   p.B = 1;
   p.H = H;
@@ -474,10 +488,53 @@ int attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float*
   p.kv_group = 1;
   p.max_seqlen = max_seqlen;
   p.n_levels = (max_seqlen + rows_per_cta - 1) / rows_per_cta;
+  p.q_scale = qs;
+  p.k_scale = ks;
+  p.v_scale = vs;
+  p.scale_stride = static_cast<int>(varlen_scale_blocks(total, n_seq));
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const cudaError_t e = causal ? launch_varlen<true>(tq, tk, tv, p, D, st) : launch_varlen<false>(tq, tk, tv, p, D, st);
+  cudaError_t e;
+  if (fp8) e = causal ? launch_varlen<true, true>(tq, tk, tv, p, D, st) : launch_varlen<true, false>(tq, tk, tv, p, D, st);
+  else e = causal ? launch_varlen<false, true>(tq, tk, tv, p, D, st) : launch_varlen<false, false>(tq, tk, tv, p, D, st);
   if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "kernel launch failed: %s", cudaGetErrorString(e));
   return ok();
+}
+
+}  // namespace
+
+extern "C" {
+
+int attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse, const int* cu_seqlens,
+                    int n_seq, int total, int max_seqlen, int H, int D, int causal, float scale, void* stream) {
+  return run_varlen(q, k, v, nullptr, nullptr, nullptr, o, lse, cu_seqlens, n_seq, total, max_seqlen, H, D, causal,
+                    scale, false, stream);
+}
+
+int attn_fwd_varlen_fp8(const void* q8, const void* k8, const void* v8, const float* q_scale, const float* k_scale,
+                        const float* v_scale, void* o, float* lse, const int* cu_seqlens, int n_seq, int total,
+                        int max_seqlen, int H, int D, int causal, float scale, void* stream) {
+  if (q_scale == nullptr || k_scale == nullptr || v_scale == nullptr)
+    return fail(ATTN_ERR_INVALID_ARG, "q_scale, k_scale and v_scale must be non-null");
+  if ((reinterpret_cast<uintptr_t>(q_scale) | reinterpret_cast<uintptr_t>(k_scale) |
+       reinterpret_cast<uintptr_t>(v_scale)) & 3u)
+    return fail(ATTN_ERR_INVALID_ARG, "scale arrays must be 4-byte aligned");
+  return run_varlen(q8, k8, v8, q_scale, k_scale, v_scale, o, lse, cu_seqlens, n_seq, total, max_seqlen, H, D,
+                    causal, scale, true, stream);
+}
+
+int attn_varlen_scale_blocks(int total, int n_seq) {
+  if (total < 0 || n_seq < 0) return 0;
+  const long long nb = varlen_scale_blocks(total, n_seq);
+  return nb > 0x7fffffffll ? 0 : static_cast<int>(nb);
+}
+
+int hadamard_rotate_quant_fp8_varlen(const void* x, void* out, float* scale, const float* signs,
+                                     const int* cu_seqlens, int n_seq, int total, int H, int D, void* stream) {
+  if (cu_seqlens == nullptr || (reinterpret_cast<uintptr_t>(cu_seqlens) & 3u))
+    return fail(ATTN_ERR_INVALID_ARG, "cu_seqlens must be a non-null, 4-byte aligned device pointer");
+  if (n_seq < 1 || n_seq > VARLEN_MAX_SEQ)
+    return fail(ATTN_ERR_INVALID_ARG, "n_seq must be in [1, %d] (got %d)", VARLEN_MAX_SEQ, n_seq);
+  return run_quant(x, nullptr, 0, out, scale, signs, 1, H, total, D, stream, cu_seqlens, n_seq);
 }
 
 size_t attn_bwd_workspace_bytes(int B, int H, int S) {
@@ -705,6 +762,6 @@ int attn_selftest_bounded_wait(long long spin_cycles, void* stream) {
   return ok();
 }
 
-int attn_version(void) { return 106; }
+int attn_version(void) { return 107; }
 
 }  // extern "C"

@@ -292,7 +292,8 @@ __global__ void __launch_bounds__(AttnCfg<D, FP8>::THREADS, 1)
   // An item: query rows q0 .. q0 + 128 NT - 1 of sequence (b, h), positions counted from the
   // sequence's first token.  VARLEN: the sequence is tokens s0 .. s0 + len - 1 of the packed
   // axis; otherwise it is batch b and len = S (read from the parameters, not kept).
-  struct Item { int h, b, q0, hb, nmax, s0, len; int n[NT]; };
+  // sb (VARLEN with FP8): the sequence's first scale block, cu[s] / 128 + s
+  struct Item { int h, b, q0, hb, nmax, s0, len, sb; int n[NT]; };
   auto seq_len = [&](const Item& it) {
     if constexpr (VARLEN) return it.len; else return p.S;
   };
@@ -329,6 +330,7 @@ __global__ void __launch_bounds__(AttnCfg<D, FP8>::THREADS, 1)
       it.b = 0;
       it.hb = it.h;
       it.s0 = s0;
+      it.sb = (s0 >> 7) + sq;
     } else {
       if (CAUSAL) {
         qb = p.nQB - 1 - item / HB;
@@ -531,16 +533,19 @@ __global__ void __launch_bounds__(AttnCfg<D, FP8>::THREADS, 1)
       const int nt = (r0 >= seq_len(it)) ? 0 : (CAUSAL ? (r0 / 128 + 1) : key_tiles(it));
       if (nt == 0) continue;
       const int row = it.q0 + 128 * t + row_local;
-      const size_t blk_base = static_cast<size_t>(it.hb) * p.nK;   // (b*H + h) * nK
-      // the K/V block scales belong to the shared key/value head: (b * Hkv + h / G) * nK
-      const size_t kv_base = static_cast<size_t>(it.b * (p.H / p.kv_group) + it.h / p.kv_group) * p.nK;
+      // FP8 block scales: (b*H + h) * nK; the K/V ones belong to the shared key/value head,
+      // (b * Hkv + h / G) * nK.  VARLEN: h * stride + the sequence's first block.
+      const size_t blk_base = VARLEN ? static_cast<size_t>(it.h) * p.scale_stride + it.sb
+                                     : static_cast<size_t>(it.hb) * p.nK;
+      const size_t kv_base = VARLEN ? blk_base
+                                    : static_cast<size_t>(it.b * (p.H / p.kv_group) + it.h / p.kv_group) * p.nK;
 
       float sq = 1.f, sv_max = 1.f;
       if (FP8) {
         if (p.q_scale != nullptr) sq = p.q_scale[blk_base + (it.q0 + 128 * t) / 128];
         if (p.v_scale != nullptr) {
           sv_max = 0.f;
-          for (int j = static_cast<int>(lane); j < p.nK; j += 32) sv_max = fmaxf(sv_max, p.v_scale[kv_base + j]);
+          for (int j = static_cast<int>(lane); j < key_tiles(it); j += 32) sv_max = fmaxf(sv_max, p.v_scale[kv_base + j]);
 #pragma unroll
           for (int o = 16; o > 0; o >>= 1) sv_max = fmaxf(sv_max, __shfl_xor_sync(0xffffffffu, sv_max, o));
         }
@@ -745,7 +750,6 @@ cudaError_t launch_attn(const CUtensorMap& tq, const CUtensorMap& tk, const CUte
   using C = AttnCfg<D, FP8>;
   constexpr int SMEM = C::SMEM_BYTES + (VARLEN ? VARLEN_SMEM_BYTES : 0);
   static_assert(SMEM <= 227 * 1024, "shared memory budget");
-  static_assert(!(VARLEN && FP8), "variable-length batches are BF16 only");
   static std::atomic<unsigned long long> configured{0};   // one bit per device
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);

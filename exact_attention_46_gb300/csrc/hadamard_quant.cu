@@ -30,6 +30,15 @@
 // bytes each, twice the block's own input), so the kernel rebuilds (cos, sin)(p theta_i) with
 // the angle-addition identity, as the complex product of table row 128 blk + 16 r1 (8 rows per
 // block, bulk-copied with the block) and table row r0 (16 rows, resident), r = 16 r1 + r0.
+//
+// Packed variable-length batches (VARLEN): x is [total, H, D] with sequence offsets cu_seqlens,
+// and a block never straddles two sequences -- sequence s is cut into 128-token blocks from its
+// own first token.  Block k of sequence s has scale index cu[s] / 128 + s + k (no two sequences
+// share one; at most one index per sequence stays unused), so a work item is (index, head) and
+// a binary search over the strictly increasing cu[s] / 128 + s finds its sequence.  Rows past
+// the sequence's end arrive with the box but count as zero; a whole block leaves by tensor
+// store, a partial one row by row from registers (a tensor store would overwrite the next
+// sequence's rows).  The offsets are checked before anything is written.
 #include <atomic>
 #include <cstdint>
 #include <cuda_bf16.h>
@@ -73,7 +82,8 @@ struct QCfg {
   static constexpr int OFF_BAR = OFF_SIGN + SIGN_BYTES;
   static constexpr int OFF_WMAX = OFF_BAR + 8 * NSTAGE;
   static constexpr int OFF_ABORT = OFF_WMAX + 2 * NWARPS * 4;
-  static constexpr int SMEM_BYTES = 1024 + OFF_ABORT + 16;
+  static constexpr int OFF_INFO = OFF_ABORT + 16;                          // VARLEN: [NSTAGE] (tok0, rows)
+  static constexpr int SMEM_BYTES = 1024 + OFF_INFO + 8 * NSTAGE;
   static constexpr uint32_t TX_BYTES = STAGE_BYTES + (ROPE ? NCOARSE * 4 * D : 0);
   // E4M3 codes of a block, staged in the consumed input stage for one tensor store per
   // 128-byte panel (64-byte rows, 64-byte swizzle at D = 64)
@@ -103,11 +113,12 @@ __device__ __forceinline__ void rotary_pair(float& v0, float& v1, float ac, floa
   v1 = x0 * s + x1 * c;
 }
 
-template <int D, bool ROTATE, bool ROPE>
+template <int D, bool ROTATE, bool ROPE, bool VARLEN>
 __global__ void __launch_bounds__(QCfg<D, ROPE>::THREADS, QCfg<D, ROPE>::CTAS_PER_SM)
     hadamard_quant_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmOut,
                           const QuantParams p) {
   using C = QCfg<D, ROPE>;
+  static_assert(!(VARLEN && ROPE), "no rotary embedding on packed batches");
   constexpr int VPT = C::VPT;
   constexpr int NSTAGE = C::NSTAGE;
   constexpr int NW = VPT / 8;         // 16-byte input chunks per thread
@@ -120,6 +131,7 @@ __global__ void __launch_bounds__(QCfg<D, ROPE>::THREADS, QCfg<D, ROPE>::CTAS_PE
   const uint32_t bar0 = base_u32 + C::OFF_BAR;
   float* warp_max = reinterpret_cast<float*>(base + C::OFF_WMAX);          // [2][NWARPS]
   volatile int* abort_flag = reinterpret_cast<volatile int*>(base + C::OFF_ABORT);
+  int2* stage_info = reinterpret_cast<int2*>(base + C::OFF_INFO);         // VARLEN: (tok0, rows)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // row and the part of it this thread owns: a warp holds RPW rows, lanes l, l + RPW, ... share
@@ -154,6 +166,17 @@ __global__ void __launch_bounds__(QCfg<D, ROPE>::THREADS, QCfg<D, ROPE>::CTAS_PE
       *reinterpret_cast<float2*>(base + C::OFF_FINE + f * C::TROW + 8 * i) = cs;
     }
   }
+  if constexpr (VARLEN) {
+    // offsets that are not 0 .. total, non-decreasing: nothing is written
+    bool bad = false;
+    for (int i = static_cast<int>(threadIdx.x); i < p.n_seq; i += C::THREADS)
+      bad |= p.cu_seqlens[i + 1] < p.cu_seqlens[i];
+    if (threadIdx.x == 0) bad |= p.cu_seqlens[0] != 0 || p.cu_seqlens[p.n_seq] != p.S;
+    if (__syncthreads_or(bad)) {
+      if (threadIdx.x == 0 && atomicCAS(p.err_word, 0, 1 /* ATTN_ERR_INVALID_ARG */) == 0) atomicExch(p.err_info, 11);
+      return;
+    }
+  }
   __syncthreads();
   const WaitCtl ctl{p.spin_limit, abort_flag, p.err_word, p.err_info};
 
@@ -163,10 +186,29 @@ __global__ void __launch_bounds__(QCfg<D, ROPE>::THREADS, QCfg<D, ROPE>::CTAS_PE
     const int h = bi % p.H, blk = (bi / p.H) % p.nblk, b = bi / (p.H * p.nblk);
     const uint32_t st = base_u32 + (k % NSTAGE) * C::STAGE_BYTES;
     const uint32_t bar = bar0 + 8u * (k % NSTAGE);
+    int tok0 = blk * QROWS;
+    if constexpr (VARLEN) {
+      // the sequence of index blk: the last s with cu[s] / 128 + s <= blk (cu[0] / 128 + 0 = 0)
+      int lo = 0, hi = p.n_seq - 1;
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if ((p.cu_seqlens[mid] >> 7) + mid <= blk) lo = mid; else hi = mid - 1;
+      }
+      const int s0 = p.cu_seqlens[lo], len = p.cu_seqlens[lo + 1] - s0;
+      const int kb = blk - ((s0 >> 7) + lo);
+      const int rows = 128 * kb < len ? min(QROWS, len - 128 * kb) : 0;
+      tok0 = s0 + 128 * kb;
+      stage_info[k % NSTAGE] = make_int2(tok0, rows);
+      if (rows == 0) {                // an index no block lives at
+        mbar_arrive(bar);
+        n_issued = k + 1;
+        return;
+      }
+    }
     mbar_arrive_expect_tx(bar, C::TX_BYTES);
 #pragma unroll
     for (int pn = 0; pn < C::NPANEL; ++pn)
-      tma_load_4d(st + pn * C::PANEL_BYTES, &tmX, bar, 64 * pn, h, blk * QROWS, b,
+      tma_load_4d(st + pn * C::PANEL_BYTES, &tmX, bar, 64 * pn, h, tok0, b,
                   l2_policy_evict_first());
     if (ROPE) {
       // coarse rows 128 blk + 16 r1 into slot k % NCSLOT.  The slot last held block
@@ -194,6 +236,18 @@ __global__ void __launch_bounds__(QCfg<D, ROPE>::THREADS, QCfg<D, ROPE>::CTAS_PE
     const int stage = k % NSTAGE;
     const uint32_t st = base_u32 + stage * C::STAGE_BYTES;
     const bool ok = wait_bounded(bar0 + 8u * stage, (k / NSTAGE) & 1, ctl, 10);
+    int tok0 = blk * QROWS, rows = QROWS;
+    if constexpr (VARLEN) {
+      const int2 inf = stage_info[stage];
+      tok0 = inf.x;
+      rows = inf.y;
+      if (rows == 0) {
+        // nothing at this index: pass the stage on once every thread has read its info
+        if (__syncthreads_or(!ok)) break;
+        if (threadIdx.x == 0 && k + NSTAGE < my_blocks) issue(k + NSTAGE);
+        continue;
+      }
+    }
 
     float v[VPT];
 #pragma unroll
@@ -213,6 +267,11 @@ __global__ void __launch_bounds__(QCfg<D, ROPE>::THREADS, QCfg<D, ROPE>::CTAS_PE
         v[8 * c + 2 * q] = __uint_as_float(w[q] << 16);
         v[8 * c + 2 * q + 1] = __uint_as_float(w[q] & 0xFFFF0000u);
       }
+    }
+
+    if (VARLEN && r >= rows) {        // the next sequence's row (or past the end): not this block's
+#pragma unroll
+      for (int e = 0; e < VPT; ++e) v[e] = 0.f;
     }
 
     // Every thread has its values in registers; the stage now takes this block's codes.
@@ -307,6 +366,14 @@ __global__ void __launch_bounds__(QCfg<D, ROPE>::THREADS, QCfg<D, ROPE>::CTAS_PE
           wq[q] = pack_e4m3x4(y[0], y[1], y[2], y[3]);
         }
         const int idx = part * VPT + 16 * c;                          // byte in the code row
+        if (VARLEN && rows < QROWS) {
+          // a partial block: the row straight to global memory, rows past the sequence not at all
+          if (r < rows)
+            *reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.out) +
+                                      (static_cast<size_t>(tok0 + r) * p.H + h) * D + idx) =
+                make_uint4(wq[0], wq[1], wq[2], wq[3]);
+          continue;
+        }
         const int pn = idx / C::CODE_PANEL, cc = (idx % C::CODE_PANEL) / 16;
         const int sw = C::CODE_PANEL == 128 ? (r & 7) : ((r >> 1) & 3);
         const uint32_t addr = st + pn * (QROWS * C::CODE_PANEL) + r * C::CODE_PANEL + ((cc ^ sw) << 4);
@@ -318,12 +385,14 @@ __global__ void __launch_bounds__(QCfg<D, ROPE>::THREADS, QCfg<D, ROPE>::CTAS_PE
     fence_proxy_async_smem();
     __syncthreads();
     if (threadIdx.x == 0) {
+      if (rows == QROWS) {
 #pragma unroll
-      for (int pn = 0; pn < C::NCPANEL; ++pn)
-        tma_store_4d(&tmOut, st + pn * (QROWS * C::CODE_PANEL), pn * C::CODE_PANEL, h, blk * QROWS, b);
-      bulk_commit_group();
-      // the stage is free once the store has read it: refill it for block k + NSTAGE
-      bulk_wait_read_all();
+        for (int pn = 0; pn < C::NCPANEL; ++pn)
+          tma_store_4d(&tmOut, st + pn * (QROWS * C::CODE_PANEL), pn * C::CODE_PANEL, h, tok0, b);
+        bulk_commit_group();
+        // the stage is free once the store has read it: refill it for block k + NSTAGE
+        bulk_wait_read_all();
+      }
       if (k + NSTAGE < my_blocks) issue(k + NSTAGE);
     }
   }
@@ -343,20 +412,20 @@ __global__ void __launch_bounds__(QCfg<D, ROPE>::THREADS, QCfg<D, ROPE>::CTAS_PE
   }
 }
 
-template <int D, bool ROTATE, bool ROPE>
+template <int D, bool ROTATE, bool ROPE, bool VARLEN = false>
 cudaError_t launch_variant(const CUtensorMap& tx, const CUtensorMap& tout, const QuantParams& p, int sm_count,
                            cudaStream_t stream) {
   using C = QCfg<D, ROPE>;
   const long long nblocks = static_cast<long long>(p.nblk) * p.H * p.B;
   const long long cap = static_cast<long long>(sm_count) * C::CTAS_PER_SM;
   const unsigned grid = static_cast<unsigned>(nblocks < cap ? nblocks : cap);
-  hadamard_quant_kernel<D, ROTATE, ROPE><<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(tx, tout, p);
+  hadamard_quant_kernel<D, ROTATE, ROPE, VARLEN><<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(tx, tout, p);
   return cudaGetLastError();
 }
 
-template <int D, bool ROTATE, bool ROPE>
+template <int D, bool ROTATE, bool ROPE, bool VARLEN = false>
 cudaError_t set_smem() {
-  return cudaFuncSetAttribute(hadamard_quant_kernel<D, ROTATE, ROPE>,
+  return cudaFuncSetAttribute(hadamard_quant_kernel<D, ROTATE, ROPE, VARLEN>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize, QCfg<D, ROPE>::SMEM_BYTES);
 }
 
@@ -376,6 +445,8 @@ cudaError_t launch_hadamard_quant(const CUtensorMap& tx, const CUtensorMap& tout
     if ((e = set_smem<D, false, false>()) != cudaSuccess) return e;
     if ((e = set_smem<D, true, true>()) != cudaSuccess) return e;
     if ((e = set_smem<D, false, true>()) != cudaSuccess) return e;
+    if ((e = set_smem<D, true, false, true>()) != cudaSuccess) return e;
+    if ((e = set_smem<D, false, false, true>()) != cudaSuccess) return e;
     int n = 0;
     e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
@@ -384,6 +455,9 @@ cudaError_t launch_hadamard_quant(const CUtensorMap& tx, const CUtensorMap& tout
   }
   const int sms = sm_count[dev & 63];
   const bool rot = p.signs != nullptr, rope = p.rope_cs != nullptr;
+  if (p.cu_seqlens != nullptr)
+    return rot ? launch_variant<D, true, false, true>(tx, tout, p, sms, stream)
+               : launch_variant<D, false, false, true>(tx, tout, p, sms, stream);
   if (rope)
     return rot ? launch_variant<D, true, true>(tx, tout, p, sms, stream)
                : launch_variant<D, false, true>(tx, tout, p, sms, stream);

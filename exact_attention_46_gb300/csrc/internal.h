@@ -28,6 +28,9 @@ struct AttnParams {
   int n_levels;          // ceil(max_seqlen / query rows per CTA)
   // grouped-query attention: query head h reads key/value head h / kv_group (1 = plain)
   int kv_group;
+  // VARLEN with FP8: scale entries per head (total / 128 + n_seq + 1); the scale blocks of
+  // sequence s start at index cu[s] / 128 + s
+  int scale_stride;
 };
 
 // Sequences and query-block levels a variable-length launch may hold: each CTA keeps the
@@ -104,6 +107,11 @@ struct QuantParams {
   long long spin_limit; // cycles a bounded wait may spin
   int* err_word;        // device error word
   int* err_info;
+  // packed variable-length batch (B = 1, S = total tokens): blocks of 128 tokens start at
+  // every sequence's first token; block k of sequence s has scale index cu[s] / 128 + s + k,
+  // nblk = total / 128 + n_seq + 1 indices per head (scale [H, nblk]); nullptr = fixed length
+  const int* cu_seqlens;
+  int n_seq;
 };
 
 // x is read through `tx`, the same [B, S, H, D] bf16 tensor map the attention kernel uses;

@@ -94,6 +94,54 @@ def attn_fwd_varlen(q, k, v, cu_seqlens, max_seqlen=None, causal=False, scale=0.
     return out, lse
 
 
+def _check_cu(cu_seqlens):
+    if cu_seqlens.dtype != torch.int32 or not cu_seqlens.is_cuda or cu_seqlens.dim() != 1:
+        raise ValueError("cu_seqlens must be a 1-D int32 CUDA tensor")
+
+
+def varlen_scale_blocks(total, n_seq):
+    """Scale entries per head of a packed batch's block scales: total // 128 + n_seq + 1."""
+    return int(_lib.load().attn_varlen_scale_blocks(int(total), int(n_seq)))
+
+
+def hadamard_rotate_quant_fp8_varlen(x, cu_seqlens, signs=None, out=None, scale=None, stream=None):
+    """E4M3 codes (uint8 [total, H, D]) and block scales (fp32 [H, varlen_scale_blocks]) of a
+    packed bf16 batch x [total, H, D]; the blocks restart at every sequence's first token."""
+    if x.dim() != 3 or not x.is_cuda or not x.is_contiguous():
+        raise ValueError("x must be a contiguous CUDA tensor [total, H, D]")
+    _check_cu(cu_seqlens)
+    total, H, D = x.shape
+    n_seq = int(cu_seqlens.numel() - 1)
+    if out is None:
+        out = torch.empty((total, H, D), dtype=torch.uint8, device=x.device)
+    if scale is None:
+        scale = torch.empty((H, varlen_scale_blocks(total, n_seq)), dtype=torch.float32, device=x.device)
+    _lib.call("hadamard_rotate_quant_fp8_varlen", _ptr(x), _ptr(out), _ptr(scale), _ptr(signs), _ptr(cu_seqlens),
+              n_seq, total, H, D, _stream(stream))
+    return out, scale
+
+
+def attn_fwd_varlen_fp8(q8, k8, v8, q_scale, k_scale, v_scale, cu_seqlens, max_seqlen=None, causal=False,
+                        scale=0.0, out=None, lse=None, want_lse=True, stream=None):
+    """attn_fwd_varlen on E4M3 codes [total, H, D] with the block scales of
+    hadamard_rotate_quant_fp8_varlen -> (o [total, H, D] bf16, lse [H, total] fp32 or None)."""
+    for t in (q8, k8, v8):
+        if t.dim() != 3 or not t.is_cuda or not t.is_contiguous():
+            raise ValueError("q8, k8, v8 must be contiguous CUDA tensors [total, H, D]")
+    _check_cu(cu_seqlens)
+    total, H, D = q8.shape
+    if max_seqlen is None:
+        max_seqlen = max(1, int((cu_seqlens[1:] - cu_seqlens[:-1]).max().item()))
+    if out is None:
+        out = torch.empty((total, H, D), dtype=torch.bfloat16, device=q8.device)
+    if lse is None and want_lse:
+        lse = torch.empty((H, total), dtype=torch.float32, device=q8.device)
+    _lib.call("attn_fwd_varlen_fp8", _ptr(q8), _ptr(k8), _ptr(v8), _ptr(q_scale), _ptr(k_scale), _ptr(v_scale),
+              _ptr(out), _ptr(lse), _ptr(cu_seqlens), int(cu_seqlens.numel() - 1), total, int(max_seqlen), H, D,
+              int(bool(causal)), float(scale), _stream(stream))
+    return out, lse
+
+
 def attn_fwd_gqa(q, k, v, causal=False, scale=0.0, out=None, lse=None, want_lse=True, stream=None):
     """Grouped-query attention: q [B, S, Hq, D], k, v [B, S, Hkv, D] bf16 -> (o, lse [B, Hq, S])."""
     _check4(q, k, v)

@@ -119,6 +119,39 @@ int attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float*
                     int causal, float scale, void* stream);
 
 /*
+ * The FP8 path on packed variable-length batches: the rotation and block
+ *   quantisation of [HADA] "Niedrige FP8-Präzision und incoherent processing"
+ *   with the packed batches of [HADA] "Weitere Optimierungen und künftige
+ *   Integration".  Reading (the pages define neither the combination nor a
+ *   layout): a scale block never straddles two sequences -- sequence s is cut
+ *   into 128-token blocks from its own first token -- and the scales of all
+ *   sequences share one array [H, NB], NB = attn_varlen_scale_blocks(total,
+ *   n_seq) = total / 128 + n_seq + 1, block k of sequence s at index
+ *   cu_seqlens[s] / 128 + s + k (indices no block uses are left unwritten).
+ *
+ * attn_varlen_scale_blocks -- NB above (0 for negative arguments).
+ *
+ * hadamard_rotate_quant_fp8_varlen -- hadamard_rotate_quant_fp8 on a packed
+ *   batch: x [total, H, D] bf16 -> out [total, H, D] E4M3, scale [H, NB] fp32.
+ *   cu_seqlens as attn_fwd_varlen (device int32 [n_seq + 1], n_seq 1..4096);
+ *   offsets that are not 0 .. total, non-decreasing, make the launch write
+ *   nothing and leave ATTN_ERR_INVALID_ARG for attn_check().  No RoPE fusion.
+ *
+ * attn_fwd_varlen_fp8 -- attn_fwd_varlen on E4M3 codes with those scales
+ *   (q_scale, k_scale, v_scale [H, NB] fp32, non-null, 4-byte aligned); the
+ *   value scales enter as in attn_fwd_fp8, with the largest taken over the
+ *   sequence's own blocks.  Other arguments and errors as attn_fwd_varlen.
+ */
+int attn_varlen_scale_blocks(int total, int n_seq);
+int hadamard_rotate_quant_fp8_varlen(const void* x, void* out, float* scale, const float* signs,
+                                     const int* cu_seqlens, int n_seq, int total, int H, int D,
+                                     void* stream);
+int attn_fwd_varlen_fp8(const void* q8, const void* k8, const void* v8, const float* q_scale,
+                        const float* k_scale, const float* v_scale, void* o, float* lse,
+                        const int* cu_seqlens, int n_seq, int total, int max_seqlen, int H, int D,
+                        int causal, float scale, void* stream);
+
+/*
  * attn_fwd_gqa -- attn_fwd (BF16) with grouped key/value heads.
  *   The pages name LLM inference as future work ([HADA] "Weitere
  *   Optimierungen und künftige Integration"); grouped-query attention is

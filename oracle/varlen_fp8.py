@@ -44,8 +44,9 @@ def block_base(cu_seqlens):
 def quantise_varlen(x, cu_seqlens, signs=None):
     """Quantise packed x [total, H, D] (fp64 values) sequence by sequence.
 
-    Returns a dict with ``q`` (E4M3 values) and ``codes`` [total, H, D], ``scale`` [H, NB]
-    (NaN where no block lives), and ``deq``, the de-quantised values [total, H, D].
+    Returns a dict with ``q`` (E4M3 values), ``codes`` and ``pre`` (the value rounded, as in
+    ``quantise_blocks``) [total, H, D], ``scale`` [H, NB] (NaN where no block lives), and
+    ``deq``, the de-quantised values [total, H, D].
     """
     x = np.asarray(x, dtype=np.float64)
     total, H, D = x.shape
@@ -53,6 +54,7 @@ def quantise_varlen(x, cu_seqlens, signs=None):
     base = block_base(cu_seqlens)
     scale = np.full((H, scale_blocks(total, len(segs))), np.nan)
     q = np.zeros_like(x)
+    pre = np.zeros_like(x)
     codes = np.zeros(x.shape, dtype=np.uint8)
     deq = np.zeros_like(x)
     for s, (s0, n) in enumerate(segs):
@@ -62,9 +64,10 @@ def quantise_varlen(x, cu_seqlens, signs=None):
         nblk = r["scale"].shape[2]
         scale[:, base[s]:base[s] + nblk] = r["scale"][0]
         q[s0:s0 + n] = r["q"][0]
+        pre[s0:s0 + n] = r["pre"][0]
         codes[s0:s0 + n] = r["codes"][0]
         deq[s0:s0 + n] = dequantise(r["q"], r["scale"])[0]
-    return {"q": q, "codes": codes, "scale": scale, "deq": deq}
+    return {"q": q, "pre": pre, "codes": codes, "scale": scale, "deq": deq}
 
 
 def fp8_attention_varlen(qd, kd, vd, v_scale, cu_seqlens, scale, causal=False, round_p=True, fold_v=True):

@@ -40,7 +40,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_version(lib):
-    assert lib.attn_version() == 106
+    assert lib.attn_version() == 107
 
 
 FAKE = 1 << 20   # 16-byte aligned non-null fake device addresses: never dereferenced
@@ -160,6 +160,35 @@ def test_gqa_and_decode_reject_bad_arguments(lib):
         a[i] = val
         assert d(*a) == code, (i, val)
     assert lib.attn_decode_workspace_bytes(0, 8, 2, 1, 4096, 128) == 0
+
+
+def test_varlen_fp8_and_quantiser_reject_bad_arguments(lib):
+    assert lib.attn_varlen_scale_blocks(300, 3) == 300 // 128 + 3 + 1
+    assert lib.attn_varlen_scale_blocks(-1, 3) == 0
+    q = lib.hadamard_rotate_quant_fp8_varlen
+    ok = [FAKE, FAKE * 4, FAKE * 8, None, FAKE * 12, 3, 300, 2, 128, None]
+    for i, val, code in ((4, None, 1),          # cu_seqlens missing
+                         (4, FAKE * 12 + 2, 1), # misaligned
+                         (5, 0, 1),             # n_seq = 0
+                         (5, 5000, 1),          # n_seq above 4096
+                         (8, 96, 2),            # D = 96
+                         (1, FAKE, 1),          # out aliases x
+                         (2, None, 1)):         # scale missing
+        a = list(ok)
+        a[i] = val
+        assert q(*a) == code, (i, val)
+    f = lib.attn_fwd_varlen_fp8
+    ok = [FAKE, FAKE * 2, FAKE * 3, FAKE * 4, FAKE * 5, FAKE * 6, FAKE * 8, None, FAKE * 12, 3, 300, 200, 2, 128,
+          0, 0.0, None]
+    for i, val, code in ((3, None, 1),           # q_scale missing
+                         (5, FAKE * 6 + 1, 1),   # v_scale misaligned
+                         (8, None, 1),           # cu_seqlens missing
+                         (9, 0, 1),              # n_seq = 0
+                         (11, 0, 1),             # max_seqlen = 0
+                         (13, 96, 2)):           # D = 96
+        a = list(ok)
+        a[i] = val
+        assert f(*a) == code, (i, val)
 
 
 def test_gqa_fp8_rejects_bad_arguments(lib):
