@@ -257,8 +257,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       const float* l2 = dlt + 128;
       // the stage's Delta / lse came by TMA: acquire them from the stage's own barrier (its
       // phase cannot move on before this warp's P arrival releases the stage)
-      if (!wait_bounded(BAR_FULL(s), (i / NSTAGE) & 1, ctl, WHERE_BWD_COMPUTE)) { ok = false; break; }
-      if (!wait_bounded(BAR_S, i & 1, ctl, WHERE_BWD_COMPUTE)) { ok = false; break; }
+      if (!warp_wait(BAR_FULL(s), (i / NSTAGE) & 1, ctl, WHERE_BWD_COMPUTE)) { ok = false; break; }
+      if (!warp_wait(BAR_S, i & 1, ctl, WHERE_BWD_COMPUTE)) { ok = false; break; }
       tc_fence_after();
       // masks are needed only on the diagonal tile (causal) and the ragged last query tile
       const bool masked = (CAUSAL && j0 + i == kt) || q0 + 128 > p.S;
@@ -301,7 +301,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(BAR_P);
     }
-    if (ok && wait_bounded(BAR_ACC, 0, ctl, WHERE_BWD_COMPUTE)) {
+    if (ok && warp_wait(BAR_ACC, 0, ctl, WHERE_BWD_COMPUTE)) {
       tc_fence_after();
       const bool valid = key < p.S;
       const size_t row = ((static_cast<size_t>(b) * p.S + (valid ? key : 0)) * p.H + h) * D;
@@ -467,7 +467,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     for (int i = 0; ok && i < ntile; ++i) {
       const int kb = 128 * i;
       const bool masked = (CAUSAL && i == qt) || kb + 128 > p.S;
-      if (!wait_bounded(BAR_S, i & 1, ctl, WHERE_BWD_COMPUTE)) { ok = false; break; }
+      if (!warp_wait(BAR_S, i & 1, ctl, WHERE_BWD_COMPUTE)) { ok = false; break; }
       tc_fence_after();
 #pragma unroll 1
       for (int c = 0; c < 4; ++c) {
@@ -499,7 +499,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(BAR_P);
     }
-    if (ok && wait_bounded(BAR_ACC, 0, ctl, WHERE_BWD_COMPUTE)) {
+    if (ok && warp_wait(BAR_ACC, 0, ctl, WHERE_BWD_COMPUTE)) {
       tc_fence_after();
       __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(p.dq) +
                            ((static_cast<size_t>(b) * p.S + (valid ? qrow : 0)) * p.H + h) * D;

@@ -94,12 +94,6 @@ __device__ __forceinline__ void wait_drain_dec(uint32_t bar, uint32_t parity, lo
     if (clock64() - t0 > limit) return;
 }
 
-// A bounded wait whose outcome is the same in every lane of the warp (the lanes' own waits may
-// give up at different moments), so that the warp stays converged for .sync.aligned work.
-__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const WaitCtl& ctl, int where) {
-  return __all_sync(0xffffffffu, wait_bounded(bar, parity, ctl, where));
-}
-
 // REP: copies of the R packed query rows in the 128-row tile (R <= 128 / REP); copy c takes
 // keys [c * 128 / REP, (c + 1) * 128 / REP) of every tile.
 template <int D, bool FP8, bool CAUSAL, int REP>

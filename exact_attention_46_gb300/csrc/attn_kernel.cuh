@@ -563,7 +563,7 @@ __global__ void __launch_bounds__(AttnCfg<D, FP8>::THREADS, 1)
           bias = __log2f(sv / sv_max);
           inv_r = sv_max / sv;
         }
-        if (!wait_bounded(BAR_S_FULL(t), sc & 1, ctl, WHERE_SOFTMAX)) { ok = false; break; }
+        if (!warp_wait(BAR_S_FULL(t), sc & 1, ctl, WHERE_SOFTMAX)) { ok = false; break; }
         ++sc;
         tc_fence_after();
         uint32_t sr[4][32];
@@ -698,7 +698,7 @@ __global__ void __launch_bounds__(AttnCfg<D, FP8>::THREADS, 1)
       if (!ok) break;
 
       // ---- epilogue: O / l -> bf16, lse; then hand O_t back to the MMA warp ----
-      if (!wait_bounded(BAR_O_FULL(t), ouse & 1, ctl, WHERE_SOFTMAX)) { ok = false; break; }
+      if (!warp_wait(BAR_O_FULL(t), ouse & 1, ctl, WHERE_SOFTMAX)) { ok = false; break; }
       ++ouse;
       tc_fence_after();
       const float inv_l = sv_max / l_run;

@@ -82,6 +82,13 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, cons
   }
 }
 
+// The same wait made uniform across the warp: the lanes' own waits may give up at different
+// moments, and a warp that goes on to .sync.aligned Tensor Memory instructions must do so
+// with every lane or none.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const WaitCtl& ctl, int where) {
+  return __all_sync(0xffffffffu, wait_bounded(bar, parity, ctl, where));
+}
+
 // ----------------------------------------------------------------------- TMA --
 
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
