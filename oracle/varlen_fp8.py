@@ -18,13 +18,16 @@ Readings:
   (a sequence of length L starting at a covers ceil(L / 128) <= (a + L) // 128 - a // 128 + 1
   indices) and stay below NB; unused indices carry no meaning;
 * the attention of every sequence is the FP8 path of ``fp8_path`` on its own de-quantised
-  values, with V's block ratios taken over the sequence's own blocks.
+  values, with V's block ratios taken over the sequence's own blocks;
+* with rotary embedding in front (``rope_base``), positions restart at every sequence's first
+  token: each sequence is embedded as ``rope.rope`` embeds a tensor of its own.
 """
 
 import numpy as np
 
 from . import fp8_path
 from .quantise import quantise_blocks, dequantise
+from .rope import rope
 from .varlen import segments
 
 __all__ = ["scale_blocks", "block_base", "quantise_varlen", "fp8_attention_varlen"]
@@ -41,8 +44,9 @@ def block_base(cu_seqlens):
     return cu[:-1] // 128 + np.arange(cu.size - 1)
 
 
-def quantise_varlen(x, cu_seqlens, signs=None):
-    """Quantise packed x [total, H, D] (fp64 values) sequence by sequence.
+def quantise_varlen(x, cu_seqlens, signs=None, rope_base=None):
+    """Quantise packed x [total, H, D] (fp64 values) sequence by sequence (after rotary
+    embedding with positions 0 .. len-1 of each sequence when ``rope_base`` is given).
 
     Returns a dict with ``q`` (E4M3 values), ``codes`` and ``pre`` (the value rounded, as in
     ``quantise_blocks``) [total, H, D], ``scale`` [H, NB] (NaN where no block lives), and
@@ -60,7 +64,8 @@ def quantise_varlen(x, cu_seqlens, signs=None):
     for s, (s0, n) in enumerate(segs):
         if n == 0:
             continue
-        r = quantise_blocks(x[None, s0:s0 + n], signs)
+        xs = x[None, s0:s0 + n] if rope_base is None else rope(x[None, s0:s0 + n], rope_base)
+        r = quantise_blocks(xs, signs)
         nblk = r["scale"].shape[2]
         scale[:, base[s]:base[s] + nblk] = r["scale"][0]
         q[s0:s0 + n] = r["q"][0]

@@ -64,3 +64,20 @@ def test_one_sequence_is_the_fixed_length_fp8_path():
     O1, lse1, _ = fp8_path.fp8_attention(q[None], k[None], v[None], None, 0.2, True, fold_v=True)
     np.testing.assert_allclose(O, O1[0], rtol=1e-13, atol=1e-14)
     np.testing.assert_allclose(lse, lse1[0], rtol=1e-13)
+
+
+def test_rotary_positions_restart_at_every_sequence():
+    from oracle import rope as R
+    cu = np.array([0, 200, 200, 330])
+    x = RNG.standard_normal((330, 2, 16))
+    s = np.where(RNG.random(16) < 0.5, -1.0, 1.0)
+    r = VF.quantise_varlen(x, cu, s, rope_base=10000.0)
+    a = R.rope_quantise_blocks(x[None, :200], s)                 # sequence 0 alone
+    b = R.rope_quantise_blocks(x[None, 200:], s)                 # sequence 2 alone, positions from 0
+    np.testing.assert_array_equal(r["codes"][:200], a["codes"][0])
+    np.testing.assert_array_equal(r["codes"][200:], b["codes"][0])
+    base = VF.block_base(cu)
+    np.testing.assert_array_equal(r["scale"][:, base[2]:base[2] + 2], b["scale"][0])
+    # not the embedding of the packed axis: positions 200 .. 329 would give other codes
+    c = R.rope_quantise_blocks(x[None], s)
+    assert not np.array_equal(r["codes"][200:], c["codes"][0, 200:])
