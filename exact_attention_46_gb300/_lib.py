@@ -24,6 +24,7 @@ SIGNATURES = {
     "attn_fwd_gqa": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P]),
     "attn_varlen_scale_blocks": (_I, [_I, _I]),
     "hadamard_rotate_quant_fp8_varlen": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _P]),
+    "rope_hadamard_rotate_quant_fp8_varlen": (_I, [_P, _P, _I, _P, _P, _P, _P, _I, _I, _I, _I, _P]),
     "attn_fwd_varlen_fp8": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P]),
     "attn_fwd_gqa_fp8": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P]),
     "attn_decode_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I, _I]),

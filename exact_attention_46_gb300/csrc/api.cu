@@ -258,7 +258,7 @@ int run_quant(const void* x, const float* rope_cs, int n_pos, void* out, float* 
   if (n > (1ull << 40) / 2 || nblk_ll * H * B >= 0x7fffffffll || H > 65535 || B > 65535)
     return fail(ATTN_ERR_INVALID_ARG, "tensor too large for the grid");
   const int nblk = static_cast<int>(nblk_ll);
-  if (rope_cs != nullptr && n_pos < 128 * nblk)
+  if (rope_cs != nullptr && cu_seqlens == nullptr && n_pos < 128 * nblk)
     return fail(ATTN_ERR_INVALID_ARG,
                 "the rotary table needs rows for every position of the last 128-token block: "
                 "n_pos = %d < %d", n_pos, 128 * nblk);
@@ -279,7 +279,7 @@ int run_quant(const void* x, const float* rope_cs, int n_pos, void* out, float* 
   CUtensorMap tx, tout;
   if ((rc = make_qkv_map(&tx, x, B, S, H, D, false)) != ATTN_OK) return rc;
   if ((rc = make_qkv_map(&tout, out, B, S, H, D, true)) != ATTN_OK) return rc;
-  QuantParams p{B, H, S, nblk, out, scale, signs, rope_cs, spin_limit(), err, err + 1, cu_seqlens, n_seq};
+  QuantParams p{B, H, S, nblk, out, scale, signs, rope_cs, spin_limit(), err, err + 1, cu_seqlens, n_seq, n_pos};
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e = D == 64    ? launch_hadamard_quant<64>(tx, tout, p, st)
                   : D == 128 ? launch_hadamard_quant<128>(tx, tout, p, st)
@@ -537,6 +537,19 @@ int hadamard_rotate_quant_fp8_varlen(const void* x, void* out, float* scale, con
   return run_quant(x, nullptr, 0, out, scale, signs, 1, H, total, D, stream, cu_seqlens, n_seq);
 }
 
+int rope_hadamard_rotate_quant_fp8_varlen(const void* x, const float* rope_cs, int n_pos, void* out, float* scale,
+                                          const float* signs, const int* cu_seqlens, int n_seq, int total, int H,
+                                          int D, void* stream) {
+  if (rope_cs == nullptr) return fail(ATTN_ERR_INVALID_ARG, "rope_cs must be a non-null device pointer");
+  if (n_pos < 128)
+    return fail(ATTN_ERR_INVALID_ARG, "the rotary table needs at least the 128 rows of one block (n_pos = %d)", n_pos);
+  if (cu_seqlens == nullptr || (reinterpret_cast<uintptr_t>(cu_seqlens) & 3u))
+    return fail(ATTN_ERR_INVALID_ARG, "cu_seqlens must be a non-null, 4-byte aligned device pointer");
+  if (n_seq < 1 || n_seq > VARLEN_MAX_SEQ)
+    return fail(ATTN_ERR_INVALID_ARG, "n_seq must be in [1, %d] (got %d)", VARLEN_MAX_SEQ, n_seq);
+  return run_quant(x, rope_cs, n_pos, out, scale, signs, 1, H, total, D, stream, cu_seqlens, n_seq);
+}
+
 size_t attn_bwd_workspace_bytes(int B, int H, int S) {
   if (B < 1 || H < 1 || S < 1) return 0;
   return 8ull * B * H * ((static_cast<size_t>(S) + 127) / 128 * 128);
@@ -762,6 +775,6 @@ int attn_selftest_bounded_wait(long long spin_cycles, void* stream) {
   return ok();
 }
 
-int attn_version(void) { return 107; }
+int attn_version(void) { return 108; }
 
 }  // extern "C"

@@ -38,7 +38,10 @@
 // a binary search over the strictly increasing cu[s] / 128 + s finds its sequence.  Rows past
 // the sequence's end arrive with the box but count as zero; a whole block leaves by tensor
 // store, a partial one row by row from registers (a tensor store would overwrite the next
-// sequence's rows).  The offsets are checked before anything is written.
+// sequence's rows).  The offsets are checked before anything is written.  With RoPE the
+// positions restart at every sequence's first token (the table rows of block k of a sequence
+// are those of block k of a tensor of its own), and a table too short for some sequence is an
+// error found in the same check.
 #include <atomic>
 #include <cstdint>
 #include <cuda_bf16.h>
@@ -118,7 +121,6 @@ __global__ void __launch_bounds__(QCfg<D, ROPE>::THREADS, QCfg<D, ROPE>::CTAS_PE
     hadamard_quant_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmOut,
                           const QuantParams p) {
   using C = QCfg<D, ROPE>;
-  static_assert(!(VARLEN && ROPE), "no rotary embedding on packed batches");
   constexpr int VPT = C::VPT;
   constexpr int NSTAGE = C::NSTAGE;
   constexpr int NW = VPT / 8;         // 16-byte input chunks per thread
@@ -169,8 +171,11 @@ __global__ void __launch_bounds__(QCfg<D, ROPE>::THREADS, QCfg<D, ROPE>::CTAS_PE
   if constexpr (VARLEN) {
     // offsets that are not 0 .. total, non-decreasing: nothing is written
     bool bad = false;
-    for (int i = static_cast<int>(threadIdx.x); i < p.n_seq; i += C::THREADS)
-      bad |= p.cu_seqlens[i + 1] < p.cu_seqlens[i];
+    for (int i = static_cast<int>(threadIdx.x); i < p.n_seq; i += C::THREADS) {
+      const int len = p.cu_seqlens[i + 1] - p.cu_seqlens[i];
+      bad |= len < 0;
+      if (ROPE) bad |= static_cast<long long>(len + QROWS - 1) / QROWS * QROWS > p.n_pos;
+    }
     if (threadIdx.x == 0) bad |= p.cu_seqlens[0] != 0 || p.cu_seqlens[p.n_seq] != p.S;
     if (__syncthreads_or(bad)) {
       if (threadIdx.x == 0 && atomicCAS(p.err_word, 0, 1 /* ATTN_ERR_INVALID_ARG */) == 0) atomicExch(p.err_info, 11);
@@ -186,7 +191,7 @@ __global__ void __launch_bounds__(QCfg<D, ROPE>::THREADS, QCfg<D, ROPE>::CTAS_PE
     const int h = bi % p.H, blk = (bi / p.H) % p.nblk, b = bi / (p.H * p.nblk);
     const uint32_t st = base_u32 + (k % NSTAGE) * C::STAGE_BYTES;
     const uint32_t bar = bar0 + 8u * (k % NSTAGE);
-    int tok0 = blk * QROWS;
+    int tok0 = blk * QROWS, rblk = blk;   // rblk: the block's position block for RoPE
     if constexpr (VARLEN) {
       // the sequence of index blk: the last s with cu[s] / 128 + s <= blk (cu[0] / 128 + 0 = 0)
       int lo = 0, hi = p.n_seq - 1;
@@ -198,6 +203,7 @@ __global__ void __launch_bounds__(QCfg<D, ROPE>::THREADS, QCfg<D, ROPE>::CTAS_PE
       const int kb = blk - ((s0 >> 7) + lo);
       const int rows = 128 * kb < len ? min(QROWS, len - 128 * kb) : 0;
       tok0 = s0 + 128 * kb;
+      rblk = kb;
       stage_info[k % NSTAGE] = make_int2(tok0, rows);
       if (rows == 0) {                // an index no block lives at
         mbar_arrive(bar);
@@ -217,7 +223,7 @@ __global__ void __launch_bounds__(QCfg<D, ROPE>::THREADS, QCfg<D, ROPE>::CTAS_PE
       const uint32_t slot = base_u32 + C::OFF_COARSE + (k % C::NCSLOT) * NCOARSE * C::TROW;
 #pragma unroll
       for (int r1 = 0; r1 < NCOARSE; ++r1)
-        bulk_load(slot + r1 * C::TROW, p.rope_cs + static_cast<size_t>(blk * QROWS + 16 * r1) * D, 4 * D, bar,
+        bulk_load(slot + r1 * C::TROW, p.rope_cs + static_cast<size_t>(rblk * QROWS + 16 * r1) * D, 4 * D, bar,
                   l2_policy_evict_last());
     }
     n_issued = k + 1;
@@ -447,6 +453,8 @@ cudaError_t launch_hadamard_quant(const CUtensorMap& tx, const CUtensorMap& tout
     if ((e = set_smem<D, false, true>()) != cudaSuccess) return e;
     if ((e = set_smem<D, true, false, true>()) != cudaSuccess) return e;
     if ((e = set_smem<D, false, false, true>()) != cudaSuccess) return e;
+    if ((e = set_smem<D, true, true, true>()) != cudaSuccess) return e;
+    if ((e = set_smem<D, false, true, true>()) != cudaSuccess) return e;
     int n = 0;
     e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
@@ -455,9 +463,13 @@ cudaError_t launch_hadamard_quant(const CUtensorMap& tx, const CUtensorMap& tout
   }
   const int sms = sm_count[dev & 63];
   const bool rot = p.signs != nullptr, rope = p.rope_cs != nullptr;
-  if (p.cu_seqlens != nullptr)
+  if (p.cu_seqlens != nullptr) {
+    if (rope)
+      return rot ? launch_variant<D, true, true, true>(tx, tout, p, sms, stream)
+                 : launch_variant<D, false, true, true>(tx, tout, p, sms, stream);
     return rot ? launch_variant<D, true, false, true>(tx, tout, p, sms, stream)
                : launch_variant<D, false, false, true>(tx, tout, p, sms, stream);
+  }
   if (rope)
     return rot ? launch_variant<D, true, true>(tx, tout, p, sms, stream)
                : launch_variant<D, false, true>(tx, tout, p, sms, stream);

@@ -112,6 +112,7 @@ struct QuantParams {
   // nblk = total / 128 + n_seq + 1 indices per head (scale [H, nblk]); nullptr = fixed length
   const int* cu_seqlens;
   int n_seq;
+  int n_pos;            // rows of rope_cs (VARLEN: checked against every sequence on the device)
 };
 
 // x is read through `tx`, the same [B, S, H, D] bf16 tensor map the attention kernel uses;

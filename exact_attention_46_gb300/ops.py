@@ -121,6 +121,24 @@ def hadamard_rotate_quant_fp8_varlen(x, cu_seqlens, signs=None, out=None, scale=
     return out, scale
 
 
+def rope_hadamard_rotate_quant_fp8_varlen(x, rope_cs, cu_seqlens, signs=None, out=None, scale=None, stream=None):
+    """Rotary embedding (positions restarting at every sequence), then
+    ``hadamard_rotate_quant_fp8_varlen``, in one kernel.  ``rope_cs``: a table from
+    ``rope_cos_sin_table`` with at least 128 * ceil(len / 128) rows for the longest sequence."""
+    if x.dim() != 3 or not x.is_cuda or not x.is_contiguous():
+        raise ValueError("x must be a contiguous CUDA tensor [total, H, D]")
+    _check_cu(cu_seqlens)
+    total, H, D = x.shape
+    n_seq = int(cu_seqlens.numel() - 1)
+    if out is None:
+        out = torch.empty((total, H, D), dtype=torch.uint8, device=x.device)
+    if scale is None:
+        scale = torch.empty((H, varlen_scale_blocks(total, n_seq)), dtype=torch.float32, device=x.device)
+    _lib.call("rope_hadamard_rotate_quant_fp8_varlen", _ptr(x), _ptr(rope_cs), int(rope_cs.shape[0]), _ptr(out),
+              _ptr(scale), _ptr(signs), _ptr(cu_seqlens), n_seq, total, H, D, _stream(stream))
+    return out, scale
+
+
 def attn_fwd_varlen_fp8(q8, k8, v8, q_scale, k_scale, v_scale, cu_seqlens, max_seqlen=None, causal=False,
                         scale=0.0, out=None, lse=None, want_lse=True, stream=None):
     """attn_fwd_varlen on E4M3 codes [total, H, D] with the block scales of

@@ -146,6 +146,16 @@ int attn_varlen_scale_blocks(int total, int n_seq);
 int hadamard_rotate_quant_fp8_varlen(const void* x, void* out, float* scale, const float* signs,
                                      const int* cu_seqlens, int n_seq, int total, int H, int D,
                                      void* stream);
+/*
+ * rope_hadamard_rotate_quant_fp8_varlen -- the same with rotary embedding in front
+ *   (rope_hadamard_rotate_quant_fp8 on a packed batch): positions restart at
+ *   every sequence's first token.  rope_cs as rope_cos_sin_table writes it,
+ *   n_pos >= 128 rows; a sequence with 128 * ceil(len / 128) > n_pos is an error
+ *   found on the device with the offsets check (nothing is written).
+ */
+int rope_hadamard_rotate_quant_fp8_varlen(const void* x, const float* rope_cs, int n_pos, void* out,
+                                          float* scale, const float* signs, const int* cu_seqlens,
+                                          int n_seq, int total, int H, int D, void* stream);
 int attn_fwd_varlen_fp8(const void* q8, const void* k8, const void* v8, const float* q_scale,
                         const float* k_scale, const float* v_scale, void* o, float* lse,
                         const int* cu_seqlens, int n_seq, int total, int max_seqlen, int H, int D,

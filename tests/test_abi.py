@@ -40,7 +40,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_version(lib):
-    assert lib.attn_version() == 107
+    assert lib.attn_version() == 108
 
 
 FAKE = 1 << 20   # 16-byte aligned non-null fake device addresses: never dereferenced
@@ -177,6 +177,16 @@ def test_varlen_fp8_and_quantiser_reject_bad_arguments(lib):
         a = list(ok)
         a[i] = val
         assert q(*a) == code, (i, val)
+    r = lib.rope_hadamard_rotate_quant_fp8_varlen
+    ok = [FAKE, FAKE * 20, 256, FAKE * 4, FAKE * 8, None, FAKE * 12, 3, 300, 2, 128, None]
+    for i, val, code in ((1, None, 1),          # rope_cs missing
+                         (2, 100, 1),           # fewer than 128 table rows
+                         (6, None, 1),          # cu_seqlens missing
+                         (7, 0, 1),             # n_seq = 0
+                         (10, 96, 2)):          # D = 96
+        a = list(ok)
+        a[i] = val
+        assert r(*a) == code, (i, val)
     f = lib.attn_fwd_varlen_fp8
     ok = [FAKE, FAKE * 2, FAKE * 3, FAKE * 4, FAKE * 5, FAKE * 6, FAKE * 8, None, FAKE * 12, 3, 300, 200, 2, 128,
           0, 0.0, None]

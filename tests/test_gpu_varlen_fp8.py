@@ -172,3 +172,40 @@ def test_end_to_end_from_the_quantiser():
     bound = e_in + 2 * e_p + rms(half_ulp_bf16(O_deq)) + 1e-4
     assert rms(to64(o) - O_ref) <= bound, (rms(to64(o) - O_ref), e_in, e_p)
     assert float(np.abs(to64(lse) - lse_ref).max()) <= float(np.abs(lse_deq - lse_ref).max()) + 1e-3
+
+
+@pytest.mark.parametrize("rotate", [False, True])
+@pytest.mark.parametrize("D", [64, 128, 256])
+@pytest.mark.parametrize("mix", sorted(MIXES))
+def test_rope_quantiser_matches_oracle(mix, D, rotate):
+    # RoPE in front, positions restarting at every sequence; codes within the fused RoPE
+    # quantiser's tie rule (its fp32 rotary arithmetic is a few ulps from fp64)
+    cu = np.asarray(MIXES[mix], dtype=np.int32)
+    x = packed(int(cu[-1]), 3, D, case=96)[0]
+    s = signs(96, D) if rotate else None
+    dev = torch.device("cuda")
+    max_len = int(np.diff(cu).max())
+    cs = ops.rope_cos_sin_table(128 * ((max_len + 127) // 128), D)
+    codes, scale = ops.rope_hadamard_rotate_quant_fp8_varlen(x.to(dev), cs, torch.from_numpy(cu).to(dev),
+                                                             torch.from_numpy(s).to(dev) if rotate else None)
+    ops.check()
+    ref = VF.quantise_varlen(to64(x), cu, None if s is None else s.astype(np.float64), rope_base=10000.0)
+    live = ~np.isnan(ref["scale"])
+    np.testing.assert_allclose(scale.cpu().double().numpy()[live], ref["scale"][live], rtol=1e-5, atol=0)
+    helpers.check_codes(codes.cpu().numpy(), ref, 1e-5, 5e-4, 1e-4)
+
+
+def test_rope_table_too_short_writes_nothing():
+    dev = torch.device("cuda")
+    x = packed(400, 2, 128, case=97)[0].to(dev)
+    cu = torch.tensor([0, 100, 400], dtype=torch.int32, device=dev)    # 300 tokens need 384 rows
+    cs = ops.rope_cos_sin_table(256, 128)
+    out = torch.full((400, 2, 128), 7, dtype=torch.uint8, device=dev)
+    sc = torch.full((2, ops.varlen_scale_blocks(400, 2)), 7.0, device=dev)
+    ops.rope_hadamard_rotate_quant_fp8_varlen(x, cs, cu, None, out=out, scale=sc)
+    with pytest.raises(_lib.AttnError) as e:
+        ops.check()
+    assert e.value.status == 1
+    assert bool((out == 7).all()) and bool((sc == 7.0).all())
+    ops.rope_hadamard_rotate_quant_fp8_varlen(x, ops.rope_cos_sin_table(384, 128), cu)
+    ops.check()
