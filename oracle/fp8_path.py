@@ -46,10 +46,12 @@ def quantise_qkv(q, k, v, signs=None):
 
 
 def v_block_ratio(v_scale, S, block=128):
-    """r [B, H, S]: the block scale of each key over the largest block scale of its head."""
+    """r [B, H, S]: the block scale of each key over the largest block scale of its head
+    (0 for every key of a head whose scales are all 0)."""
     v_scale = np.asarray(v_scale, dtype=np.float64)
     per_key = v_scale[:, :, np.arange(S) // block]
-    return per_key / v_scale.max(axis=2, keepdims=True)
+    mx = v_scale.max(axis=2, keepdims=True)
+    return np.where(mx > 0, per_key / np.where(mx > 0, mx, 1.0), 0.0)
 
 
 def attention_rounded_p(qd, kd, vd, scale, causal=False, rows=None, round_p=True, v_ratio=None):
@@ -77,8 +79,10 @@ def attention_rounded_p(qd, kd, vd, scale, causal=False, rows=None, round_p=True
             elif v_ratio is None:
                 p = round_e4m3(e)
             else:
+                # a key whose block scale is 0 has V = 0: its term vanishes (the limit r -> 0)
                 r = np.asarray(v_ratio, dtype=np.float64)[b, h][None, :]
-                p = round_e4m3(e * r) / r
+                rs = np.where(r > 0, r, 1.0)
+                p = np.where(r > 0, round_e4m3(e * rs) / rs, 0.0)
             O[b, :, h, :] = (p @ vd[b, :, h, :]) / l[:, None]
             lse[b, h, :] = m + np.log(l)
     return O, lse

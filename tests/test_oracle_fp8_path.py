@@ -146,3 +146,15 @@ def test_ratios_belong_to_keys_by_hand():
     want = ((0.3125 / 0.3) * v[0, 0, 0] + v[0, 1, 0]) / 2
     np.testing.assert_allclose(O[0, 0, 0], want, rtol=1e-15)
     np.testing.assert_allclose(O[0, 1, 0], want, rtol=1e-15)
+
+
+def test_zero_block_scale_terms_vanish():
+    # a key of a zero-scale block has V = 0; its folded term is 0 (not 0/0) and l still counts it
+    q = np.zeros((1, 2, 1, 4))
+    k = np.zeros((1, 2, 1, 4))
+    v = np.array([[0.0, 0.0, 0.0, 0.0], [3.0, -1.0, 2.0, 1.0]]).reshape(1, 2, 1, 4)
+    O, lse = fp8_path.attention_rounded_p(q, k, v, 1.0, round_p=True, v_ratio=np.array([[[0.0, 1.0]]]))
+    np.testing.assert_allclose(O[0, 0, 0], v[0, 1, 0] / 2, rtol=1e-15)
+    np.testing.assert_allclose(lse[0, 0], np.log(2.0), rtol=1e-15)
+    r = fp8_path.v_block_ratio(np.zeros((1, 1, 2)), 200)
+    assert np.array_equal(r, np.zeros((1, 1, 200)))
