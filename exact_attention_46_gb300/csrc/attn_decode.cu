@@ -249,6 +249,7 @@ __global__ void __launch_bounds__(DecCfg<D, FP8>::THREADS, 1)
         for (int jj = static_cast<int>(lane); jj < ntile; jj += 32) sv_max = fmaxf(sv_max, p.v_scale[kv_blk + t0 + jj]);
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) sv_max = fmaxf(sv_max, __shfl_xor_sync(0xffffffffu, sv_max, o));
+        sv_max = fmaxf(sv_max, 0x1p-96f);  // every value scale 0: O = 0, l still counts
       }
     }
     if constexpr (REP > 1) {
@@ -307,7 +308,10 @@ __global__ void __launch_bounds__(DecCfg<D, FP8>::THREADS, 1)
           fetch_scales(j + 32, sk_nxt, sv_nxt);
         }
         const float sk = __shfl_sync(0xffffffffu, sk_cur, j & 31);
-        const float sv = __shfl_sync(0xffffffffu, sv_cur, j & 31);
+        const float sv_raw = __shfl_sync(0xffffffffu, sv_cur, j & 31);
+        // a zero scale (a block of zeros) as 2^-30 of the largest: its numerators vanish in E4M3,
+        // the row sum still takes them at full weight
+        const float sv = fmaxf(sv_raw, sv_max * 0x1p-30f);
         cmul = cq * sk;
         bias = __log2f(sv / sv_max);
         inv_r = sv_max / sv;

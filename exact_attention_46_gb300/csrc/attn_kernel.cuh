@@ -548,6 +548,7 @@ __global__ void __launch_bounds__(AttnCfg<D, FP8>::THREADS, 1)
           for (int j = static_cast<int>(lane); j < key_tiles(it); j += 32) sv_max = fmaxf(sv_max, p.v_scale[kv_base + j]);
 #pragma unroll
           for (int o = 16; o > 0; o >>= 1) sv_max = fmaxf(sv_max, __shfl_xor_sync(0xffffffffu, sv_max, o));
+          sv_max = fmaxf(sv_max, 0x1p-96f);  // every value scale 0: O = 0, l still counts
         }
       }
 
@@ -558,7 +559,10 @@ __global__ void __launch_bounds__(AttnCfg<D, FP8>::THREADS, 1)
         float cmul = p.c_log2, bias = 0.f, inv_r = 1.f;
         if (FP8) {
           const float sk = p.k_scale != nullptr ? p.k_scale[kv_base + j] : 1.f;
-          const float sv = p.v_scale != nullptr ? p.v_scale[kv_base + j] : 1.f;
+          const float sv_raw = p.v_scale != nullptr ? p.v_scale[kv_base + j] : 1.f;
+          // a zero scale (a block of zeros) as 2^-30 of the largest: its numerators vanish in E4M3,
+          // the row sum still takes them at full weight
+          const float sv = fmaxf(sv_raw, sv_max * 0x1p-30f);
           cmul *= sq * sk;
           bias = __log2f(sv / sv_max);
           inv_r = sv_max / sv;

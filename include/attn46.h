@@ -78,8 +78,10 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
  *   inputs come from hadamard_rotate_quant_fp8.
  *   q8, k8, v8 : [B, S, H, D] E4M3 bytes; the value of an element is
  *                code * its block's scale.
- *   q_scale, k_scale, v_scale : [B, H, ceil(S/128)] fp32 positive scales, as
- *                written by hadamard_rotate_quant_fp8.
+ *   q_scale, k_scale, v_scale : [B, H, ceil(S/128)] fp32 scales, as written by
+ *                hadamard_rotate_quant_fp8 (which never writes 0).  Scales must be
+ *                finite; Q and K scales positive, V scales >= 0 (a 0 block holds
+ *                zeros: it adds nothing to O and its keys still count in lse).
  *   o, lse, causal, scale : as for attn_fwd (scale refers to the original
  *                head dimension; the rotation does not change it).
  *   The softmax numerators are rounded to E4M3 for the P-V GEMM; the row sums

@@ -182,3 +182,32 @@ def test_incoherent_processing_ratio_matches_emulation(S):
 def test_incoherent_processing_halves_error():
     r_gpu, _ = _experiment(1024, case=41)
     assert r_gpu <= 0.5
+
+
+def test_zero_value_scales():
+    # A V block with scale 0 holds zeros (value = code * scale), and one head's V scales are all
+    # 0: O and lse stay finite, the zero block contributes nothing, the all-zero head gives O = 0.
+    B, S, H, D = 1, 700, 2, 128
+    q, k, v = inputs(B, S, H, D, case=25)
+    Qq, Kq, Vq = fp8_path.quantise_qkv(to64(q), to64(k), to64(v), None)
+    vs = Vq["scale"].astype(np.float32)
+    vs[0, 0, 2] = 0.0
+    vs[0, 1, :] = 0.0
+    sc32 = [Qq["scale"].astype(np.float32), Kq["scale"].astype(np.float32), vs]
+    dev = torch.device("cuda")
+    up = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+    qd, kd, vd = (quantise.dequantise(r["q"], s.astype(np.float64)) for r, s in zip((Qq, Kq, Vq), sc32))
+    ratio = fp8_path.v_block_ratio(sc32[2], S)
+    for causal in (False, True):
+        o, lse = ops.attn_fwd_fp8(up(Qq["codes"]), up(Kq["codes"]), up(Vq["codes"]), *(up(s) for s in sc32),
+                                  causal=causal)
+        ops.check()
+        O_deq, lse_deq = fp8_path.attention_rounded_p(qd, kd, vd, 1 / np.sqrt(D), causal, round_p=False)
+        O_emul, _ = fp8_path.attention_rounded_p(qd, kd, vd, 1 / np.sqrt(D), causal, v_ratio=ratio)
+        og = to64(o)
+        assert np.isfinite(og).all() and np.isfinite(to64(lse)).all()
+        assert np.all(og[:, :, 1] == 0.0)
+        _, e_gpu = stats(og, O_deq)
+        _, e_emul = stats(O_emul, O_deq)
+        assert e_gpu <= 2 * e_emul + 1e-4, (causal, e_gpu, e_emul)
+        assert np.abs(to64(lse) - lse_deq).max() <= 1e-3

@@ -159,3 +159,24 @@ def test_decode_fp8_without_lse_and_repeatable():
     b, lb = ops.attn_decode_fp8(q8, k8, v8, sq, sk, sv, causal=True, want_lse=False)
     ops.check()
     assert lb is None and torch.equal(a, b)
+
+
+def test_decode_fp8_zero_value_scales():
+    # one V block with scale 0 and one key/value head whose V scales are all 0
+    B, Sq, Sk, Hq, Hkv, D = 2, 1, 3000, 8, 2, 128
+    q, k, v = raw_inputs(B, Sq, Sk, Hq, Hkv, D, case=88)
+    (q8, sq, qd), (k8, sk, kd), (v8, sv, _) = quantised(q, None), quantised(k, None), quantised(v, None)
+    sv = sv.copy()
+    sv[0, 0, 5] = 0.0
+    sv[1, 1, :] = 0.0
+    rv = quantise.quantise_blocks(np.asarray(v, np.float64))
+    vd = quantise.dequantise(rv["q"], sv.astype(np.float64))
+    dev = torch.device("cuda")
+    t = [torch.from_numpy(np.ascontiguousarray(a)).to(dev) for a in (q8, k8, v8, sq, sk, sv)]
+    o, lse = ops.attn_decode_fp8(*t, causal=True)
+    ops.check()
+    O_deq, lse_deq = oracle_gqa.attention_gqa(qd, kd, vd, causal=True)
+    O_emul, _ = oracle_gqa.attention_gqa(qd, kd, vd, causal=True, round_p=True)
+    og = to64(o)
+    assert np.all(og[1, :, 4:8] == 0.0)                     # query heads of key/value head 1, batch 1
+    check(og, to64(lse), O_deq, O_emul, lse_deq)
