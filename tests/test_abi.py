@@ -232,3 +232,18 @@ def test_decode_fp8_rejects_bad_arguments(lib):
         a = list(ok)
         a[i] = val
         assert d(*a) == code, (i, val)
+
+
+def test_missing_library_raises_instead_of_falling_back(monkeypatch, tmp_path):
+    # with no compiled library every binding raises; nothing computes the result another way
+    import torch
+    from exact_attention_46_gb300 import ops
+    monkeypatch.setattr(_lib, "LIB_PATH", str(tmp_path / "absent.so"))
+    monkeypatch.setattr(_lib, "_lib", None)
+    x = torch.zeros((1, 4, 1, 64), dtype=torch.bfloat16)
+    with pytest.raises(ImportError):
+        _lib.load()
+    with pytest.raises((ImportError, ValueError)):
+        ops.attn_fwd(x, x, x)
+    with pytest.raises(ImportError):
+        ops.varlen_scale_blocks(300, 3)
