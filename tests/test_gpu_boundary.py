@@ -39,3 +39,24 @@ def test_invalid_arguments_raise_and_launch_nothing():
     with pytest.raises(_lib.AttnError):
         ops.attn_fwd(q, q, q, out=q)               # output aliases input
     ops.check()
+
+
+def test_binding_rejects_malformed_tensors_before_the_library():
+    import torch
+    from exact_attention_46_gb300 import ops
+    dev = torch.device("cuda")
+    q = torch.zeros((1, 256, 2, 128), dtype=torch.bfloat16, device=dev)
+    codes = torch.zeros((1, 256, 2, 128), dtype=torch.uint8, device=dev)
+    sc = torch.ones((1, 2, 2), dtype=torch.float32, device=dev)
+    with pytest.raises(ValueError, match="shape"):
+        ops.attn_fwd_fp8(codes, codes, codes, sc, sc, sc[:, :, :1].contiguous())     # one block short
+    with pytest.raises(ValueError, match="dtype"):
+        ops.attn_fwd_fp8(codes, codes, codes, sc, sc.double(), sc)
+    with pytest.raises(ValueError, match="dtype"):
+        ops.attn_fwd(q, codes, codes)                                             # mixed families
+    with pytest.raises(ValueError, match="dtype"):
+        ops.attn_fwd(q, q, q, out=torch.empty_like(q, dtype=torch.float32))
+    with pytest.raises(ValueError, match="shape"):
+        ops.attn_decode(q[:, :1].contiguous(), q, q[:, :128].contiguous())
+    with pytest.raises(ValueError, match="shape"):
+        ops.hadamard_rotate_quant_fp8(q, torch.ones(64, device=dev))               # signs of D values
