@@ -16,13 +16,18 @@ derivatives of the definition in ``attention`` (plain calculus), per (b, h):
     dQ  = scale * dS K,     dK = scale * dS^T Q
 
 O and P here are the oracle's own fp64 values computed from Q, K, V (never the GPU's).
+
+Grouped-query attention (``gqa.attention_gqa``: query head h reads key/value head h // G) is
+multi-head attention with every key/value head repeated G times, so its gradients are those
+of the repeated problem with dK and dV summed over each group (the gradient of a repeated
+input is the sum of the copies' gradients): ``attention_backward_gqa``.
 """
 
 import numpy as np
 
 from .attention import attention_weights, default_scale
 
-__all__ = ["attention_backward"]
+__all__ = ["attention_backward", "attention_backward_gqa"]
 
 
 def attention_backward(q, k, v, do, scale=None, causal=False):
@@ -47,3 +52,17 @@ def attention_backward(q, k, v, do, scale=None, causal=False):
             dq[b, :, h] = scale * dS @ k[b, :, h]
             dk[b, :, h] = scale * dS.T @ q[b, :, h]
     return dq, dk, dv
+
+
+def attention_backward_gqa(q, k, v, do, scale=None, causal=False):
+    """(dQ [B, S, Hq, D], dK, dV [B, S, Hkv, D]) of grouped-query attention."""
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    Hq, Hkv = q.shape[2], k.shape[2]
+    if Hq % Hkv:
+        raise ValueError("Hq must be a multiple of Hkv")
+    G = Hq // Hkv
+    dq, dk_rep, dv_rep = attention_backward(q, np.repeat(k, G, axis=2), np.repeat(v, G, axis=2), do, scale, causal)
+    B, S, _, D = k.shape
+    return dq, dk_rep.reshape(B, S, Hkv, G, D).sum(axis=3), dv_rep.reshape(B, S, Hkv, G, D).sum(axis=3)

@@ -76,3 +76,33 @@ def test_single_key_row_has_no_query_gradient():
     q, k, v, do = (RNG.standard_normal((B, S, H, D)) for _ in range(4))
     dq, _, _ = backward.attention_backward(q, k, v, do, causal=True)
     np.testing.assert_allclose(dq[0, 0], 0.0, atol=1e-14)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_gqa_gradients_match_finite_differences(causal):
+    # the loss sum(dO * O) of grouped-query attention, differentiated numerically
+    from oracle import gqa
+    rng = np.random.default_rng(5)
+    B, S, Hq, Hkv, D = 1, 6, 4, 2, 3
+    q, do = rng.standard_normal((B, S, Hq, D)), rng.standard_normal((B, S, Hq, D))
+    k, v = rng.standard_normal((B, S, Hkv, D)), rng.standard_normal((B, S, Hkv, D))
+    dq, dk, dv = backward.attention_backward_gqa(q, k, v, do, 0.7, causal)
+    loss = lambda q_, k_, v_: float((gqa.attention_gqa(q_, k_, v_, 0.7, causal)[0] * do).sum())
+    h = 1e-6
+    for arr, grad, idx in ((q, dq, (0, 3, 2, 1)), (k, dk, (0, 1, 1, 2)), (v, dv, (0, 4, 0, 0)), (k, dk, (0, 5, 0, 1))):
+        plus, minus = arr.copy(), arr.copy()
+        plus[idx] += h
+        minus[idx] -= h
+        args_p = [plus if a is arr else a for a in (q, k, v)]
+        args_m = [minus if a is arr else a for a in (q, k, v)]
+        fd = (loss(*args_p) - loss(*args_m)) / (2 * h)
+        assert abs(fd - grad[idx]) <= 1e-6 * max(1.0, abs(fd)), (idx, fd, grad[idx])
+
+
+def test_gqa_with_one_group_per_head_is_the_plain_backward():
+    rng = np.random.default_rng(6)
+    q, k, v, do = (rng.standard_normal((2, 9, 3, 4)) for _ in range(4))
+    a = backward.attention_backward_gqa(q, k, v, do, causal=True)
+    b = backward.attention_backward(q, k, v, do, causal=True)
+    for x, y in zip(a, b):
+        np.testing.assert_array_equal(x, y)
