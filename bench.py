@@ -451,7 +451,8 @@ def decode_leg(dev, n=20):
 
 
 def backward_leg(dev, n=10):
-    """attn_bwd at the benchmark size (B=2, S=8192, H=16, D=128), non-causal and causal.
+    """attn_bwd at the benchmark size (B=2, S=8192, H=16, D=128), non-causal and causal, then
+    attn_bwd_gqa on the same query heads over H/8 key/value heads.
     TFLOPS by the usual convention for the backward pass: 2.5x the forward's FLOPs (five
     S x S x D GEMMs against two); the kernels execute seven (S and dP are recomputed in both
     the dK/dV and the dQ kernel)."""
@@ -477,6 +478,28 @@ def backward_leg(dev, n=10):
         ms = e0.elapsed_time(e1) / n
         flops = 2.5 * attention_flops(B, H, S, D, causal)
         key = "causal" if causal else "non_causal"
+        res[key + "_ms"] = round(ms, 4)
+        res[key + "_tflops"] = round(flops / ms / 1e9, 1)
+    # grouped-query: the same query heads over H / 8 key/value heads (dK, dV summed over groups of 8)
+    Hkv = H // 8
+    kg, vg = k[:, :, :Hkv].contiguous(), v[:, :, :Hkv].contiguous()
+    dkg, dvg = torch.empty_like(kg), torch.empty_like(vg)
+    res["gqa_workload"] = f"Hq={H} Hkv={Hkv}, otherwise as above"
+    for causal in (False, True):
+        o, lse = ops.attn_fwd_gqa(q, kg, vg, causal=causal)
+        fn = lambda: ops.attn_bwd_gqa(q, kg, vg, o, lse, do, causal=causal, dq=dq, dk=dkg, dv=dvg, workspace=ws)
+        for _ in range(3):
+            fn()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record()
+        for _ in range(n):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / n
+        flops = 2.5 * attention_flops(B, H, S, D, causal)
+        key = "gqa_causal" if causal else "gqa_non_causal"
         res[key + "_ms"] = round(ms, 4)
         res[key + "_tflops"] = round(flops / ms / 1e9, 1)
     ops.check()

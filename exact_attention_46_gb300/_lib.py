@@ -32,6 +32,7 @@ SIGNATURES = {
     "attn_decode_fp8": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _I, _I, _I, _I, _I, _I, _I, _F, _P]),
     "attn_bwd_workspace_bytes": (_SZ, [_I, _I, _I]),
     "attn_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _I, _I, _I, _I, _I, _F, _P]),
+    "attn_bwd_gqa": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _I, _I, _I, _I, _I, _I, _F, _P]),
     "attn_bwd_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _P]),
     "hadamard_rotate_quant_fp8": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _P]),
     "rope_cos_sin_table": (_I, [_P, _I, _I, _D, _P]),

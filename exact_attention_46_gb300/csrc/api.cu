@@ -355,6 +355,64 @@ int check_gqa_args(const void* q, const void* k, const void* v, const void* o, c
   return ATTN_OK;
 }
 
+// The backward pass: H query heads over Hkv key/value heads (Hkv = H: plain multi-head).
+int run_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
+            void* dq, void* dk, void* dv, float* workspace, size_t workspace_bytes, int B, int H, int Hkv, int S,
+            int D, int causal, float scale, void* stream) {
+  if (o == nullptr || dout == nullptr || lse == nullptr || dq == nullptr || dk == nullptr || dv == nullptr ||
+      workspace == nullptr)
+    return fail(ATTN_ERR_INVALID_ARG, "o, dout, lse, dq, dk, dv and workspace must be non-null device pointers");
+  if (D == 256) return fail(ATTN_ERR_UNSUPPORTED, "the backward pass supports D = 64 and 128 (got 256)");
+  int rc = check_gqa_args(q, k, v, dq, nullptr, B, H, Hkv, S, S, D, causal, scale, false, 2);
+  if (rc != ATTN_OK) return rc;
+  if (!aligned16(o) || !aligned16(dout) || !aligned16(dk) || !aligned16(dv) || !aligned16(workspace) ||
+      (reinterpret_cast<uintptr_t>(lse) & 3u))
+    return fail(ATTN_ERR_INVALID_ARG, "tensors and workspace must be 16-byte aligned (lse 4-byte)");
+  const size_t need = attn_bwd_workspace_bytes(B, H, S);
+  if (workspace_bytes < need)
+    return fail(ATTN_ERR_INVALID_ARG, "workspace of %zu bytes is smaller than the %zu needed", workspace_bytes, need);
+  const size_t n = 2ull * B * S * H * D, nkv = 2ull * B * S * Hkv * D, nl = 4ull * B * H * S;
+  const void* ins[6] = {q, k, v, o, dout, lse};
+  const size_t in_bytes[6] = {n, nkv, nkv, n, n, nl};
+  void* outs[4] = {dq, dk, dv, workspace};
+  const size_t out_bytes[4] = {n, nkv, nkv, need};
+  for (int a = 0; a < 4; ++a) {
+    for (int i = 0; i < 6; ++i)
+      if (overlap(outs[a], out_bytes[a], ins[i], in_bytes[i]))
+        return fail(ATTN_ERR_INVALID_ARG, "an output or the workspace overlaps an input");
+    for (int c = a + 1; c < 4; ++c)
+      if (overlap(outs[a], out_bytes[a], outs[c], out_bytes[c]))
+        return fail(ATTN_ERR_INVALID_ARG, "outputs overlap each other or the workspace");
+  }
+  int* err = nullptr;
+  if ((rc = err_words(&err)) != ATTN_OK) return rc;
+  CUtensorMap maps[4];
+  const void* srcs[4] = {q, k, v, dout};
+  for (int i = 0; i < 4; ++i)
+    if ((rc = make_qkv_map(&maps[i], srcs[i], B, S, (i == 1 || i == 2) ? Hkv : H, D, false)) != ATTN_OK) return rc;
+  BwdParams p{};
+  p.B = B;
+  p.H = H;
+  p.Hkv = Hkv;
+  p.S = S;
+  p.Sp = (S + 127) / 128 * 128;
+  p.scale = scale > 0.f ? scale : 1.0f / std::sqrt(static_cast<float>(D));
+  p.c_log2 = p.scale * 1.4426950408889634f;
+  p.o = o;
+  p.dout = dout;
+  p.lse = lse;
+  p.ws = workspace;
+  p.dq = dq;
+  p.dk = dk;
+  p.dv = dv;
+  p.spin_limit = spin_limit();
+  p.err_word = err;
+  p.err_info = err + 1;
+  const cudaError_t e = launch_attn_bwd(maps, p, D, causal != 0, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "backward launch failed: %s", cudaGetErrorString(e));
+  return ok();
+}
+
 // Grouped-query prefill: bf16 inputs (qs = ks = vs = nullptr) or E4M3 codes with block scales
 // (q_scale [B, Hq, nK], k_scale and v_scale [B, Hkv, nK]).
 int run_gqa(const void* q, const void* k, const void* v, const float* qs, const float* ks, const float* vs, void* o,
@@ -558,57 +616,16 @@ size_t attn_bwd_workspace_bytes(int B, int H, int S) {
 int attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
              void* dq, void* dk, void* dv, float* workspace, size_t workspace_bytes, int B, int H, int S, int D,
              int causal, float scale, void* stream) {
-  if (o == nullptr || dout == nullptr || lse == nullptr || dq == nullptr || dk == nullptr || dv == nullptr ||
-      workspace == nullptr)
-    return fail(ATTN_ERR_INVALID_ARG, "o, dout, lse, dq, dk, dv and workspace must be non-null device pointers");
-  if (D == 256) return fail(ATTN_ERR_UNSUPPORTED, "the backward pass supports D = 64 and 128 (got 256)");
-  int rc = check_attn_args(q, k, v, dq, nullptr, B, H, S, D, causal, scale, 2);
-  if (rc != ATTN_OK) return rc;
-  if (!aligned16(o) || !aligned16(dout) || !aligned16(dk) || !aligned16(dv) || !aligned16(workspace) ||
-      (reinterpret_cast<uintptr_t>(lse) & 3u))
-    return fail(ATTN_ERR_INVALID_ARG, "tensors and workspace must be 16-byte aligned (lse 4-byte)");
-  const size_t need = attn_bwd_workspace_bytes(B, H, S);
-  if (workspace_bytes < need)
-    return fail(ATTN_ERR_INVALID_ARG, "workspace of %zu bytes is smaller than the %zu needed", workspace_bytes, need);
-  const size_t n = 2ull * B * S * H * D, nl = 4ull * B * H * S;
-  const void* ins[6] = {q, k, v, o, dout, lse};
-  const size_t in_bytes[6] = {n, n, n, n, n, nl};
-  void* outs[4] = {dq, dk, dv, workspace};
-  const size_t out_bytes[4] = {n, n, n, need};
-  for (int a = 0; a < 4; ++a) {
-    for (int i = 0; i < 6; ++i)
-      if (overlap(outs[a], out_bytes[a], ins[i], in_bytes[i]))
-        return fail(ATTN_ERR_INVALID_ARG, "an output or the workspace overlaps an input");
-    for (int c = a + 1; c < 4; ++c)
-      if (overlap(outs[a], out_bytes[a], outs[c], out_bytes[c]))
-        return fail(ATTN_ERR_INVALID_ARG, "outputs overlap each other or the workspace");
-  }
-  int* err = nullptr;
-  if ((rc = err_words(&err)) != ATTN_OK) return rc;
-  CUtensorMap maps[4];
-  const void* srcs[4] = {q, k, v, dout};
-  for (int i = 0; i < 4; ++i)
-    if ((rc = make_qkv_map(&maps[i], srcs[i], B, S, H, D, false)) != ATTN_OK) return rc;
-  BwdParams p{};
-  p.B = B;
-  p.H = H;
-  p.S = S;
-  p.Sp = (S + 127) / 128 * 128;
-  p.scale = scale > 0.f ? scale : 1.0f / std::sqrt(static_cast<float>(D));
-  p.c_log2 = p.scale * 1.4426950408889634f;
-  p.o = o;
-  p.dout = dout;
-  p.lse = lse;
-  p.ws = workspace;
-  p.dq = dq;
-  p.dk = dk;
-  p.dv = dv;
-  p.spin_limit = spin_limit();
-  p.err_word = err;
-  p.err_info = err + 1;
-  const cudaError_t e = launch_attn_bwd(maps, p, D, causal != 0, static_cast<cudaStream_t>(stream));
-  if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "backward launch failed: %s", cudaGetErrorString(e));
-  return ok();
+  return run_bwd(q, k, v, o, dout, lse, dq, dk, dv, workspace, workspace_bytes, B, H, H, S, D, causal, scale, stream);
+}
+
+int attn_bwd_gqa(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
+                 void* dq, void* dk, void* dv, float* workspace, size_t workspace_bytes, int B, int Hq, int Hkv,
+                 int S, int D, int causal, float scale, void* stream) {
+  if (Hkv < 1 || Hq < 1 || Hq % Hkv != 0)
+    return fail(ATTN_ERR_INVALID_ARG, "Hq (%d) must be a positive multiple of Hkv (%d)", Hq, Hkv);
+  return run_bwd(q, k, v, o, dout, lse, dq, dk, dv, workspace, workspace_bytes, B, Hq, Hkv, S, D, causal, scale,
+                 stream);
 }
 
 int attn_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const void* dout,
@@ -775,6 +792,6 @@ int attn_selftest_bounded_wait(long long spin_cycles, void* stream) {
   return ok();
 }
 
-int attn_version(void) { return 108; }
+int attn_version(void) { return 109; }
 
 }  // extern "C"

@@ -21,6 +21,12 @@
 //   Recomputing S and dP in both kernels costs two extra GEMMs per tile pair but needs no
 //   atomics and no fp32 dQ accumulator in device memory.
 //
+// Grouped-query attention (H query heads over Hkv key/value heads, query head h reading head
+// h / (H / Hkv)) is the same computation with each K/V head repeated over its group: dQ is
+// unchanged, and dK, dV of a key/value head are the sums over the group's query heads.  The
+// dK/dV CTA therefore belongs to (key tile, b, key/value head) and streams the query tiles of
+// every head of the group through the same ring, so the sum stays in Tensor Memory.
+//
 // Tensor Memory (512 columns): S (P over its first 64 columns) at 0, dP (dS over its first 64)
 // at 128, then the accumulators (dV, dK at 256 and 256 + D; dQ at 256).  D = 64 or 128.
 //
@@ -147,15 +153,20 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
   const uint32_t BAR_DONE = bar0 + 32 + 8u * (2 * NSTAGE);
 
   const uint32_t warp = warp_id(), lane = lane_id();
-  // CTA -> (key tile, b, h): key tile slowest, so the causal key tiles with the most query
-  // tiles start first
-  const int BH = p.B * p.H;
-  const int kt = static_cast<int>(blockIdx.x) / BH, bh = static_cast<int>(blockIdx.x) % BH;
-  const int b = bh / p.H, h = bh % p.H;
+  // CTA -> (key tile, b, key/value head): key tile slowest, so the causal key tiles with the
+  // most query tiles start first.  The query heads of the group (G = H / Hkv, head hkv * G + g)
+  // all read these keys: iteration i takes query tile j0 + i % nqt of head g = i / nqt, and
+  // dK, dV accumulate over all of them.
+  const int BH = p.B * p.Hkv, G = p.H / p.Hkv;
+  const int kt = static_cast<int>(blockIdx.x) / BH, bkv = static_cast<int>(blockIdx.x) % BH;
+  const int b = bkv / p.Hkv, hkv = bkv % p.Hkv;
   const int k0 = 128 * kt;
   const int nq = (p.S + 127) / 128;
   const int j0 = CAUSAL ? kt : 0;          // first query tile that sees these keys
-  const int ntile = nq - j0;
+  const int nqt = nq - j0;
+  const int ntile = G * nqt;
+  auto q_tile = [&](int i) { return j0 + i % nqt; };
+  auto q_head = [&](int i) { return hkv * G + i / nqt; };
 
   if (threadIdx.x == 0) {
     mbar_init(BAR_KV, 1);
@@ -182,14 +193,14 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       const uint64_t pol_res = l2_policy_evict_first(), pol_str = l2_policy_evict_last();
       mbar_arrive_expect_tx(BAR_KV, 2 * C::TILE_BYTES);
       for (int pn = 0; pn < C::NPANEL; ++pn) {
-        tma_load_4d(sK + pn * C::PANEL_BYTES, &tmK, BAR_KV, pn * C::PANEL_ELEMS, h, k0, b, pol_res);
-        tma_load_4d(sV + pn * C::PANEL_BYTES, &tmV, BAR_KV, pn * C::PANEL_ELEMS, h, k0, b, pol_res);
+        tma_load_4d(sK + pn * C::PANEL_BYTES, &tmK, BAR_KV, pn * C::PANEL_ELEMS, hkv, k0, b, pol_res);
+        tma_load_4d(sV + pn * C::PANEL_BYTES, &tmV, BAR_KV, pn * C::PANEL_ELEMS, hkv, k0, b, pol_res);
       }
       int i = 0;
       for (; i < ntile && !*abort_flag; ++i) {
         const int s = i % NSTAGE;
         if (!wait_bounded(BAR_EMPTY(s), ((i / NSTAGE) & 1) ^ 1u, ctl, WHERE_BWD_LOAD)) break;
-        const int q0 = 128 * (j0 + i);
+        const int q0 = 128 * q_tile(i), h = q_head(i), bh = b * p.H + h;
         mbar_arrive_expect_tx(BAR_FULL(s), 2 * C::TILE_BYTES + C::VEC_BYTES);
         for (int pn = 0; pn < C::NPANEL; ++pn) {
           tma_load_4d(sQ(s) + pn * C::PANEL_BYTES, &tmQ, BAR_FULL(s), pn * C::PANEL_ELEMS, h, q0, b, pol_str);
@@ -252,7 +263,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     bool ok = true;
     for (int i = 0; ok && i < ntile; ++i) {
       const int s = i % NSTAGE;
-      const int q0 = 128 * (j0 + i);
+      const int q0 = 128 * q_tile(i);
       const float* dlt = vec(s);
       const float* l2 = dlt + 128;
       // the stage's Delta / lse came by TMA: acquire them from the stage's own barrier (its
@@ -261,7 +272,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       if (!warp_wait(BAR_S, i & 1, ctl, WHERE_BWD_COMPUTE)) { ok = false; break; }
       tc_fence_after();
       // masks are needed only on the diagonal tile (causal) and the ragged last query tile
-      const bool masked = (CAUSAL && j0 + i == kt) || q0 + 128 > p.S;
+      const bool masked = (CAUSAL && q_tile(i) == kt) || q0 + 128 > p.S;
 #pragma unroll 1
       for (int c = 0; c < 4; ++c) {
         uint32_t sv[32], pv[32];
@@ -304,7 +315,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     if (ok && warp_wait(BAR_ACC, 0, ctl, WHERE_BWD_COMPUTE)) {
       tc_fence_after();
       const bool valid = key < p.S;
-      const size_t row = ((static_cast<size_t>(b) * p.S + (valid ? key : 0)) * p.H + h) * D;
+      const size_t row = ((static_cast<size_t>(b) * p.S + (valid ? key : 0)) * p.Hkv + hkv) * D;
 #pragma unroll 1
       for (int part = 0; part < 2; ++part) {           // dV, then dK (times the softmax scale)
         __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(part ? p.dk : p.dv) + row;
@@ -371,6 +382,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
   const int qt = CAUSAL ? nq - 1 - static_cast<int>(blockIdx.x) / BH : static_cast<int>(blockIdx.x) / BH;
   const int bh = static_cast<int>(blockIdx.x) % BH;
   const int b = bh / p.H, h = bh % p.H;
+  const int hkv = h / (p.H / p.Hkv);       // the key/value head this query head reads
   const int q0 = 128 * qt;
   const int ntile = CAUSAL ? qt + 1 : nq;
 
@@ -408,8 +420,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
         if (!wait_bounded(BAR_EMPTY(s), ((i / NSTAGE) & 1) ^ 1u, ctl, WHERE_BWD_LOAD)) break;
         mbar_arrive_expect_tx(BAR_FULL(s), 2 * C::TILE_BYTES);
         for (int pn = 0; pn < C::NPANEL; ++pn) {
-          tma_load_4d(sK(s) + pn * C::PANEL_BYTES, &tmK, BAR_FULL(s), pn * C::PANEL_ELEMS, h, 128 * i, b, pol_str);
-          tma_load_4d(sV(s) + pn * C::PANEL_BYTES, &tmV, BAR_FULL(s), pn * C::PANEL_ELEMS, h, 128 * i, b, pol_str);
+          tma_load_4d(sK(s) + pn * C::PANEL_BYTES, &tmK, BAR_FULL(s), pn * C::PANEL_ELEMS, hkv, 128 * i, b, pol_str);
+          tma_load_4d(sV(s) + pn * C::PANEL_BYTES, &tmV, BAR_FULL(s), pn * C::PANEL_ELEMS, hkv, 128 * i, b, pol_str);
         }
       }
       if (*abort_flag) {
@@ -553,10 +565,13 @@ cudaError_t launch_bwd_d(const CUtensorMap* maps, const BwdParams& p, cudaStream
       static_cast<const __nv_bfloat16*>(p.o), static_cast<const __nv_bfloat16*>(p.dout), p.lse, p.ws, p.B, p.H,
       p.S, p.Sp);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  const unsigned tiles = static_cast<unsigned>(p.B * p.H * ((p.S + 127) / 128));
-  bwd_dkdv_kernel<D, CAUSAL><<<tiles, C::THREADS, C::SMEM_BYTES, st>>>(maps[0], maps[1], maps[2], maps[3], p);
+  const unsigned nqt = static_cast<unsigned>((p.S + 127) / 128);
+  // dK/dV: one CTA per (key tile, b, key/value head); dQ: one per (query tile, b, query head)
+  bwd_dkdv_kernel<D, CAUSAL><<<static_cast<unsigned>(p.B * p.Hkv) * nqt, C::THREADS, C::SMEM_BYTES, st>>>(
+      maps[0], maps[1], maps[2], maps[3], p);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  bwd_dq_kernel<D, CAUSAL><<<tiles, C::THREADS, C::SMEM_BYTES, st>>>(maps[0], maps[1], maps[2], maps[3], p);
+  bwd_dq_kernel<D, CAUSAL><<<static_cast<unsigned>(p.B * p.H) * nqt, C::THREADS, C::SMEM_BYTES, st>>>(
+      maps[0], maps[1], maps[2], maps[3], p);
   return cudaGetLastError();
 }
 

@@ -74,7 +74,8 @@ cudaError_t launch_attn_decode(const CUtensorMap& tq, const CUtensorMap& tk, con
 
 // Backward pass (attn_bwd.cu).
 struct BwdParams {
-  int B, H, S;
+  int B, H, S;          // H: query heads
+  int Hkv;              // key/value heads (H a multiple of Hkv; query head h reads h / (H / Hkv))
   int Sp;               // S rounded up to 128: row stride of the workspace
   float c_log2;         // softmax scale * log2(e)
   float scale;          // softmax scale
@@ -83,7 +84,7 @@ struct BwdParams {
   const float* lse;     // [B, H, S] fp32, the forward's log-sum-exp
   float* ws;            // [B*H][2][Sp] fp32: Delta, lse*log2(e)
   void* dq;             // [B, S, H, D] bf16 outputs
-  void* dk;
+  void* dk;             // [B, S, Hkv, D] bf16
   void* dv;
   long long spin_limit;
   int* err_word;
@@ -95,7 +96,8 @@ struct BwdParams {
 constexpr size_t NOALLOC_BWD_SCRATCH_BYTES = size_t(16) << 20;
 cudaError_t noalloc_bwd_scratch(float** out);
 
-// Delta kernel, dK/dV kernel, dQ kernel on `st`.  maps = Q, K, V, dO ([B, S, H, D] bf16 maps).
+// Delta kernel, dK/dV kernel, dQ kernel on `st`.  maps = Q, K, V, dO (bf16 maps: Q and dO over H
+// heads, K and V over Hkv).
 cudaError_t launch_attn_bwd(const CUtensorMap* maps, const BwdParams& p, int D, bool causal, cudaStream_t st);
 
 struct QuantParams {

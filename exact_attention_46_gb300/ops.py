@@ -12,7 +12,8 @@ import torch
 from . import _lib
 
 __all__ = ["attn_fwd", "attn_fwd_fp8", "attn_fwd_varlen", "attn_fwd_varlen_fp8", "attn_fwd_gqa",
-           "attn_fwd_gqa_fp8", "attn_decode", "attn_decode_fp8", "attn_bwd", "hadamard_rotate_quant_fp8",
+           "attn_fwd_gqa_fp8", "attn_decode", "attn_decode_fp8", "attn_bwd", "attn_bwd_gqa",
+           "hadamard_rotate_quant_fp8",
            "hadamard_rotate_quant_fp8_varlen", "rope_cos_sin_table", "rope_hadamard_rotate_quant_fp8",
            "rope_hadamard_rotate_quant_fp8_varlen", "varlen_scale_blocks", "block_count", "check",
            "set_spin_limit", "selftest_bounded_wait", "ATTN_BF16", "ATTN_FP8_E4M3"]
@@ -329,6 +330,33 @@ def attn_bwd(q, k, v, o, lse, dout, causal=False, scale=0.0, dq=None, dk=None, d
     _lib.call("attn_bwd", _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv),
               _ptr(workspace), workspace.numel() * workspace.element_size(), B, H, S, D, int(bool(causal)),
               float(scale), _stream(stream))
+    return dq, dk, dv
+
+
+def attn_bwd_gqa(q, k, v, o, lse, dout, causal=False, scale=0.0, dq=None, dk=None, dv=None, workspace=None,
+                 stream=None):
+    """Gradients of attn_fwd_gqa: dq bf16 [B, S, Hq, D]; dk, dv bf16 [B, S, Hkv, D], summed over each group."""
+    dev = _inputs(("q", "k", "v", "o", "dout"), (q, k, v, o, dout), _BF16, 4)
+    B, S, Hq, D = q.shape
+    Hkv = k.shape[2]
+    for n, t in (("k", k), ("v", v)):
+        _arg(t, n, _BF16, shape=(B, S, Hkv, D))
+    for n, t in (("o", o), ("dout", dout)):
+        _arg(t, n, _BF16, shape=q.shape)
+    _arg(lse, "lse", _F32, shape=(B, Hq, S), device=dev)
+    _opt(dq, "dq", _BF16, shape=q.shape, device=dev)
+    for n, t in (("dk", dk), ("dv", dv)):
+        _opt(t, n, _BF16, shape=k.shape, device=dev)
+    _opt(workspace, "workspace", _F32, dim=1, device=dev)
+    nbytes = _lib.load().attn_bwd_workspace_bytes(B, Hq, S)
+    if workspace is None:
+        workspace = torch.empty(max(nbytes // 4, 1), dtype=torch.float32, device=dev)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    _lib.call("attn_bwd_gqa", _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse), _ptr(dq), _ptr(dk),
+              _ptr(dv), _ptr(workspace), workspace.numel() * workspace.element_size(), B, Hq, Hkv, S, D,
+              int(bool(causal)), float(scale), _stream(stream))
     return dq, dk, dv
 
 

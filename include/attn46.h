@@ -259,6 +259,27 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const v
              void* stream);
 
 /*
+ * attn_bwd_gqa -- attn_bwd for grouped-query attention: the gradients of
+ *   attn_fwd_gqa (Hq query heads over Hkv key/value heads, query head h
+ *   reading key/value head h / (Hq / Hkv)).  This is the backward of
+ *   multi-head attention with each key/value head repeated over its group of
+ *   G = Hq / Hkv query heads; dQ is that backward's dQ, and dK, dV of a
+ *   key/value head are the sums of the repeated heads' dK, dV over the group.
+ *   q, o, dout : [B, S, Hq, D] bf16.   k, v : [B, S, Hkv, D] bf16.
+ *   lse        : [B, Hq, S] fp32 (attn_fwd_gqa's).
+ *   dq         : [B, S, Hq, D] bf16 output; dk, dv : [B, S, Hkv, D] bf16.
+ *   workspace  : workspace_bytes >= attn_bwd_workspace_bytes(B, Hq, S).
+ *   Hq a positive multiple of Hkv, else ATTN_ERR_INVALID_ARG; Hkv = Hq gives
+ *   exactly attn_bwd.  Everything else as attn_bwd.  The group's sum is
+ *   formed in fp32 inside one CTA per (128 keys, b, key/value head) and
+ *   rounded to bf16 once.
+ */
+int attn_bwd_gqa(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                 const float* lse, void* dq, void* dk, void* dv, float* workspace,
+                 size_t workspace_bytes, int B, int Hq, int Hkv, int S, int D, int causal,
+                 float scale, void* stream);
+
+/*
  * attn_bwd_noalloc -- attn_bwd without a caller workspace.  The paper has no
  *   counterpart; this is a convenience of this library.
  *   For callers that cannot allocate device memory where they run the

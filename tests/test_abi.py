@@ -40,7 +40,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_version(lib):
-    assert lib.attn_version() == 108
+    assert lib.attn_version() == 109
 
 
 FAKE = 1 << 20   # 16-byte aligned non-null fake device addresses: never dereferenced
@@ -130,6 +130,28 @@ def test_backward_rejects_bad_arguments(lib):
     bad(6, FAKE * 3)              # dq aliases v
     bad(9, FAKE * 8)              # workspace on dk
     bad(4, FAKE * 5 + 8)          # misaligned dout
+
+
+def test_grouped_query_backward_rejects_bad_arguments(lib):
+    f = lib.attn_bwd_gqa
+    B, Hq, Hkv, S, D = 1, 8, 2, 300, 128
+    ws = lib.attn_bwd_workspace_bytes(B, Hq, S)
+    kv_bytes = 2 * B * S * Hkv * D        # 153,600: dk, dv sized by the key/value heads
+    ok = [FAKE, FAKE * 2, FAKE * 3, FAKE * 4, FAKE * 5, FAKE * 6, FAKE * 7, FAKE * 8, FAKE * 9, FAKE * 10, ws,
+          B, Hq, Hkv, S, D, 0, 0.0, None]
+    def bad(i, val, code=1):
+        a = list(ok)
+        a[i] = val
+        assert f(*a) == code, (i, val)
+    bad(13, 3)                    # Hq not a multiple of Hkv
+    bad(13, 0)                    # Hkv = 0
+    bad(12, 0)                    # Hq = 0
+    bad(13, 16)                   # Hkv > Hq
+    bad(15, 256, 2)               # D = 256 unsupported here
+    bad(10, lib.attn_bwd_workspace_bytes(B, Hkv, S))   # workspace sized by the wrong head count
+    bad(7, FAKE * 2)              # dk aliases k
+    bad(8, FAKE * 8 + kv_bytes - 16)   # dv overlaps the last row of dk
+    bad(6, FAKE * 3 - 16)         # dq runs into v
 
 
 def test_backward_without_workspace_rejects_problems_beyond_its_scratch(lib):

@@ -24,3 +24,5 @@ def test_first_argument_checks():
         ops.attn_fwd(bf.transpose(1, 3), bf, bf)
     with pytest.raises(ValueError, match="CUDA"):
         ops.attn_fwd(bf, bf, bf)
+    with pytest.raises(ValueError, match="dtype"):
+        ops.attn_bwd_gqa(x32, bf, bf, bf, None, bf)                   # q must be bf16
