@@ -40,6 +40,8 @@ SIGNATURES = {
     "attn_get_last_error": (ctypes.c_char_p, []),
     "attn_check": (_I, [_P]),
     "attn_set_spin_limit": (None, [_LL]),
+    "attn_set_key_split": (None, [_I]),
+    "attn_key_split_plan": (_I, [_LL, _I, _I, _I, _P]),
     "attn_selftest_bounded_wait": (_I, [_LL, _P]),
     "attn_version": (_I, []),
 }

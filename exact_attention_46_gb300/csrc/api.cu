@@ -126,6 +126,122 @@ bool overlap(const void* a, size_t na, const void* b, size_t nb) {
   return x < y + nb && y < x + na;
 }
 
+// ---- key-split tail of the fixed-length, non-causal forward (attn_kernel.cuh) ----
+
+std::atomic<int> g_key_split_max{KEY_SPLIT_MAX_PARTS};
+
+struct SplitPlan {
+  long long n_whole, n_tail;
+  int n_parts;
+};
+
+// n_items equal items on `sms` persistent CTAs take ceil(n_items / sms) rounds, the last one
+// partly idle.  Cutting each of its n_tail = n_items mod sms blocks into s key ranges makes it
+// ceil(n_tail * s / sms) rounds of ranges of at most ceil(nK / s) key tiles.  Measured on
+// GB300, an item costs about KEY_SPLIT_ITEM_TILES key tiles on top of its own (start and
+// epilogue), and the merge about KEY_SPLIT_MERGE_TILES.  In key tiles, the last round costs
+// nK + ITEM unsplit and ceil(n_tail s / sms) (ceil(nK / s) + ITEM) + MERGE split; the plan
+// takes the cheapest s <= max_parts (every range at least KEY_SPLIT_MIN_TILES tiles) if it
+// costs at most 85 % of the unsplit round.  Problems without one full round are not split.
+SplitPlan key_split_plan(long long n_items, int sms, int nK, int max_parts) {
+  SplitPlan sp{n_items, 0, 1};
+  if (sms < 1 || n_items <= sms) return sp;
+  const long long tail = n_items % sms;
+  if (tail == 0) return sp;
+  const long long whole = nK + KEY_SPLIT_ITEM_TILES;
+  int best = 1;
+  long long best_cost = whole;
+  for (int s = 2; s <= max_parts && s <= KEY_SPLIT_MAX_PARTS; ++s) {
+    if (nK < KEY_SPLIT_MIN_TILES * s) break;
+    const long long rounds = (tail * s + sms - 1) / sms;
+    const long long cost = rounds * ((nK + s - 1) / s + KEY_SPLIT_ITEM_TILES) + KEY_SPLIT_MERGE_TILES;
+    if (cost < best_cost) {
+      best = s;
+      best_cost = cost;
+    }
+  }
+  if (best == 1 || 100 * best_cost > 85 * whole) return sp;
+  sp.n_whole = n_items - tail;
+  sp.n_tail = tail;
+  sp.n_parts = best;
+  return sp;
+}
+
+// Per-device pool of split scratch; freed blocks stay in the pool for the next launch.
+cudaMemPool_t g_split_pool[kMaxDevices] = {};
+
+cudaError_t split_pool(int dev, cudaMemPool_t* out) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (g_split_pool[dev] == nullptr) {
+    cudaMemPoolProps props{};
+    props.allocType = cudaMemAllocationTypePinned;
+    props.location.type = cudaMemLocationTypeDevice;
+    props.location.id = dev;
+    cudaMemPool_t pool = nullptr;
+    cudaError_t e = cudaMemPoolCreate(&pool, &props);
+    if (e != cudaSuccess) return e;
+    uint64_t keep = ~0ull;
+    e = cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &keep);
+    if (e != cudaSuccess) {
+      cudaMemPoolDestroy(pool);
+      return e;
+    }
+    g_split_pool[dev] = pool;
+  }
+  *out = g_split_pool[dev];
+  return cudaSuccess;
+}
+
+// The split plan of one launch and its scratch, handed back to the pool on the launch's stream
+// when the launching call returns (after the launch is queued).
+struct SplitScratch {
+  SplitParams sp{0, 0, 1, nullptr, nullptr};
+  void* ptr = nullptr;
+  cudaStream_t st = nullptr;
+  const SplitParams* plan() const { return sp.n_parts > 1 ? &sp : nullptr; }
+  ~SplitScratch() {
+    if (ptr != nullptr) cudaFreeAsync(ptr, st);
+  }
+};
+
+// Plans the split for p (nQB, H, B, nK set) and sets up its scratch on `st`.  Causal launches,
+// launches under stream capture, and launches whose scratch cannot be had run unsplit.
+int prepare_key_split(const AttnParams* p, int D, int causal, cudaStream_t st, SplitScratch* sc) {
+  const int max_parts = g_key_split_max.load();
+  if (causal || max_parts < 2) return ATTN_OK;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return ATTN_OK;
+  }
+  const SplitPlan sp = key_split_plan(1ll * p->nQB * p->H * p->B, sms, p->nK, max_parts);
+  if (sp.n_parts < 2) return ATTN_OK;
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(st, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone) {
+    (void)cudaGetLastError();
+    return ATTN_OK;
+  }
+  const size_t rows = 128ull * attn_q_tiles(D) * sp.n_tail * sp.n_parts;
+  const size_t o_bytes = rows * D * 4, l_bytes = rows * 4;
+  cudaMemPool_t pool = nullptr;
+  void* ptr = nullptr;
+  if (split_pool(dev, &pool) != cudaSuccess ||
+      cudaMallocFromPoolAsync(&ptr, o_bytes + l_bytes, pool, st) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return ATTN_OK;
+  }
+  sc->ptr = ptr;
+  sc->st = st;
+  char* base = static_cast<char*>(ptr);
+  sc->sp.n_whole = static_cast<int>(sp.n_whole);
+  sc->sp.n_tail = static_cast<int>(sp.n_tail);
+  sc->sp.n_parts = sp.n_parts;
+  sc->sp.part_o = reinterpret_cast<float*>(base);
+  sc->sp.part_l = reinterpret_cast<float*>(base + o_bytes);
+  return ATTN_OK;
+}
+
 // Shape and pointer checks shared by the attention entry points.
 int check_attn_args(const void* q, const void* k, const void* v, const void* o, const float* lse,
                     int B, int H, int S, int D, int causal, float scale, int esz) {
@@ -164,15 +280,15 @@ int check_attn_args(const void* q, const void* k, const void* v, const void* o, 
 
 template <bool FP8>
 int dispatch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-             const AttnParams& p, int D, int causal, cudaStream_t st) {
+             const AttnParams& p, int D, int causal, cudaStream_t st, const SplitParams* sp) {
   cudaError_t e = cudaErrorInvalidValue;
   switch (D * 2 + causal) {
-    case 64 * 2 + 0: e = launch_attn<64, FP8, false>(tq, tk, tv, p, st); break;
-    case 64 * 2 + 1: e = launch_attn<64, FP8, true>(tq, tk, tv, p, st); break;
-    case 128 * 2 + 0: e = launch_attn<128, FP8, false>(tq, tk, tv, p, st); break;
-    case 128 * 2 + 1: e = launch_attn<128, FP8, true>(tq, tk, tv, p, st); break;
-    case 256 * 2 + 0: e = launch_attn<256, FP8, false>(tq, tk, tv, p, st); break;
-    case 256 * 2 + 1: e = launch_attn<256, FP8, true>(tq, tk, tv, p, st); break;
+    case 64 * 2 + 0: e = launch_attn<64, FP8, false>(tq, tk, tv, p, st, sp); break;
+    case 64 * 2 + 1: e = launch_attn<64, FP8, true>(tq, tk, tv, p, st, nullptr); break;
+    case 128 * 2 + 0: e = launch_attn<128, FP8, false>(tq, tk, tv, p, st, sp); break;
+    case 128 * 2 + 1: e = launch_attn<128, FP8, true>(tq, tk, tv, p, st, nullptr); break;
+    case 256 * 2 + 0: e = launch_attn<256, FP8, false>(tq, tk, tv, p, st, sp); break;
+    case 256 * 2 + 1: e = launch_attn<256, FP8, true>(tq, tk, tv, p, st, nullptr); break;
     default: break;
   }
   if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "attention launch failed: %s", cudaGetErrorString(e));
@@ -209,16 +325,18 @@ int run_attn(const void* q, const void* k, const void* v, const float* qs, const
   p.err_info = err + 1;
   p.kv_group = 1;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  return fp8 ? dispatch<true>(tq, tk, tv, p, D, causal, st)
-             : dispatch<false>(tq, tk, tv, p, D, causal, st);
+  SplitScratch scratch;
+  if ((rc = prepare_key_split(&p, D, causal, st, &scratch)) != ATTN_OK) return rc;
+  return fp8 ? dispatch<true>(tq, tk, tv, p, D, causal, st, scratch.plan())
+             : dispatch<false>(tq, tk, tv, p, D, causal, st, scratch.plan());
 }
 
 template <bool FP8, bool CAUSAL>
 cudaError_t launch_varlen(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                           const AttnParams& p, int D, cudaStream_t st) {
-  return D == 64    ? launch_attn<64, FP8, CAUSAL, true>(tq, tk, tv, p, st)
-         : D == 128 ? launch_attn<128, FP8, CAUSAL, true>(tq, tk, tv, p, st)
-                    : launch_attn<256, FP8, CAUSAL, true>(tq, tk, tv, p, st);
+  return D == 64    ? launch_attn<64, FP8, CAUSAL, true>(tq, tk, tv, p, st, nullptr)
+         : D == 128 ? launch_attn<128, FP8, CAUSAL, true>(tq, tk, tv, p, st, nullptr)
+                    : launch_attn<256, FP8, CAUSAL, true>(tq, tk, tv, p, st, nullptr);
 }
 
 // Scale entries per head of a packed batch's block scales.
@@ -444,7 +562,10 @@ int run_gqa(const void* q, const void* k, const void* v, const float* qs, const 
   p.err_info = err + 1;
   p.kv_group = Hq / Hkv;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  return fp8 ? dispatch<true>(tq, tk, tv, p, D, causal, st) : dispatch<false>(tq, tk, tv, p, D, causal, st);
+  SplitScratch scratch;
+  if ((rc = prepare_key_split(&p, D, causal, st, &scratch)) != ATTN_OK) return rc;
+  return fp8 ? dispatch<true>(tq, tk, tv, p, D, causal, st, scratch.plan())
+             : dispatch<false>(tq, tk, tv, p, D, causal, st, scratch.plan());
 }
 
 }  // namespace
@@ -792,6 +913,20 @@ int attn_selftest_bounded_wait(long long spin_cycles, void* stream) {
   return ok();
 }
 
-int attn_version(void) { return 109; }
+int attn_version(void) { return 110; }
+
+void attn_set_key_split(int max_parts) {
+  g_key_split_max.store(max_parts < 1 ? 1 : (max_parts > KEY_SPLIT_MAX_PARTS ? KEY_SPLIT_MAX_PARTS : max_parts));
+}
+
+int attn_key_split_plan(long long n_items, int sms, int key_tiles, int max_parts, long long* out) {
+  if (out == nullptr || n_items < 0 || sms < 1 || key_tiles < 0)
+    return fail(ATTN_ERR_INVALID_ARG, "need out != NULL, n_items >= 0, sms >= 1, key_tiles >= 0");
+  const SplitPlan sp = key_split_plan(n_items, sms, key_tiles, max_parts);
+  out[0] = sp.n_whole;
+  out[1] = sp.n_tail;
+  out[2] = sp.n_parts;
+  return ok();
+}
 
 }  // extern "C"

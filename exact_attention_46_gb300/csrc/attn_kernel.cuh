@@ -53,6 +53,16 @@
 //   sequence are masked like the ragged tail of a fixed length, and rows past the sequence
 //   are never stored.
 //
+//   Key-split tail (fixed length, not causal): every item is the same amount of work, so a
+//   persistent grid of P CTAs runs ceil(N / P) rounds for N items and the last round is
+//   partly idle.  When the host plans a split, the first n_whole = P * floor(N / P) items run
+//   whole and each of the last n_tail items is cut into n_parts ranges of key tiles, so the
+//   tail takes ceil(n_tail * n_parts / P) rounds of 1 / n_parts the length.  A part writes its
+//   normalised partial O (fp32) and lse (log2 units) to a scratch buffer; split_merge_kernel,
+//   launched next on the same stream, merges each cut row in part order (lse = log2 sum
+//   2^lse_p, O = sum 2^(lse_p - lse) O_p) with a warp per row and the lanes across the
+//   columns, so its reads are whole row segments.
+
 // Every mbarrier wait is bounded (ptx.cuh, wait_bounded): a wait that runs out records
 // ATTN_ERR_TIMEOUT in the device error word, raises the CTA's abort flag, and every role then
 // drains its in-flight copies / MMAs and leaves through the common exit, which frees Tensor
@@ -123,14 +133,117 @@ __device__ __forceinline__ void wait_drain(uint32_t bar, uint32_t parity, long l
   }
 }
 
+// Epilogue of one key range of a split tail block: the warp's 32 rows of partial O
+// (accumulator * inv_l, fp32) and their lse (log2 units) go to the scratch, kept in L2 by an
+// evict-last hint for split_merge_kernel, and O_t goes back to the MMA warp.  Rows past the
+// sequence (valid = false) store nothing.
+template <int D, int NT>
+__device__ __noinline__ void split_store(const SplitParams& sp, int slot, int part, int t, int row_local, bool valid,
+                                         uint32_t o_addr, float inv_l, float lse2, uint32_t bar_o_empty) {
+  constexpr int ROWS = 128 * NT;
+  const uint32_t lane = lane_id();
+  const size_t r = (static_cast<size_t>(slot) * sp.n_parts + part) * ROWS + 128 * t + row_local;
+  float* po = sp.part_o + r * D;
+#pragma unroll 1
+  for (int c = 0; c < D / 32; ++c) {
+    uint32_t o[32];
+    tmem_ld32(o_addr + 32u * c, o);
+    tmem_wait_ld();
+#pragma unroll
+    for (int i = 0; i < 32; ++i) reg_fence(o[i]);
+    if (valid) {
+#pragma unroll
+      for (int v4 = 0; v4 < 8; ++v4)
+        __stcg(reinterpret_cast<float4*>(po + 32 * c + 4 * v4),
+               make_float4(__uint_as_float(o[4 * v4]) * inv_l, __uint_as_float(o[4 * v4 + 1]) * inv_l,
+                           __uint_as_float(o[4 * v4 + 2]) * inv_l, __uint_as_float(o[4 * v4 + 3]) * inv_l));
+    }
+  }
+  tc_fence_before();
+  __syncwarp();
+  if (lane == 0) mbar_arrive(bar_o_empty);
+  if (valid) sp.part_l[r] = lse2;
+}
+
+// Merge of the split tail blocks, after the attention kernel on the same stream: one warp per
+// row of a cut block, lanes across the columns.  L = log2 sum_p 2^L_p, O = sum_p 2^(L_p - L) O_p
+// in part order (bf16), lse = L ln 2.
+template <int D, int NT>
+__global__ void __launch_bounds__(256) split_merge_kernel(const AttnParams p, const SplitParams sp) {
+  constexpr int ROWS = 128 * NT;
+  constexpr int CPL = D / 32;
+  const long long wid = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int lane = static_cast<int>(threadIdx.x & 31);
+  if (wid >= static_cast<long long>(sp.n_tail) * ROWS) return;
+  const int slot = static_cast<int>(wid / ROWS), ir = static_cast<int>(wid % ROWS);
+  const int id = sp.n_whole + slot;                // the cut block's item (not causal)
+  const int qb = id % p.nQB, hb = id / p.nQB;
+  const int h = hb % p.H, b = hb / p.H;
+  const int row = qb * ROWS + ir;
+  if (row >= p.S) return;
+  const uint64_t drop = l2_policy_evict_first();
+  const size_t r0 = static_cast<size_t>(slot) * sp.n_parts * ROWS + ir;   // part 0's row
+  float lp[KEY_SPLIT_MAX_PARTS];
+  float lmax = -INFINITY;
+#pragma unroll
+  for (int q = 0; q < KEY_SPLIT_MAX_PARTS; ++q) {
+    lp[q] = q < sp.n_parts ? __ldcg(sp.part_l + r0 + static_cast<size_t>(q) * ROWS) : -INFINITY;
+    lmax = fmaxf(lmax, lp[q]);
+  }
+  float sum = 0.f;
+#pragma unroll
+  for (int q = 0; q < KEY_SPLIT_MAX_PARTS; ++q) sum += q < sp.n_parts ? ex2(lp[q] - lmax) : 0.f;
+  const float L = lmax + __log2f(sum);
+  float x[KEY_SPLIT_MAX_PARTS][CPL];
+#pragma unroll
+  for (int q = 0; q < KEY_SPLIT_MAX_PARTS; ++q) {
+    const float* src = sp.part_o + (r0 + static_cast<size_t>(q) * ROWS) * D + CPL * lane;
+#pragma unroll
+    for (int e = 0; e < CPL; e += (CPL >= 4 ? 4 : 2)) {
+      if (q < sp.n_parts) {
+        if constexpr (CPL >= 4) {
+          const float4 v = ld_cg_v4_hint(src + e, drop);
+          x[q][e] = v.x; x[q][e + 1] = v.y; x[q][e + 2] = v.z; x[q][e + 3] = v.w;
+        } else {
+          const float2 v = ld_cg_v2_hint(src + e, drop);
+          x[q][e] = v.x; x[q][e + 1] = v.y;
+        }
+      } else {
+#pragma unroll
+        for (int f = 0; f < (CPL >= 4 ? 4 : 2); ++f) x[q][e + f] = 0.f;
+      }
+    }
+  }
+  float acc[CPL];
+#pragma unroll
+  for (int e = 0; e < CPL; ++e) acc[e] = 0.f;
+#pragma unroll
+  for (int q = 0; q < KEY_SPLIT_MAX_PARTS; ++q) {
+    const float w = q < sp.n_parts ? ex2(lp[q] - L) : 0.f;
+#pragma unroll
+    for (int e = 0; e < CPL; ++e) acc[e] = fmaf(w, x[q][e], acc[e]);
+  }
+  uint32_t pk[CPL / 2];
+#pragma unroll
+  for (int e = 0; e < CPL / 2; ++e) pk[e] = pack_bf16x2(acc[2 * e], acc[2 * e + 1]);
+  const size_t tok = static_cast<size_t>(b) * p.S + row;
+  __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(p.o) + (tok * p.H + h) * D + CPL * lane;
+  if constexpr (CPL == 2) *reinterpret_cast<uint32_t*>(dst) = pk[0];
+  else if constexpr (CPL == 4) *reinterpret_cast<uint2*>(dst) = make_uint2(pk[0], pk[1]);
+  else *reinterpret_cast<uint4*>(dst) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+  if (lane == 0 && p.lse != nullptr) p.lse[static_cast<size_t>(hb) * p.S + row] = L * LN2;
+}
+
 // Shared memory a VARLEN launch adds: offsets [n_seq + 1], two per-level arrays
 // [n_levels + 1], the item count, and the sorted sequence order (16-bit) [n_seq].
 constexpr int VARLEN_SMEM_BYTES = ((VARLEN_MAX_SEQ + 1) + 2 * (VARLEN_MAX_LEVELS + 1) + 4) * 4 + VARLEN_MAX_SEQ * 2;
 
-template <int D, bool FP8, bool CAUSAL, bool VARLEN>
+// SPLIT: the launch has a key-split tail (fixed length, not causal).  The other launches use
+// the SPLIT = false instantiation, which has none of its code.
+template <int D, bool FP8, bool CAUSAL, bool VARLEN, bool SPLIT>
 __global__ void __launch_bounds__(AttnCfg<D, FP8>::THREADS, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                    const __grid_constant__ CUtensorMap tmV, const AttnParams p) {
+                    const __grid_constant__ CUtensorMap tmV, const AttnParams p, const SplitParams sp) {
   using C = AttnCfg<D, FP8>;
   constexpr int NT = C::NT;
   constexpr int NSLOT = C::NSLOT;
@@ -285,15 +398,18 @@ __global__ void __launch_bounds__(AttnCfg<D, FP8>::THREADS, 1)
   // n*G + k in even rounds n and n*G + G-1-k in odd rounds (zig-zag), G = gridDim.x.
   const int HB = p.H * p.B;
   int n_items;
-  if constexpr (VARLEN) n_items = *s_nitems; else n_items = p.nQB * HB;
+  if constexpr (VARLEN) n_items = *s_nitems;
+  else if constexpr (SPLIT) n_items = sp.n_whole + sp.n_tail * sp.n_parts;
+  else n_items = p.nQB * HB;
   const int G = static_cast<int>(gridDim.x);
   const int k_cta = static_cast<int>(blockIdx.x);
   auto item_of = [&](int n) { return n * G + ((n & 1) ? (G - 1 - k_cta) : k_cta); };
   // An item: query rows q0 .. q0 + 128 NT - 1 of sequence (b, h), positions counted from the
   // sequence's first token.  VARLEN: the sequence is tokens s0 .. s0 + len - 1 of the packed
   // axis; otherwise it is batch b and len = S (read from the parameters, not kept).
-  // sb (VARLEN with FP8): the sequence's first scale block, cu[s] / 128 + s
-  struct Item { int h, b, q0, hb, nmax, s0, len, sb; int n[NT]; };
+  // sb (VARLEN with FP8): the sequence's first scale block, cu[s] / 128 + s.  SPLIT only: key
+  // tiles kt0 .. kt1-1 are the item's (all of them unless it is part `part` of tail block `slot`).
+  struct Item { int h, b, q0, hb, nmax, s0, len, sb, kt0, kt1, part, slot; int n[NT]; };
   auto seq_len = [&](const Item& it) {
     if constexpr (VARLEN) return it.len; else return p.S;
   };
@@ -305,6 +421,10 @@ __global__ void __launch_bounds__(AttnCfg<D, FP8>::THREADS, 1)
   };
   auto decode = [&](int item, Item& it) {
     int qb;
+    if constexpr (SPLIT) {
+      it.part = -1;
+      it.slot = 0;
+    }
     if constexpr (VARLEN) {
       // lowest level (causal) or block count (otherwise) whose first item is <= item
       int lo = CAUSAL ? 0 : 1, hi = CAUSAL ? p.n_levels - 1 : p.n_levels;
@@ -332,22 +452,39 @@ __global__ void __launch_bounds__(AttnCfg<D, FP8>::THREADS, 1)
       it.s0 = s0;
       it.sb = (s0 >> 7) + sq;
     } else {
+      int id = item;
+      if constexpr (SPLIT) {
+        if (item >= sp.n_whole) {
+          const int u = item - sp.n_whole;
+          it.part = u / sp.n_tail;
+          it.slot = u % sp.n_tail;
+          id = sp.n_whole + it.slot;
+        }
+      }
       if (CAUSAL) {
-        qb = p.nQB - 1 - item / HB;
-        it.hb = item % HB;
+        qb = p.nQB - 1 - id / HB;
+        it.hb = id % HB;
       } else {
-        qb = item % p.nQB;
-        it.hb = item / p.nQB;
+        qb = id % p.nQB;
+        it.hb = id / p.nQB;
       }
       it.h = it.hb % p.H;
       it.b = it.hb / p.H;
     }
     it.q0 = qb * 128 * NT;
+    if constexpr (SPLIT) {
+      it.kt0 = 0;
+      it.kt1 = key_tiles(it);
+      if (it.part >= 0) {
+        it.kt0 = it.part * p.nK / sp.n_parts;
+        it.kt1 = (it.part + 1) * p.nK / sp.n_parts;
+      }
+    }
     it.nmax = 0;
 #pragma unroll
     for (int t = 0; t < NT; ++t) {
       const int r0 = it.q0 + 128 * t;
-      it.n[t] = (r0 >= seq_len(it)) ? 0 : (CAUSAL ? (r0 / 128 + 1) : key_tiles(it));
+      it.n[t] = (r0 >= seq_len(it)) ? 0 : (CAUSAL ? (r0 / 128 + 1) : (SPLIT ? it.kt1 - it.kt0 : key_tiles(it)));
       it.nmax = it.n[t] > it.nmax ? it.n[t] : it.nmax;
     }
   };
@@ -391,7 +528,7 @@ __global__ void __launch_bounds__(AttnCfg<D, FP8>::THREADS, 1)
 #pragma unroll
             for (int pn = 0; pn < C::NPANEL; ++pn)
               tma_load_4d(sKV + slot * C::TILE_BYTES + pn * C::PANEL_BYTES, m, BAR_KV_FULL(slot),
-                          pn * C::PANEL_ELEMS, kvh, tma_row(it, 128 * j), it.b, pol_kv);
+                          pn * C::PANEL_ELEMS, kvh, tma_row(it, 128 * ((SPLIT ? it.kt0 : 0) + j)), it.b, pol_kv);
             ++issued;
           }
         }
@@ -530,7 +667,7 @@ __global__ void __launch_bounds__(AttnCfg<D, FP8>::THREADS, 1)
       Item it;
       decode(item, it);
       const int r0 = it.q0 + 128 * t;
-      const int nt = (r0 >= seq_len(it)) ? 0 : (CAUSAL ? (r0 / 128 + 1) : key_tiles(it));
+      const int nt = SPLIT ? it.n[t] : ((r0 >= seq_len(it)) ? 0 : (CAUSAL ? (r0 / 128 + 1) : key_tiles(it)));
       if (nt == 0) continue;
       const int row = it.q0 + 128 * t + row_local;
       // FP8 block scales: (b*H + h) * nK; the K/V ones belong to the shared key/value head,
@@ -545,12 +682,18 @@ __global__ void __launch_bounds__(AttnCfg<D, FP8>::THREADS, 1)
         if (p.q_scale != nullptr) sq = p.q_scale[blk_base + (it.q0 + 128 * t) / 128];
         if (p.v_scale != nullptr) {
           sv_max = 0.f;
-          for (int j = static_cast<int>(lane); j < key_tiles(it); j += 32) sv_max = fmaxf(sv_max, p.v_scale[kv_base + j]);
+          const int j0 = SPLIT ? it.kt0 : 0, j1 = SPLIT ? it.kt1 : key_tiles(it);
+          for (int j = j0 + static_cast<int>(lane); j < j1; j += 32) sv_max = fmaxf(sv_max, p.v_scale[kv_base + j]);
 #pragma unroll
           for (int o = 16; o > 0; o >>= 1) sv_max = fmaxf(sv_max, __shfl_xor_sync(0xffffffffu, sv_max, o));
           sv_max = fmaxf(sv_max, 0x1p-96f);  // every value scale 0: O = 0, l still counts
         }
       }
+
+      // SPLIT: this item's key tiles start at kt0; without the causal mask only the sequence's
+      // last key tile can be ragged, and it is the item's last tile when the item reaches it
+      const size_t kv_tile0 = kv_base + (SPLIT ? it.kt0 : 0);
+      const bool ragged_end = SPLIT && it.kt1 == key_tiles(it) && (seq_len(it) & 127) != 0;
 
       float m_run = -INFINITY;
       float l_run = 0.f;
@@ -558,8 +701,8 @@ __global__ void __launch_bounds__(AttnCfg<D, FP8>::THREADS, 1)
         // Per-tile FP8 scales are read before waiting for S, so the loads overlap the wait.
         float cmul = p.c_log2, bias = 0.f, inv_r = 1.f;
         if (FP8) {
-          const float sk = p.k_scale != nullptr ? p.k_scale[kv_base + j] : 1.f;
-          const float sv_raw = p.v_scale != nullptr ? p.v_scale[kv_base + j] : 1.f;
+          const float sk = p.k_scale != nullptr ? p.k_scale[kv_tile0 + j] : 1.f;
+          const float sv_raw = p.v_scale != nullptr ? p.v_scale[kv_tile0 + j] : 1.f;
           // a zero scale (a block of zeros) as 2^-30 of the largest: its numerators vanish in E4M3,
           // the row sum still takes them at full weight
           const float sv = fmaxf(sv_raw, sv_max * 0x1p-30f);
@@ -580,8 +723,10 @@ __global__ void __launch_bounds__(AttnCfg<D, FP8>::THREADS, 1)
           for (int i = 0; i < 32; ++i) reg_fence(sr[c][i]);
 
         // masks: causal diagonal tile, or the ragged last key tile
-        if (CAUSAL ? (j == nt - 1) : (j == key_tiles(it) - 1 && (seq_len(it) & 127) != 0)) {
-          const int lim = CAUSAL ? (row - 128 * j) : (seq_len(it) - 128 * j - 1);   // last visible column
+        if (SPLIT ? (j == nt - 1 && ragged_end)
+                  : (CAUSAL ? (j == nt - 1) : (j == key_tiles(it) - 1 && (seq_len(it) & 127) != 0))) {
+          // last visible column
+          const int lim = CAUSAL ? (row - 128 * j) : (SPLIT ? ((seq_len(it) - 1) & 127) : (seq_len(it) - 128 * j - 1));
 #pragma unroll
           for (int c = 0; c < 4; ++c)
 #pragma unroll
@@ -712,6 +857,15 @@ __global__ void __launch_bounds__(AttnCfg<D, FP8>::THREADS, 1)
       if constexpr (VARLEN) tok = static_cast<size_t>(it.s0) + (valid ? row : 0);
       else tok = static_cast<size_t>(it.b) * p.S + (valid ? row : 0);
       __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(p.o) + (tok * p.H + it.h) * D;
+      if constexpr (SPLIT) {
+        // a key range of a cut block (recomputed from n: nothing of it stays live in the loop)
+        const int u = item_of(n) - sp.n_whole;
+        if (u >= 0) {
+          split_store<D, NT>(sp, u % sp.n_tail, u / sp.n_tail, t, row_local, valid, o_addr, inv_l,
+                             m_run + __log2f(l_run), BAR_O_EMPTY(t));
+          continue;
+        }
+      }
 #pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {
         uint32_t o[32];
@@ -750,19 +904,27 @@ __global__ void __launch_bounds__(AttnCfg<D, FP8>::THREADS, 1)
 
 template <int D, bool FP8, bool CAUSAL, bool VARLEN>
 cudaError_t launch_attn(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                        const AttnParams& p, cudaStream_t stream) {
+                        const AttnParams& p, cudaStream_t stream, const SplitParams* split_plan) {
   using C = AttnCfg<D, FP8>;
   constexpr int SMEM = C::SMEM_BYTES + (VARLEN ? VARLEN_SMEM_BYTES : 0);
   static_assert(SMEM <= 227 * 1024, "shared memory budget");
+  constexpr bool CAN_SPLIT = !CAUSAL && !VARLEN;
+  const bool split = CAN_SPLIT && split_plan != nullptr && split_plan->n_parts > 1;
+  const SplitParams sp = split ? *split_plan : SplitParams{0, 0, 1, nullptr, nullptr};
   static std::atomic<unsigned long long> configured{0};   // one bit per device
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   const unsigned long long bit = 1ull << (dev & 63);
   if ((configured.load() & bit) == 0) {
-    e = cudaFuncSetAttribute(attn_fwd_kernel<D, FP8, CAUSAL, VARLEN>,
+    e = cudaFuncSetAttribute(attn_fwd_kernel<D, FP8, CAUSAL, VARLEN, false>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
     if (e != cudaSuccess) return e;
+    if constexpr (CAN_SPLIT) {
+      e = cudaFuncSetAttribute(attn_fwd_kernel<D, FP8, CAUSAL, VARLEN, true>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
+      if (e != cudaSuccess) return e;
+    }
     configured.fetch_or(bit);
   }
   static int sm_count[64] = {0};
@@ -774,10 +936,21 @@ cudaError_t launch_attn(const CUtensorMap& tq, const CUtensorMap& tk, const CUte
   }
   // VARLEN: an upper bound (every sequence adds at most one partial query block per head)
   const long long items = VARLEN ? (static_cast<long long>(p.S) / (128 * C::NT) + p.n_seq) * p.H
+                         : split ? static_cast<long long>(sp.n_whole) + 1ll * sp.n_tail * sp.n_parts
                                  : static_cast<long long>(p.nQB) * p.H * p.B;
   const long long grid = items < sm_count[dev & 63] ? items : sm_count[dev & 63];   // persistent
-  attn_fwd_kernel<D, FP8, CAUSAL, VARLEN>
-      <<<static_cast<unsigned>(grid), C::THREADS, SMEM, stream>>>(tq, tk, tv, p);
+  if constexpr (CAN_SPLIT) {
+    if (split) {
+      attn_fwd_kernel<D, FP8, CAUSAL, VARLEN, true>
+          <<<static_cast<unsigned>(grid), C::THREADS, SMEM, stream>>>(tq, tk, tv, p, sp);
+      if ((e = cudaGetLastError()) != cudaSuccess) return e;
+      const long long warps = static_cast<long long>(sp.n_tail) * 128 * C::NT;
+      split_merge_kernel<D, C::NT><<<static_cast<unsigned>((warps + 7) / 8), 256, 0, stream>>>(p, sp);
+      return cudaGetLastError();
+    }
+  }
+  attn_fwd_kernel<D, FP8, CAUSAL, VARLEN, false>
+      <<<static_cast<unsigned>(grid), C::THREADS, SMEM, stream>>>(tq, tk, tv, p, sp);
   return cudaGetLastError();
 }
 

@@ -33,15 +33,33 @@ struct AttnParams {
   int scale_stride;
 };
 
+// Key-split tail of a fixed-length, non-causal launch (n_parts <= 1: none).  Items
+// 0 .. n_whole-1 are whole query blocks; item n_whole + part * n_tail + slot is key range
+// `part` of query block n_whole + slot.  Scratch, device memory:
+struct SplitParams {
+  int n_whole, n_tail, n_parts;
+  float* part_o;        // [n_tail][n_parts][128 NT rows][D] fp32 partial O (normalised)
+  float* part_l;        // [n_tail][n_parts][128 NT rows] fp32 partial lse, log2 units
+};
+
+// At most this many key ranges per split tail block, each of at least KEY_SPLIT_MIN_TILES tiles.
+constexpr int KEY_SPLIT_MAX_PARTS = 4;
+constexpr int KEY_SPLIT_MIN_TILES = 4;
+// Cost model of the plan, in key tiles: an item's fixed cost, and the merge's.
+constexpr int KEY_SPLIT_ITEM_TILES = 4;
+constexpr int KEY_SPLIT_MERGE_TILES = 4;
+
+
 // Sequences and query-block levels a variable-length launch may hold: each CTA keeps the
 // offsets, the sequences sorted by length and per-level counts in shared memory.
 constexpr int VARLEN_MAX_SEQ = 4096;
 constexpr int VARLEN_MAX_LEVELS = 1024;
 
 // Launch one attention forward.  Returns the cudaError_t of the launch.
+// `split` (fixed length, not causal; may be null) plans a key-split tail.
 template <int D, bool FP8, bool CAUSAL, bool VARLEN = false>
 cudaError_t launch_attn(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                        const AttnParams& p, cudaStream_t stream);
+                        const AttnParams& p, cudaStream_t stream, const SplitParams* split);
 
 // Query-tile count per CTA (two Q tiles share K/V loads; one at D = 256 where
 // two tiles' S and O would not fit the 512 Tensor-Memory columns).

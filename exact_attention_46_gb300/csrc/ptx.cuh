@@ -163,6 +163,25 @@ __device__ __forceinline__ uint64_t l2_policy_evict_first() {
   return p;
 }
 
+// Global stores and loads (L2 only on the load side) with an L2 eviction-priority hint.
+__device__ __forceinline__ void st_v4_hint(float* p, float a, float b, float c, float d, uint64_t pol) {
+  asm volatile("st.global.L2::cache_hint.v4.f32 [%0], {%1, %2, %3, %4}, %5;"
+               :: "l"(p), "f"(a), "f"(b), "f"(c), "f"(d), "l"(pol) : "memory");
+}
+
+__device__ __forceinline__ float4 ld_cg_v4_hint(const float* p, uint64_t pol) {
+  float4 v;
+  asm volatile("ld.global.cg.L2::cache_hint.v4.f32 {%0, %1, %2, %3}, [%4], %5;"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "l"(p), "l"(pol) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ float2 ld_cg_v2_hint(const float* p, uint64_t pol) {
+  float2 v;
+  asm volatile("ld.global.cg.L2::cache_hint.v2.f32 {%0, %1}, [%2], %3;" : "=f"(v.x), "=f"(v.y) : "l"(p), "l"(pol) : "memory");
+  return v;
+}
+
 // ------------------------------------------------------------------- tcgen05 --
 
 // Allocate `ncols` Tensor-Memory columns (power of two, 32..512); the warp

@@ -16,7 +16,7 @@ __all__ = ["attn_fwd", "attn_fwd_fp8", "attn_fwd_varlen", "attn_fwd_varlen_fp8",
            "hadamard_rotate_quant_fp8",
            "hadamard_rotate_quant_fp8_varlen", "rope_cos_sin_table", "rope_hadamard_rotate_quant_fp8",
            "rope_hadamard_rotate_quant_fp8_varlen", "varlen_scale_blocks", "block_count", "check",
-           "set_spin_limit", "selftest_bounded_wait", "ATTN_BF16", "ATTN_FP8_E4M3"]
+           "set_spin_limit", "set_key_split", "key_split_plan", "selftest_bounded_wait", "ATTN_BF16", "ATTN_FP8_E4M3"]
 
 ATTN_BF16 = 0
 ATTN_FP8_E4M3 = 1
@@ -417,6 +417,20 @@ def check(stream=None):
 
 def set_spin_limit(cycles):
     _lib.load().attn_set_spin_limit(int(cycles))
+
+
+def set_key_split(max_parts):
+    """Most key ranges a block of the last, partly filled round of a non-causal forward is cut
+    into (1 = no split; default 4)."""
+    _lib.load().attn_set_key_split(int(max_parts))
+
+
+def key_split_plan(n_items, sms, key_tiles, max_parts=4):
+    """(blocks run whole, blocks cut, ranges per cut block) for a non-causal forward; host only."""
+    import ctypes
+    out = (ctypes.c_longlong * 3)()
+    _lib.call("attn_key_split_plan", int(n_items), int(sms), int(key_tiles), int(max_parts), ctypes.addressof(out))
+    return tuple(int(x) for x in out)
 
 
 def selftest_bounded_wait(cycles, stream=None):

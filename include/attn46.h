@@ -66,6 +66,15 @@ typedef enum {
  *   causal  : 0 = every query sees every key; 1 = query i sees keys j <= i.
  *   scale   : logit multiplier; 0 selects 1/sqrt(D); negative or non-finite
  *             values are rejected.
+ *   Scheduling: one persistent CTA per SM walks the query blocks.  Without
+ *   the causal mask, when the blocks do not fill the last round of CTAs, the
+ *   blocks of that round are cut into key ranges (attn_key_split_plan) whose
+ *   partial results are merged in a fixed order; their scratch comes, per
+ *   launch, from a memory pool the library keeps on each device (stream
+ *   ordered, returned after the launch; blocks stay cached in the pool).
+ *   Under stream capture, or when that memory cannot be had, the launch runs
+ *   unsplit.  Split and unsplit results differ only by rounding.  The same
+ *   holds for attn_fwd_fp8, attn_fwd_gqa and attn_fwd_gqa_fp8.
  */
 int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
              int B, int H, int S, int D, int causal, float scale, int dtype,
@@ -377,6 +386,33 @@ int attn_check(void* stream);
  * any host thread.
  */
 void attn_set_spin_limit(long long cycles);
+
+/*
+ * attn_set_key_split -- the most key ranges a query block of the last,
+ *   partly filled round of a non-causal forward may be cut into (see
+ *   attn_fwd); clamped to [1, 4], 1 turns the split off, 4 is the default.
+ *   Applies to later launches from any host thread.  The pages have no
+ *   counterpart: this is a scheduling choice of this library.
+ */
+void attn_set_key_split(int max_parts);
+
+/*
+ * attn_key_split_plan -- the split a non-causal forward of n_items equal
+ *   query blocks (B * H * ceil(S / (128 * tiles per CTA)); tiles per CTA = 2,
+ *   or 1 at D = 256) with key_tiles = ceil(S / 128) gets on `sms` persistent
+ *   CTAs with at most max_parts ranges per block.  Host only; no device call.
+ *   out[0] = blocks run whole (a multiple of sms), out[1] = blocks cut,
+ *   out[2] = ranges per cut block (1: no split).  Cost model, in key tiles
+ *   (a block costs about 4 tiles beyond its own, and so does the merge):
+ *   the last round costs key_tiles + 4 unsplit and, cut into s ranges,
+ *   ceil(n_tail * s / sms) * (ceil(key_tiles / s) + 4) + 4, with
+ *   n_tail = n_items mod sms.  The plan takes the cheapest s <= max_parts
+ *   whose ranges have at least 4 key tiles, if it costs at most 85 % of the
+ *   unsplit round; problems with no full round are not split.
+ *   ATTN_ERR_INVALID_ARG if out is NULL, n_items < 0, sms < 1 or
+ *   key_tiles < 0.
+ */
+int attn_key_split_plan(long long n_items, int sms, int key_tiles, int max_parts, long long* out);
 
 /*
  * attn_selftest_bounded_wait -- launch one tiny kernel whose bounded wait

@@ -40,7 +40,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_version(lib):
-    assert lib.attn_version() == 109
+    assert lib.attn_version() == 110
 
 
 FAKE = 1 << 20   # 16-byte aligned non-null fake device addresses: never dereferenced
@@ -269,3 +269,54 @@ def test_missing_library_raises_instead_of_falling_back(monkeypatch, tmp_path):
         ops.attn_fwd(x, x, x)
     with pytest.raises(ImportError):
         ops.varlen_scale_blocks(300, 3)
+
+
+def _plan(lib, n_items, sms, key_tiles, max_parts):
+    out = (ctypes.c_longlong * 3)()
+    assert lib.attn_key_split_plan(n_items, sms, key_tiles, max_parts, out) == 0
+    return tuple(out)
+
+
+def test_key_split_plan_cases(lib):
+    # B=2, S=8192, D=128 on 152 SMs (64 key tiles): 1024 blocks = 6 rounds + 112; four ranges
+    # cost 3 rounds of (16 + 4) + 4 = 64 tiles against 68 unsplit: not worth it
+    assert _plan(lib, 1024, 152, 64, 4) == (1024, 0, 1)
+    # H = 17: 24 blocks left, one round of quarter ranges, 24 tiles against 68
+    assert _plan(lib, 1088, 152, 64, 4) == (1064, 24, 4)
+    assert _plan(lib, 1088, 152, 64, 2) == (1064, 24, 2)      # capped at two ranges: 40 tiles
+    # H = 15: 48 left; thirds fit one round (30 tiles), quarters need two (44)
+    assert _plan(lib, 960, 152, 64, 4) == (912, 48, 3)
+    # B=1, S=32K (256 key tiles): 72 left, halves: 128 + 4 + 4 = 136 against 260
+    assert _plan(lib, 2048, 152, 256, 4) == (1976, 72, 2)
+    assert _plan(lib, 1216, 152, 64, 4) == (1216, 0, 1)       # whole rounds
+    assert _plan(lib, 100, 152, 64, 4) == (100, 0, 1)         # no full round
+    assert _plan(lib, 1088, 152, 64, 1) == (1088, 0, 1)       # split turned off
+    # 12 key tiles: halves cost 14 of 16 (over 85 %), thirds 12; quarters would have 3 tiles
+    assert _plan(lib, 176, 152, 12, 4) == (152, 24, 3)
+    out = (ctypes.c_longlong * 3)()
+    assert lib.attn_key_split_plan(10, 0, 4, 4, out) == 1
+    assert lib.attn_key_split_plan(10, 152, 4, 4, None) == 1
+
+
+def test_key_split_plan_is_the_cheapest_last_round(lib):
+    # every plan: whole rounds first, the rest cut into ranges of >= 4 tiles; the chosen count
+    # is the cheapest under the documented cost model and costs at most 85 % of no split
+    for sms in (7, 152):
+        for n_items in range(1, 3 * sms + 5, 3):
+            for key_tiles in (1, 7, 8, 12, 16, 64, 256):
+                for max_parts in (1, 2, 4, 9):
+                    w, t, s = _plan(lib, n_items, sms, key_tiles, max_parts)
+                    assert w + t == n_items
+                    if n_items <= sms or n_items % sms == 0:
+                        assert (t, s) == (0, 1)
+                        continue
+                    tail = n_items % sms
+                    whole = key_tiles + 4
+                    cost = {k: -(-tail * k // sms) * (-(-key_tiles // k) + 4) + 4
+                            for k in range(2, min(max_parts, 4) + 1) if key_tiles >= 4 * k}
+                    best = min(cost.values(), default=None)
+                    if s == 1:
+                        assert t == 0 and (best is None or 100 * best > 85 * whole)
+                    else:
+                        assert w % sms == 0 and t == tail and cost[s] == best <= 0.85 * whole
+                        assert all(cost[k] > best for k in cost if k < s)
