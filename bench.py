@@ -331,6 +331,46 @@ def long_context(dev, n=5):
     return out
 
 
+def key_split_leg(dev, n=5):
+    """Key-split tail of the non-causal forward: B=2, S=8192, D=128 with H=15 and H=17, whose
+    last round of 152 persistent CTAs is 32 % and 16 % full, BF16 and FP8 (Q and K rotated),
+    with the split on (the library's default plan) and off (attn_set_key_split(1))."""
+    from exact_attention_46_gb300 import ops
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    res = {"workload": "B=2 S=8192 D=128 non-causal, H=15 and H=17"}
+    for H_ in (15, 17):
+        g = torch.Generator(device=dev).manual_seed(H_)
+        q, k, v = (torch.randn((2, 8192, H_, D), generator=g, device=dev).to(torch.bfloat16) for _ in range(3))
+        o = torch.empty_like(q)
+        lse = torch.empty((2, H_, 8192), device=dev)
+        s = torch.where(torch.rand(D, generator=g, device=dev) < 0.5, -1.0, 1.0)
+        q8, sq = ops.hadamard_rotate_quant_fp8(q, s)
+        k8, sk = ops.hadamard_rotate_quant_fp8(k, s)
+        v8, sv = ops.hadamard_rotate_quant_fp8(v, None)
+        r = {"plan": list(ops.key_split_plan(2 * H_ * 8192 // 256, sms, 8192 // 128))}
+        try:
+            for mp, tag in ((4, "split"), (1, "unsplit")):
+                ops.set_key_split(mp)
+                for name, fn in (("bf16", lambda: ops.attn_fwd(q, k, v, out=o, lse=lse)),
+                                 ("fp8", lambda: ops.attn_fwd_fp8(q8, k8, v8, sq, sk, sv, out=o, lse=lse))):
+                    fn()
+                    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    torch.cuda.synchronize()
+                    e0.record()
+                    for _ in range(n):
+                        fn()
+                    e1.record()
+                    torch.cuda.synchronize()
+                    ms = e0.elapsed_time(e1) / n
+                    r[f"{name}_{tag}_tflops"] = round(attention_flops(2, H_, 8192, D, False) / ms / 1e9, 1)
+        finally:
+            ops.set_key_split(4)
+        ops.check()
+        res[f"H{H_}"] = r
+        del q, k, v, o, q8, k8, v8
+    return res
+
+
 class OracleSample:
     """A bounded sample of the workload for the fp64 oracle: one head at the headline S.
 
@@ -634,6 +674,7 @@ def run_ours(args):
     bw = backward_leg(dev) if (args.sweep and rank == 0) else None
     dc = decode_leg(dev) if (args.sweep and rank == 0) else None
     lc = long_context(dev) if (args.sweep and rank == 0) else None
+    ks = key_split_leg(dev) if (args.sweep and rank == 0) else None
     peaks, peak_src = load_peaks()
     cpu = cpu_baseline_sample() if (rank == 0 and world == 1 and args.cpu_baseline) else None
 
@@ -692,6 +733,7 @@ def run_ours(args):
             "backward": bw,
             "decode": dc,
             "long_context": lc,
+            "key_split": ks,
         }
         print(json.dumps(line), flush=True)
     if dist_on:
@@ -731,7 +773,7 @@ def run_reference(args):
 
 # auxiliary legs, by name (bench.py --profile-leg NAME runs one of them alone)
 LEGS = {"varlen": varlen_mix, "rope": rope_fusion, "backward": backward_leg, "decode": decode_leg,
-        "long": long_context}
+        "long": long_context, "key_split": key_split_leg}
 
 
 def main():
