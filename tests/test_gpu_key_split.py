@@ -136,3 +136,41 @@ def test_split_repeatable_and_without_lse():
     ops.check()
     assert l3 is None
     assert torch.equal(o1, o2) and torch.equal(l1, l2) and torch.equal(o1, o3)
+
+
+def test_split_fp8_grouped_query_is_repeated_multi_head():
+    # E4M3 codes and block scales of repeated K/V heads are repeated too, so the grouped launch
+    # and the multi-head launch on the repeated codes do the same arithmetic, split the same way
+    B, S, Hq, Hkv, D = 2, 2048, 12, 4, 128
+    assert plan(B, S, Hq, D)[2] == 3
+    q, k, v = inputs(B, S, Hq, D, case=84)
+    s = signs_for(84, D)
+    dev = torch.device("cuda")
+    sd = torch.from_numpy(s).to(dev)
+    q8, sq = ops.hadamard_rotate_quant_fp8(q.to(dev), sd)
+    k8, sk = ops.hadamard_rotate_quant_fp8(k[:, :, :Hkv].contiguous().to(dev), sd)
+    v8, sv = ops.hadamard_rotate_quant_fp8(v[:, :, :Hkv].contiguous().to(dev), None)
+    a, la = ops.attn_fwd_gqa_fp8(q8, k8, v8, sq, sk, sv)
+    rep = Hq // Hkv
+    rk8, rv8 = (t.repeat_interleave(rep, dim=2).contiguous() for t in (k8, v8))
+    rsk, rsv = (t.repeat_interleave(rep, dim=1).contiguous() for t in (sk, sv))
+    b, lb = ops.attn_fwd_fp8(q8, rk8, rv8, sq, rsk, rsv)
+    ops.check()
+    assert torch.equal(a, b) and torch.equal(la, lb)
+
+
+def test_split_unit_scale_fp8_is_attn_fwd_fp8_with_unit_scales():
+    # attn_fwd on E4M3 codes (scales taken as 1) against attn_fwd_fp8 with all-one scale arrays
+    B, S, H, D = 2, 2048, 11, 128
+    assert plan(B, S, H, D)[2] == 4
+    dev = torch.device("cuda")
+    g = torch.Generator().manual_seed(85)
+    codes = [(torch.randint(0, 0x41, (B, S, H, D), generator=g, dtype=torch.int32)
+              | (torch.randint(0, 2, (B, S, H, D), generator=g, dtype=torch.int32) << 7)).to(torch.uint8).to(dev)
+             for _ in range(3)]
+    ones = torch.ones((B, H, -(-S // 128)), dtype=torch.float32, device=dev)
+    a, la = ops.attn_fwd(*codes)
+    b, lb = ops.attn_fwd_fp8(*codes, ones, ones, ones)
+    ops.check()
+    assert torch.isfinite(a.float()).all()
+    assert torch.equal(a, b) and torch.equal(la, lb)
