@@ -42,6 +42,12 @@
 
 namespace ea46 {
 
+// Programmatic dependent launch: let the next grid on the stream (launched with programmatic
+// stream serialization) start once every CTA of this grid has issued this; and wait until
+// the grid this one depends on has completed and its memory operations are visible.
+__device__ __forceinline__ void grid_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 namespace {
 
 constexpr float LOG2E = 1.4426950408889634f;
@@ -168,6 +174,9 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
   auto q_tile = [&](int i) { return j0 + i % nqt; };
   auto q_head = [&](int i) { return hkv * G + i / nqt; };
 
+  // The dQ kernel reads nothing this kernel writes: it may start on SMs this grid leaves
+  // idle once every CTA of this grid is running (programmatic dependent launch).
+  if (threadIdx.x == 0) grid_launch_dependents();
   if (threadIdx.x == 0) {
     mbar_init(BAR_KV, 1);
     mbar_init(BAR_S, 1);
@@ -543,6 +552,10 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
+  // This grid may have started before the dK/dV grid finished (programmatic dependent launch);
+  // it ends only after that grid has completed and its writes are visible, so the stream's
+  // next operation sees every gradient.
+  grid_dependency_wait();
 }
 
 template <int D, bool CAUSAL>
@@ -570,8 +583,21 @@ cudaError_t launch_bwd_d(const CUtensorMap* maps, const BwdParams& p, cudaStream
   bwd_dkdv_kernel<D, CAUSAL><<<static_cast<unsigned>(p.B * p.Hkv) * nqt, C::THREADS, C::SMEM_BYTES, st>>>(
       maps[0], maps[1], maps[2], maps[3], p);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  bwd_dq_kernel<D, CAUSAL><<<static_cast<unsigned>(p.B * p.H) * nqt, C::THREADS, C::SMEM_BYTES, st>>>(
-      maps[0], maps[1], maps[2], maps[3], p);
+  // dQ after dK/dV with programmatic stream serialization: its CTAs take the SMs the last,
+  // partly filled wave of dK/dV CTAs leaves idle (the two kernels never share an SM: each
+  // needs most of its shared memory)
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(static_cast<unsigned>(p.B * p.H) * nqt);
+  cfg.blockDim = dim3(C::THREADS);
+  cfg.dynamicSmemBytes = C::SMEM_BYTES;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, bwd_dq_kernel<D, CAUSAL>, maps[0], maps[1], maps[2], maps[3], p);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
