@@ -164,7 +164,11 @@ class HotPath:
         self.q8, self.k8, self.v8 = (torch.empty(q.shape, dtype=torch.uint8, device=dev) for _ in range(3))
         self.sq, self.sk, self.sv = (torch.empty((B, H, nb), dtype=torch.float32, device=dev) for _ in range(3))
         self.up, self.down = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
-        self.launches_per_step = 5
+        # two attention launches and three quantiser launches; a key-split forward adds its
+        # merge kernel to each attention launch (not at the headline shape: the plan keeps it whole)
+        sms = torch.cuda.get_device_properties(dev).multi_processor_count
+        split = ops.key_split_plan(B * H * ((S + 255) // 256), sms, (S + 127) // 128)[2] > 1
+        self.launches_per_step = 5 + (2 if split else 0)
 
     def step(self, ev=None, bset=0):
         """One pass of the hot path on input/output set `bset`, on the current stream."""
