@@ -18,7 +18,7 @@ Readings:
   (a sequence of length L starting at a covers ceil(L / 128) <= (a + L) // 128 - a // 128 + 1
   indices) and stay below NB; unused indices carry no meaning;
 * the attention of every sequence is the FP8 path of ``fp8_path`` on its own de-quantised
-  values, with V's block ratios taken over the sequence's own blocks;
+  values;
 * with rotary embedding in front (``rope_base``), positions restart at every sequence's first
   token: each sequence is embedded as ``rope.rope`` embeds a tensor of its own.
 """
@@ -75,23 +75,17 @@ def quantise_varlen(x, cu_seqlens, signs=None, rope_base=None):
     return {"q": q, "pre": pre, "codes": codes, "scale": scale, "deq": deq}
 
 
-def fp8_attention_varlen(qd, kd, vd, v_scale, cu_seqlens, scale, causal=False, round_p=True, fold_v=True):
-    """Attention of every packed sequence on de-quantised qd, kd, vd [total, H, D], numerators
-    rounded to E4M3 (with V's block ratios over the sequence's blocks when fold_v).
-    Returns (O [total, H, D], lse [H, total])."""
+def fp8_attention_varlen(qd, kd, vd, cu_seqlens, scale, causal=False, round_p=True):
+    """Attention of every packed sequence on de-quantised qd, kd, vd [total, H, D], with the
+    softmax numerators rounded to E4M3 (``round_p``).  Returns (O [total, H, D], lse [H, total])."""
     total, H, D = qd.shape
     O = np.zeros((total, H, D))
     lse = np.zeros((H, total))
-    base = block_base(cu_seqlens)
     for s, (s0, n) in enumerate(segments(cu_seqlens)):
         if n == 0:
             continue
-        ratio = None
-        if fold_v:
-            nblk = (n + 127) // 128
-            ratio = fp8_path.v_block_ratio(v_scale[None, :, base[s]:base[s] + nblk], n)
         o, l = fp8_path.attention_rounded_p(qd[None, s0:s0 + n], kd[None, s0:s0 + n], vd[None, s0:s0 + n], scale,
-                                            causal, None, round_p, ratio)
+                                            causal, None, round_p)
         O[s0:s0 + n] = o[0]
         lse[:, s0:s0 + n] = l[0]
     return O, lse

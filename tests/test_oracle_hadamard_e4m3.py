@@ -8,6 +8,7 @@ step 4), and it spreads an outlier over all coordinates (step 2).
 """
 
 import math
+from fractions import Fraction
 
 import numpy as np
 import pytest
@@ -182,21 +183,101 @@ def test_rotated_quantiser_rotates_before_scaling():
     np.testing.assert_allclose(out["scale"][0, 0, 0], np.abs(hadamard.rotate(x, s)).max() / 448.0, rtol=1e-14)
 
 
-def test_fp32_rounding_decision_differs_from_fp64_only_at_exact_ties():
-    # amax = 26 = 2 * 13 makes x * 448 / 26 = x * 224 / 13 an exact E4M3 midpoint for bf16
-    # values x = 39 * 2^k; elsewhere the fp32 decision equals rounding the exact quotient.
+def _brute_force(x, signs, granularity="block"):
+    """Every element decided in exact rational arithmetic from x: exact transform, exact
+    block (or tensor) maximum, exact quotient 448 y / amax, nearest E4M3 with ties to even."""
+    B, S, H, D = x.shape
+    Hm = hadamard.sylvester(D)
+    y = np.empty(x.shape, dtype=object)
+    for idx in np.ndindex(B, S, H):
+        row = [Fraction(float(a)) for a in x[idx]]
+        if signs is None:
+            y[idx] = row
+        else:
+            xs = [row[d] * int(signs[d]) for d in range(D)]
+            y[idx] = [sum(xs[d] * int(Hm[d, c]) for d in range(D)) for c in range(D)]
+    q = np.empty(x.shape)
+    A_all = max(abs(v) for v in y.reshape(-1)) if granularity == "tensor" else None
+    for b, s, h in np.ndindex(B, S, H):
+        if granularity == "tensor":
+            A = A_all
+        else:
+            t0 = s // 128 * 128
+            A = max(abs(v) for v in y[b, t0:min(S, t0 + 128), h].reshape(-1))
+        for c in range(D):
+            q[b, s, h, c] = quantise.rne_e4m3_fraction(448 * y[b, s, h, c] / A) if A > 0 else 0.0
+    return q
+
+
+def test_exact_rne_of_fractions_matches_torch_cast():
+    fin = e4m3.decode(np.arange(0, 0x7F, dtype=np.uint8))
+    mids = (fin[1:] + fin[:-1]) / 2
+    rnd = RNG.uniform(0, 448, 3000) * np.exp2(-RNG.integers(0, 14, 3000))
+    x = np.concatenate([fin, mids, rnd, mids * (1 + 2.0 ** -20), mids * (1 - 2.0 ** -20)])
+    x = np.concatenate([x, -x]).astype(np.float32).astype(np.float64)
+    ref = torch.from_numpy(x.astype(np.float32)).to(torch.float8_e4m3fn).to(torch.float64).numpy()
+    got = np.array([quantise.rne_e4m3_fraction(Fraction(float(v))) for v in x])
+    np.testing.assert_array_equal(got, ref)
+    # beyond the range torch's cast gives NaN; the quantiser saturates ("satfinite")
+    assert quantise.rne_e4m3_fraction(Fraction(500)) == 448.0
+    assert quantise.rne_e4m3_fraction(Fraction(-10 ** 6)) == -448.0
+
+
+def test_exact_midpoints_go_to_the_even_neighbour():
+    # amax = 26 and x = 39 * 2^-5: the quotient 448 * 1.21875 / 26 = 21 lies exactly half-way
+    # between the E4M3 values 20 (mantissa 2, even) and 22 (mantissa 3): even wins.  A rounding
+    # decision taken in fp32 (x * fl32(448 / 26)) lands slightly above 21 and would pick 22.
     B, S, H, D = 1, 128, 1, 128
-    x = RNG.standard_normal((B, S, H, D))
-    x = torch.from_numpy(x).to(torch.bfloat16).double().numpy()
+    x = torch.from_numpy(RNG.standard_normal((B, S, H, D))).to(torch.bfloat16).double().numpy()
     x[0, 0, 0, 0] = 26.0
-    x[0, 1:40, 0, 1] = 39 * 2.0 ** -5                      # exact ties in real arithmetic
+    x[0, 1:40, 0, 1] = 39 * 2.0 ** -5
     out = quantise.quantise_blocks(x)
-    exact = x * 448.0 / 26.0
-    q64 = e4m3.round_e4m3(exact)
-    lo = e4m3.round_e4m3(exact * (1 - 1e-9))
-    hi = e4m3.round_e4m3(exact * (1 + 1e-9))
-    tie = lo != hi                                          # a midpoint sits within 1e-9
-    assert tie[0, 1:40, 0, 1].all()
-    diff = out["q"] != q64
-    assert not (diff & ~tie).any()
-    assert ((out["q"] == lo) | (out["q"] == hi)).all()
+    assert (out["q"][0, 1:40, 0, 1] == 20.0).all()
+    assert (out["pre"][0, 1:40, 0, 1] == 21.0).all()
+    f32 = np.float32(39 * 2.0 ** -5) * (np.float32(448.0) / np.float32(26.0))
+    assert e4m3.round_e4m3(np.array([float(f32)]))[0] == 22.0
+    # and every element equals the decision taken in exact arithmetic
+    np.testing.assert_array_equal(out["q"], _brute_force(x, None))
+
+
+@pytest.mark.parametrize("rotate", [False, True])
+def test_quantiser_equals_exact_arithmetic_brute_force(rotate):
+    # bf16 inputs with outliers and planted ties, blocks of 128 and a ragged 44-token block
+    B, S, H, D = 1, 172, 2, 16
+    x = RNG.standard_normal((B, S, H, D))
+    x[RNG.random(x.shape) < 0.01] *= 10
+    x = torch.from_numpy(x).to(torch.bfloat16).double().numpy()
+    x[0, 3, 1, :] = 0.0
+    x[0, 5, 0, 0] = 26.0
+    x[0, 6:20, 0, 2] = 39 * 2.0 ** -5
+    s = RNG.choice([-1.0, 1.0], size=D) if rotate else None
+    out = quantise.quantise_blocks(x, s)
+    np.testing.assert_array_equal(out["q"], _brute_force(x, s))
+    np.testing.assert_array_equal(e4m3.decode(out["codes"]), out["q"])
+
+
+def test_rows_fp64_cannot_hold_are_transformed_exactly():
+    # 100 and 2^-60 in one row: the +-sums need about 67 significant bits, beyond fp64
+    B, S, H, D = 1, 130, 1, 16
+    x = RNG.standard_normal((B, S, H, D))
+    x[0, 7, 0, 0] = 100.0
+    x[0, 7, 0, 1:] = 2.0 ** -60
+    x[0, 129, 0, 3] = 2.0 ** -70
+    s = RNG.choice([-1.0, 1.0], size=D)
+    out = quantise.quantise_blocks(x, s)
+    np.testing.assert_array_equal(out["q"], _brute_force(x, s))
+
+
+def test_tensor_granularity_uses_one_scale():
+    B, S, H, D = 2, 300, 2, 16
+    x = RNG.standard_normal((B, S, H, D))
+    x[1, 250, 1, 3] = 37.0
+    out = quantise.quantise_blocks(x, granularity="tensor")
+    np.testing.assert_array_equal(out["scale"], np.full((B, H, 3), 37.0 / 448.0))
+    np.testing.assert_array_equal(out["q"], _brute_force(x, None, "tensor"))
+    s = RNG.choice([-1.0, 1.0], size=D)
+    rot = quantise.quantise_blocks(x, s, granularity="tensor")
+    np.testing.assert_allclose(rot["scale"], np.abs(hadamard.rotate(x, s)).max() / 448.0, rtol=1e-14)
+    np.testing.assert_array_equal(rot["q"], _brute_force(x, s, "tensor"))
+    with pytest.raises(ValueError):
+        quantise.quantise_blocks(x, granularity="row")

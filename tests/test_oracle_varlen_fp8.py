@@ -46,9 +46,8 @@ def test_exact_values_reduce_to_the_varlen_definition():
     cu = np.array([0, 5, 5, 200, 331])
     q, k, v = (RNG.standard_normal((331, 2, 16)) for _ in range(3))
     deq = [VF.quantise_varlen(t, cu)["deq"] for t in (q, k, v)]
-    vs = VF.quantise_varlen(v, cu)["scale"]
     for causal in (False, True):
-        O, lse = VF.fp8_attention_varlen(*deq, vs, cu, 0.25, causal, round_p=False)
+        O, lse = VF.fp8_attention_varlen(*deq, cu, 0.25, causal, round_p=False)
         O0, lse0 = attention_varlen(*deq, cu, 0.25, causal)
         np.testing.assert_allclose(O, O0, rtol=1e-12, atol=1e-13)
         np.testing.assert_allclose(lse, lse0, rtol=1e-12, atol=1e-13)
@@ -60,8 +59,8 @@ def test_one_sequence_is_the_fixed_length_fp8_path():
     q, k, v = (RNG.standard_normal((S, H, D)) for _ in range(3))
     rv = VF.quantise_varlen(v, cu)
     deq = [VF.quantise_varlen(t, cu)["deq"] for t in (q, k)] + [rv["deq"]]
-    O, lse = VF.fp8_attention_varlen(*deq, rv["scale"], cu, 0.2, True)
-    O1, lse1, _ = fp8_path.fp8_attention(q[None], k[None], v[None], None, 0.2, True, fold_v=True)
+    O, lse = VF.fp8_attention_varlen(*deq, cu, 0.2, True)
+    O1, lse1, _ = fp8_path.fp8_attention(q[None], k[None], v[None], None, 0.2, True)
     np.testing.assert_allclose(O, O1[0], rtol=1e-13, atol=1e-14)
     np.testing.assert_allclose(lse, lse1[0], rtol=1e-13)
 
