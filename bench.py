@@ -164,11 +164,8 @@ class HotPath:
         self.q8, self.k8, self.v8 = (torch.empty(q.shape, dtype=torch.uint8, device=dev) for _ in range(3))
         self.sq, self.sk, self.sv = (torch.empty((B, H, nb), dtype=torch.float32, device=dev) for _ in range(3))
         self.up, self.down = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
-        # two attention launches and three quantiser launches; a key-split forward adds its
-        # merge kernel to each attention launch (not at the headline shape: the plan keeps it whole)
-        sms = torch.cuda.get_device_properties(dev).multi_processor_count
-        split = ops.key_split_plan(B * H * ((S + 255) // 256), sms, (S + 127) // 128)[2] > 1
-        self.launches_per_step = 5 + (2 if split else 0)
+        # two attention launches (attn_fwd never splits) and three quantiser launches
+        self.launches_per_step = 5
 
     def step(self, ev=None, bset=0):
         """One pass of the hot path on input/output set `bset`, on the current stream."""
@@ -313,11 +310,14 @@ def long_context(dev, n=5):
         q8, sq = ops.hadamard_rotate_quant_fp8(q, s)
         k8, sk = ops.hadamard_rotate_quant_fp8(k, s)
         v8, sv = ops.hadamard_rotate_quant_fp8(v, None)
-        res = {"S": S, "B": 1}
+        # attn_fwd_split with a caller workspace: the non-causal launches may cut their last round
+        ws = torch.empty((max(1, ops.split_workspace_bytes(1, H, S, D)),), dtype=torch.uint8, device=dev)
+        res = {"S": S, "B": 1, "key_split_plan": list(ops.key_split_plan(
+            H * S // 256, torch.cuda.get_device_properties(dev).multi_processor_count, S // 128))}
         for causal in (False, True):
-            for name, fn in (("bf16", lambda: ops.attn_fwd(q, k, v, causal=causal, out=o, lse=lse)),
-                             ("fp8", lambda: ops.attn_fwd_fp8(q8, k8, v8, sq, sk, sv, causal=causal, out=o,
-                                                             lse=lse))):
+            for name, fn in (("bf16", lambda: ops.attn_fwd_split(q, k, v, causal=causal, out=o, lse=lse, workspace=ws)),
+                             ("fp8", lambda: ops.attn_fwd_split(q8, k8, v8, sq, sk, sv, causal=causal, out=o,
+                                                               lse=lse, workspace=ws))):
                 fn()
                 e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 torch.cuda.synchronize()
@@ -338,7 +338,8 @@ def long_context(dev, n=5):
 def key_split_leg(dev, n=5):
     """Key-split tail of the non-causal forward: B=2, S=8192, D=128 with H=15 and H=17, whose
     last round of 152 persistent CTAs is 32 % and 16 % full, BF16 and FP8 (Q and K rotated),
-    with the split on (the library's default plan) and off (attn_set_key_split(1))."""
+    with the split on (attn_fwd_split with a caller workspace, allocated before timing) and off
+    (attn_fwd, which never splits)."""
     from exact_attention_46_gb300 import ops
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     res = {"workload": "B=2 S=8192 D=128 non-causal, H=15 and H=17"}
@@ -352,27 +353,118 @@ def key_split_leg(dev, n=5):
         k8, sk = ops.hadamard_rotate_quant_fp8(k, s)
         v8, sv = ops.hadamard_rotate_quant_fp8(v, None)
         r = {"plan": list(ops.key_split_plan(2 * H_ * 8192 // 256, sms, 8192 // 128))}
-        try:
-            for mp, tag in ((4, "split"), (1, "unsplit")):
-                ops.set_key_split(mp)
-                for name, fn in (("bf16", lambda: ops.attn_fwd(q, k, v, out=o, lse=lse)),
-                                 ("fp8", lambda: ops.attn_fwd_fp8(q8, k8, v8, sq, sk, sv, out=o, lse=lse))):
+        ws = torch.empty((max(1, ops.split_workspace_bytes(2, H_, 8192, D)),), dtype=torch.uint8, device=dev)
+        r["workspace_bytes"] = ops.split_workspace_bytes(2, H_, 8192, D)
+        legs = (("split", lambda: ops.attn_fwd_split(q, k, v, out=o, lse=lse, workspace=ws),
+                 lambda: ops.attn_fwd_split(q8, k8, v8, sq, sk, sv, out=o, lse=lse, workspace=ws)),
+                ("unsplit", lambda: ops.attn_fwd(q, k, v, out=o, lse=lse),
+                 lambda: ops.attn_fwd_fp8(q8, k8, v8, sq, sk, sv, out=o, lse=lse)))
+        for tag, f16, f8 in legs:
+            for name, fn in (("bf16", f16), ("fp8", f8)):
+                fn()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                torch.cuda.synchronize()
+                e0.record()
+                for _ in range(n):
                     fn()
-                    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                    torch.cuda.synchronize()
-                    e0.record()
-                    for _ in range(n):
-                        fn()
-                    e1.record()
-                    torch.cuda.synchronize()
-                    ms = e0.elapsed_time(e1) / n
-                    r[f"{name}_{tag}_tflops"] = round(attention_flops(2, H_, 8192, D, False) / ms / 1e9, 1)
-        finally:
-            ops.set_key_split(4)
+                e1.record()
+                torch.cuda.synchronize()
+                ms = e0.elapsed_time(e1) / n
+                r[f"{name}_{tag}_tflops"] = round(attention_flops(2, H_, 8192, D, False) / ms / 1e9, 1)
         ops.check()
         res[f"H{H_}"] = r
         del q, k, v, o, q8, k8, v8
     return res
+
+
+def causal_sweep(dev, n=10):
+    """The causal head-dimension sweep: D in {64, 128, 256}, H = 2048 / D, S in {1K .. 16K},
+    B = 16384 / S, N(0,1) bf16 inputs; TFLOPS counts half of 4*B*H*S^2*D (device time, n launches
+    after 3 untimed ones), and the fraction of the measured bf16 peak."""
+    from exact_attention_46_gb300 import ops
+    peaks, _ = load_peaks()
+    out = []
+    for Dd in (64, 128, 256):
+        Hh = 2048 // Dd
+        for S in (1024, 2048, 4096, 8192, 16384):
+            B = TOKENS // S
+            g = torch.Generator(device=dev).manual_seed(S + Dd)
+            q, k, v = (torch.randn((B, S, Hh, Dd), generator=g, device=dev, dtype=torch.float32).to(torch.bfloat16)
+                       for _ in range(3))
+            o = torch.empty_like(q)
+            lse = torch.empty((B, Hh, S), device=dev)
+            fn = lambda: ops.attn_fwd(q, k, v, causal=True, out=o, lse=lse)
+            for _ in range(3):
+                fn()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
+            e0.record()
+            for _ in range(n):
+                fn()
+            e1.record()
+            torch.cuda.synchronize()
+            ms = e0.elapsed_time(e1) / n
+            tf = attention_flops(B, Hh, S, Dd, causal=True) / ms / 1e9
+            out.append({"D": Dd, "H": Hh, "S": S, "B": B, "tflops": round(tf, 1),
+                        "frac_of_bf16_peak": round(tf / peaks["bf16_tflops"], 4)})
+            del q, k, v, o
+    ops.check()
+    return out
+
+
+def fp8_accuracy(dev, n=1, rows_per_head=128):
+    """Incoherent processing on the FP8 workload: D=128, H=16, B=16384/S, S in {1K .. 16K},
+    Q/K/V = N(0,1) with 0.1 % of the entries replaced by N(0, 10) draws (seeded torch generator
+    on the device).  RMS of O over sampled query rows against exact attention on the bf16 inputs
+    (torch, fp64 on the device), for
+      product   -- per-block scales, Q and K rotated (the library's FP8 path);
+      per_block -- the same kernel and quantiser without the rotation;
+      standard  -- one scale per tensor (amax / 448, E4M3 by torch's cast), no rotation, run on
+                   the same attention kernel with every block scale set to that one value.
+    ratio_vs_per_block and ratio_vs_standard = RMS(product) / RMS(baseline); the target of the
+    two readings is <= 0.5."""
+    from exact_attention_46_gb300 import ops
+    out = []
+    for S in (1024, 2048, 4096, 8192, 16384):
+        B = TOKENS // S
+        g = torch.Generator(device=dev).manual_seed(4000 + S)
+
+        def draw():
+            x = torch.randn((B, S, H, D), generator=g, device=dev)
+            mask = torch.rand((B, S, H, D), generator=g, device=dev) < 1e-3
+            x = torch.where(mask, 10.0 * torch.randn((B, S, H, D), generator=g, device=dev), x)
+            return x.to(torch.bfloat16)
+
+        q, k, v = draw(), draw(), draw()
+        s = torch.where(torch.rand(D, generator=g, device=dev) < 0.5, -1.0, 1.0)
+        rows = torch.unique(torch.cat([torch.tensor([0, S - 1], device=dev),
+                                       torch.randint(0, S, (rows_per_head,), generator=g, device=dev)]))
+        qr = q[:, rows].double()
+        sc = torch.einsum("brhd,bshd->bhrs", qr, k.double()) / math.sqrt(D)
+        ref = torch.einsum("bhrs,bshd->brhd", torch.softmax(sc, dim=-1), v.double())
+        del sc, qr
+        rms = {}
+        for name, sg in (("product", s), ("per_block", None)):
+            q8, sq = ops.hadamard_rotate_quant_fp8(q, sg)
+            k8, sk = ops.hadamard_rotate_quant_fp8(k, sg)
+            v8, sv = ops.hadamard_rotate_quant_fp8(v, None)
+            o, _ = ops.attn_fwd_fp8(q8, k8, v8, sq, sk, sv, want_lse=False)
+            rms[name] = float(((o[:, rows].double() - ref) ** 2).mean().sqrt())
+        codes, scales = [], []
+        for x in (q, k, v):
+            amax = x.float().abs().max()
+            scale = amax / 448.0
+            codes.append((x.float() / scale).clamp(-448, 448).to(torch.float8_e4m3fn).view(torch.uint8))
+            scales.append(torch.full((B, H, (S + 127) // 128), float(scale), device=dev))
+        o, _ = ops.attn_fwd_fp8(*codes, *scales, want_lse=False)
+        rms["standard"] = float(((o[:, rows].double() - ref) ** 2).mean().sqrt())
+        ops.check()
+        out.append({"S": S, "B": B, "rms": {k_: round(v_, 6) for k_, v_ in rms.items()},
+                    "ratio_vs_per_block": round(rms["product"] / rms["per_block"], 4),
+                    "ratio_vs_standard": round(rms["product"] / rms["standard"], 4)})
+        del q, k, v, codes
+    return {"workload": "D=128 H=16 B=16384/S, N(0,1) + 0.1 % N(0,10) outliers; sampled query rows vs "
+                        "exact fp64 attention on the bf16 inputs", "target": "ratio <= 0.5", "by_S": out}
 
 
 class OracleSample:
@@ -425,6 +517,7 @@ class OracleSample:
 
 
 def blas_threads():
+    """Threads the oracle's numpy BLAS uses (the host's core count where that is unknown)."""
     cores = os.cpu_count()
     try:
         from threadpoolctl import threadpool_info
@@ -432,6 +525,15 @@ def blas_threads():
         return n or cores
     except ImportError:
         return cores
+
+
+def host_cores():
+    """Cores of the host (os.cpu_count(), and nproc, which honours the process's affinity)."""
+    try:
+        nproc = int(subprocess.run(["nproc"], capture_output=True, text=True, timeout=5).stdout.strip())
+    except (OSError, ValueError, subprocess.SubprocessError):
+        nproc = None
+    return {"cpu_count": os.cpu_count(), "nproc": nproc}
 
 
 def cpu_baseline_sample(budget_s=12.0):
@@ -444,7 +546,7 @@ def cpu_baseline_sample(budget_s=12.0):
         n += 1
     dt = time.perf_counter() - t0
     return {"value": n * smp.flops_per_step / dt / 1e12, "unit": "TFLOPS", "cores": blas_threads(),
-            "kind": "oracle", "sample": smp.describe(n, dt)}
+            "host_cores": host_cores(), "kind": "oracle", "sample": smp.describe(n, dt)}
 
 
 def decode_leg(dev, n=20):
@@ -679,6 +781,8 @@ def run_ours(args):
     dc = decode_leg(dev) if (args.sweep and rank == 0) else None
     lc = long_context(dev) if (args.sweep and rank == 0) else None
     ks = key_split_leg(dev) if (args.sweep and rank == 0) else None
+    cs = causal_sweep(dev) if (args.sweep and rank == 0) else None
+    fa = fp8_accuracy(dev) if (args.sweep and rank == 0) else None
     peaks, peak_src = load_peaks()
     cpu = cpu_baseline_sample() if (rank == 0 and world == 1 and args.cpu_baseline) else None
 
@@ -738,6 +842,8 @@ def run_ours(args):
             "decode": dc,
             "long_context": lc,
             "key_split": ks,
+            "causal_sweep": cs,
+            "fp8_accuracy": fa,
         }
         print(json.dumps(line), flush=True)
     if dist_on:
@@ -760,8 +866,8 @@ def run_reference(args):
     total = time.perf_counter() - t0
     dt = total / args.steps
     val = smp.flops_per_step / dt / 1e12
-    cpu = {"value": round(val, 6), "unit": "TFLOPS", "cores": blas_threads(), "kind": "oracle",
-           "sample": smp.describe(args.steps, total)}
+    cpu = {"value": round(val, 6), "unit": "TFLOPS", "cores": blas_threads(), "host_cores": host_cores(),
+           "kind": "oracle", "sample": smp.describe(args.steps, total)}
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": round(val, 6), "unit": "TFLOPS",
         "n_gpus": int(os.environ.get("WORLD_SIZE", "1")), "steps": args.steps, "warmup": args.warmup,
@@ -777,7 +883,7 @@ def run_reference(args):
 
 # auxiliary legs, by name (bench.py --profile-leg NAME runs one of them alone)
 LEGS = {"varlen": varlen_mix, "rope": rope_fusion, "backward": backward_leg, "decode": decode_leg,
-        "long": long_context, "key_split": key_split_leg}
+        "long": long_context, "key_split": key_split_leg, "causal": causal_sweep, "fp8_accuracy": fp8_accuracy}
 
 
 def main():

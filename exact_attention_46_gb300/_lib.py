@@ -42,6 +42,8 @@ SIGNATURES = {
     "attn_set_spin_limit": (None, [_LL]),
     "attn_set_key_split": (None, [_I]),
     "attn_key_split_plan": (_I, [_LL, _I, _I, _I, _P]),
+    "attn_fwd_split": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _P, _SZ, _P]),
+    "attn_fwd_split_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I]),
     "attn_selftest_bounded_wait": (_I, [_LL, _P]),
     "attn_version": (_I, []),
 }

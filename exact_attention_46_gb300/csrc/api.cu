@@ -43,27 +43,18 @@ long long spin_limit() {
 }
 
 // Device error word: [0] = first error code of the launches since the last attn_check,
-// [1] = where it happened.  One copy per device (module-scope device variable).
+// [1] = where it happened.  One copy per device (module-scope device variable).  Its address
+// is looked up on every call, with the caller's device current: the lookup is a host query,
+// not stream work, and an address kept from an earlier context (before a device reset) would
+// be stale.
 __device__ int g_err_word[2];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_mu;
-int* g_err_ptr[kMaxDevices] = {};
-
 int err_words(int** out) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
-  if (dev < 0 || dev >= kMaxDevices) return fail(ATTN_ERR_UNSUPPORTED, "device index %d", dev);
-  std::lock_guard<std::mutex> lk(g_mu);
-  if (g_err_ptr[dev] == nullptr) {
-    void* ptr = nullptr;
-    e = cudaGetSymbolAddress(&ptr, g_err_word);
-    if (e != cudaSuccess)
-      return fail(ATTN_ERR_CUDA, "cudaGetSymbolAddress(error word): %s", cudaGetErrorString(e));
-    g_err_ptr[dev] = static_cast<int*>(ptr);
-  }
-  *out = g_err_ptr[dev];
+  void* ptr = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&ptr, g_err_word);
+  if (e != cudaSuccess)
+    return fail(ATTN_ERR_CUDA, "cudaGetSymbolAddress(error word): %s", cudaGetErrorString(e));
+  *out = static_cast<int*>(ptr);
   return ATTN_OK;
 }
 
@@ -167,78 +158,56 @@ SplitPlan key_split_plan(long long n_items, int sms, int nK, int max_parts) {
   return sp;
 }
 
-// Per-device pool of split scratch; freed blocks stay in the pool for the next launch.
-cudaMemPool_t g_split_pool[kMaxDevices] = {};
-
-cudaError_t split_pool(int dev, cudaMemPool_t* out) {
-  std::lock_guard<std::mutex> lk(g_mu);
-  if (g_split_pool[dev] == nullptr) {
-    cudaMemPoolProps props{};
-    props.allocType = cudaMemAllocationTypePinned;
-    props.location.type = cudaMemLocationTypeDevice;
-    props.location.id = dev;
-    cudaMemPool_t pool = nullptr;
-    cudaError_t e = cudaMemPoolCreate(&pool, &props);
-    if (e != cudaSuccess) return e;
-    uint64_t keep = ~0ull;
-    e = cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &keep);
-    if (e != cudaSuccess) {
-      cudaMemPoolDestroy(pool);
-      return e;
-    }
-    g_split_pool[dev] = pool;
-  }
-  *out = g_split_pool[dev];
-  return cudaSuccess;
-}
-
-// The split plan of one launch and its scratch, handed back to the pool on the launch's stream
-// when the launching call returns (after the launch is queued).
-struct SplitScratch {
-  SplitParams sp{0, 0, 1, nullptr, nullptr};
-  void* ptr = nullptr;
-  cudaStream_t st = nullptr;
-  const SplitParams* plan() const { return sp.n_parts > 1 ? &sp : nullptr; }
-  ~SplitScratch() {
-    if (ptr != nullptr) cudaFreeAsync(ptr, st);
-  }
+// The split of a launch (fixed length, not causal) on the current device, and the workspace it
+// needs: per cut range, 128 * (query tiles per CTA) rows of D fp32 partial outputs, then one fp32
+// lse per row.  0 bytes (and n_parts = 1) when the launch runs unsplit.
+struct KeySplit {
+  SplitPlan plan{0, 0, 1};
+  size_t o_bytes = 0, l_bytes = 0;
+  size_t bytes() const { return o_bytes + l_bytes; }
 };
 
-// Plans the split for p (nQB, H, B, nK set) and sets up its scratch on `st`.  Causal launches,
-// launches under stream capture, and launches whose scratch cannot be had run unsplit.
-int prepare_key_split(const AttnParams* p, int D, int causal, cudaStream_t st, SplitScratch* sc) {
+int plan_key_split(long long n_items, int nK, int D, int causal, KeySplit* ks) {
+  *ks = KeySplit{};
+  ks->plan.n_whole = n_items;
   const int max_parts = g_key_split_max.load();
   if (causal || max_parts < 2) return ATTN_OK;
   int dev = 0, sms = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices ||
-      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
-    (void)cudaGetLastError();
-    return ATTN_OK;
-  }
-  const SplitPlan sp = key_split_plan(1ll * p->nQB * p->H * p->B, sms, p->nK, max_parts);
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "device query: %s", cudaGetErrorString(e));
+  const SplitPlan sp = key_split_plan(n_items, sms, nK, max_parts);
   if (sp.n_parts < 2) return ATTN_OK;
-  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
-  if (cudaStreamIsCapturing(st, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone) {
-    (void)cudaGetLastError();
-    return ATTN_OK;
-  }
+  if (sp.n_whole > 0x7fffffffll || sp.n_tail > 0x7fffffffll)
+    return fail(ATTN_ERR_INVALID_ARG, "too many query blocks");
+  ks->plan = sp;
   const size_t rows = 128ull * attn_q_tiles(D) * sp.n_tail * sp.n_parts;
-  const size_t o_bytes = rows * D * 4, l_bytes = rows * 4;
-  cudaMemPool_t pool = nullptr;
-  void* ptr = nullptr;
-  if (split_pool(dev, &pool) != cudaSuccess ||
-      cudaMallocFromPoolAsync(&ptr, o_bytes + l_bytes, pool, st) != cudaSuccess) {
-    (void)cudaGetLastError();
-    return ATTN_OK;
-  }
-  sc->ptr = ptr;
-  sc->st = st;
-  char* base = static_cast<char*>(ptr);
-  sc->sp.n_whole = static_cast<int>(sp.n_whole);
-  sc->sp.n_tail = static_cast<int>(sp.n_tail);
-  sc->sp.n_parts = sp.n_parts;
-  sc->sp.part_o = reinterpret_cast<float*>(base);
-  sc->sp.part_l = reinterpret_cast<float*>(base + o_bytes);
+  ks->o_bytes = rows * D * 4;
+  ks->l_bytes = rows * 4;
+  return ATTN_OK;
+}
+
+// The split parameters of a launch with the caller's workspace (nullptr: unsplit).  A
+// workspace smaller than the plan needs is an error, never a silent fallback: the same
+// arguments always give the same launches.
+int key_split_params(const AttnParams& p, int D, int causal, void* ws, size_t ws_bytes, SplitParams* out,
+                     bool* split) {
+  *split = false;
+  if (ws == nullptr) return ATTN_OK;
+  KeySplit ks;
+  int rc = plan_key_split(1ll * p.nQB * p.H * p.B, p.nK, D, causal, &ks);
+  if (rc != ATTN_OK) return rc;
+  if (ks.plan.n_parts < 2) return ATTN_OK;
+  if (ws_bytes < ks.bytes())
+    return fail(ATTN_ERR_INVALID_ARG, "workspace of %zu bytes is smaller than the %zu the key split needs "
+                "(attn_fwd_split_workspace_bytes)", ws_bytes, ks.bytes());
+  char* base = static_cast<char*>(ws);
+  out->n_whole = static_cast<int>(ks.plan.n_whole);
+  out->n_tail = static_cast<int>(ks.plan.n_tail);
+  out->n_parts = ks.plan.n_parts;
+  out->part_o = reinterpret_cast<float*>(base);
+  out->part_l = reinterpret_cast<float*>(base + ks.o_bytes);
+  *split = true;
   return ATTN_OK;
 }
 
@@ -325,10 +294,8 @@ int run_attn(const void* q, const void* k, const void* v, const float* qs, const
   p.err_info = err + 1;
   p.kv_group = 1;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  SplitScratch scratch;
-  if ((rc = prepare_key_split(&p, D, causal, st, &scratch)) != ATTN_OK) return rc;
-  return fp8 ? dispatch<true>(tq, tk, tv, p, D, causal, st, scratch.plan())
-             : dispatch<false>(tq, tk, tv, p, D, causal, st, scratch.plan());
+  return fp8 ? dispatch<true>(tq, tk, tv, p, D, causal, st, nullptr)
+             : dispatch<false>(tq, tk, tv, p, D, causal, st, nullptr);
 }
 
 template <bool FP8, bool CAUSAL>
@@ -534,9 +501,18 @@ int run_bwd(const void* q, const void* k, const void* v, const void* o, const vo
 // Grouped-query prefill: bf16 inputs (qs = ks = vs = nullptr) or E4M3 codes with block scales
 // (q_scale [B, Hq, nK], k_scale and v_scale [B, Hkv, nK]).
 int run_gqa(const void* q, const void* k, const void* v, const float* qs, const float* ks, const float* vs, void* o,
-            float* lse, int B, int Hq, int Hkv, int S, int D, int causal, float scale, bool fp8, void* stream) {
+            float* lse, int B, int Hq, int Hkv, int S, int D, int causal, float scale, bool fp8, void* stream,
+            void* ws = nullptr, size_t ws_bytes = 0) {
   int rc = check_gqa_args(q, k, v, o, lse, B, Hq, Hkv, S, S, D, causal, scale, true, fp8 ? 1 : 2);
   if (rc != ATTN_OK) return rc;
+  if (ws != nullptr) {
+    if (!aligned16(ws)) return fail(ATTN_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
+    const size_t nq = 1ull * B * S * Hq * D, nkv = 1ull * B * S * Hkv * D, esz = fp8 ? 1 : 2;
+    if (overlap(ws, ws_bytes, q, nq * esz) || overlap(ws, ws_bytes, k, nkv * esz) ||
+        overlap(ws, ws_bytes, v, nkv * esz) || overlap(ws, ws_bytes, o, nq * 2) ||
+        (lse != nullptr && overlap(ws, ws_bytes, lse, 4ull * B * Hq * S)))
+      return fail(ATTN_ERR_INVALID_ARG, "workspace overlaps an input or output");
+  }
   int* err = nullptr;
   if ((rc = err_words(&err)) != ATTN_OK) return rc;
   CUtensorMap tq, tk, tv;
@@ -562,10 +538,11 @@ int run_gqa(const void* q, const void* k, const void* v, const float* qs, const 
   p.err_info = err + 1;
   p.kv_group = Hq / Hkv;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  SplitScratch scratch;
-  if ((rc = prepare_key_split(&p, D, causal, st, &scratch)) != ATTN_OK) return rc;
-  return fp8 ? dispatch<true>(tq, tk, tv, p, D, causal, st, scratch.plan())
-             : dispatch<false>(tq, tk, tv, p, D, causal, st, scratch.plan());
+  SplitParams sp{};
+  bool split = false;
+  if ((rc = key_split_params(p, D, causal, ws, ws_bytes, &sp, &split)) != ATTN_OK) return rc;
+  return fp8 ? dispatch<true>(tq, tk, tv, p, D, causal, st, split ? &sp : nullptr)
+             : dispatch<false>(tq, tk, tv, p, D, causal, st, split ? &sp : nullptr);
 }
 
 }  // namespace
@@ -913,7 +890,7 @@ int attn_selftest_bounded_wait(long long spin_cycles, void* stream) {
   return ok();
 }
 
-int attn_version(void) { return 110; }
+int attn_version(void) { return 120; }
 
 void attn_set_key_split(int max_parts) {
   g_key_split_max.store(max_parts < 1 ? 1 : (max_parts > KEY_SPLIT_MAX_PARTS ? KEY_SPLIT_MAX_PARTS : max_parts));
@@ -927,6 +904,31 @@ int attn_key_split_plan(long long n_items, int sms, int key_tiles, int max_parts
   out[1] = sp.n_tail;
   out[2] = sp.n_parts;
   return ok();
+}
+
+size_t attn_fwd_split_workspace_bytes(int B, int Hq, int S, int D, int causal) {
+  if (B < 1 || Hq < 1 || S < 1 || (D != 64 && D != 128 && D != 256) || (causal != 0 && causal != 1)) return 0;
+  const long long rows_per_cta = 128ll * attn_q_tiles(D);
+  const long long n_items = 1ll * ((S + rows_per_cta - 1) / rows_per_cta) * Hq * B;
+  KeySplit ks;
+  if (plan_key_split(n_items, (S + 127) / 128, D, causal, &ks) != ATTN_OK) return 0;
+  return ks.bytes();
+}
+
+int attn_fwd_split(const void* q, const void* k, const void* v, const float* q_scale, const float* k_scale,
+                   const float* v_scale, void* o, float* lse, int B, int Hq, int Hkv, int S, int D, int causal,
+                   float scale, int dtype, void* workspace, size_t workspace_bytes, void* stream) {
+  if (dtype != ATTN_BF16 && dtype != ATTN_FP8_E4M3)
+    return fail(ATTN_ERR_INVALID_ARG, "dtype must be ATTN_BF16 (0) or ATTN_FP8_E4M3 (1)");
+  const int n_scales = (q_scale != nullptr) + (k_scale != nullptr) + (v_scale != nullptr);
+  if (dtype == ATTN_BF16 && n_scales != 0) return fail(ATTN_ERR_INVALID_ARG, "bf16 inputs take no scales");
+  if (n_scales != 0 && n_scales != 3)
+    return fail(ATTN_ERR_INVALID_ARG, "give all three scale arrays or none (unit scales)");
+  if ((reinterpret_cast<uintptr_t>(q_scale) | reinterpret_cast<uintptr_t>(k_scale) |
+       reinterpret_cast<uintptr_t>(v_scale)) & 3u)
+    return fail(ATTN_ERR_INVALID_ARG, "scale arrays must be 4-byte aligned");
+  return run_gqa(q, k, v, q_scale, k_scale, v_scale, o, lse, B, Hq, Hkv, S, D, causal, scale,
+                 dtype == ATTN_FP8_E4M3, stream, workspace, workspace_bytes);
 }
 
 }  // extern "C"

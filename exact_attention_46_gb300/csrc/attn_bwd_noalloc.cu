@@ -15,8 +15,6 @@
 // the array and may produce wrong gradients; serialise them.
 #include <cuda_runtime.h>
 
-#include <mutex>
-
 #include "internal.h"
 
 namespace ea46 {
@@ -26,28 +24,18 @@ namespace {
 // The scratch itself: NOALLOC_BWD_SCRATCH_BYTES (16 MiB) per GPU.
 static __device__ __align__(256) float g_bwd_scratch[NOALLOC_BWD_SCRATCH_BYTES / sizeof(float)];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_scratch_mu;
-float* g_scratch_ptr[kMaxDevices] = {};
-
 }  // namespace
 
 // The device address of the current GPU's scratch.  In host code g_bwd_scratch names a host
-// stand-in, not device memory, so the address comes from cudaGetSymbolAddress, once per device,
-// on the first call made while that device is current.
+// stand-in, not device memory, so the address comes from cudaGetSymbolAddress, with the
+// caller's device current.  It is looked up on every call rather than kept: the lookup is a
+// host-side query (no stream work), and an address kept from an earlier context -- before a
+// device reset reloaded the module -- would point at memory that no longer exists.
 cudaError_t noalloc_bwd_scratch(float** out) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  void* p = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&p, g_bwd_scratch);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  std::lock_guard<std::mutex> lk(g_scratch_mu);
-  if (g_scratch_ptr[dev] == nullptr) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_bwd_scratch);
-    if (e != cudaSuccess) return e;
-    g_scratch_ptr[dev] = static_cast<float*>(p);
-  }
-  *out = g_scratch_ptr[dev];
+  *out = static_cast<float*>(p);
   return cudaSuccess;
 }
 

@@ -16,7 +16,8 @@ __all__ = ["attn_fwd", "attn_fwd_fp8", "attn_fwd_varlen", "attn_fwd_varlen_fp8",
            "hadamard_rotate_quant_fp8",
            "hadamard_rotate_quant_fp8_varlen", "rope_cos_sin_table", "rope_hadamard_rotate_quant_fp8",
            "rope_hadamard_rotate_quant_fp8_varlen", "varlen_scale_blocks", "block_count", "check",
-           "set_spin_limit", "set_key_split", "key_split_plan", "selftest_bounded_wait", "ATTN_BF16", "ATTN_FP8_E4M3"]
+           "set_spin_limit", "set_key_split", "key_split_plan", "attn_fwd_split", "split_workspace_bytes",
+           "selftest_bounded_wait", "ATTN_BF16", "ATTN_FP8_E4M3"]
 
 ATTN_BF16 = 0
 ATTN_FP8_E4M3 = 1
@@ -431,6 +432,51 @@ def key_split_plan(n_items, sms, key_tiles, max_parts=4):
     out = (ctypes.c_longlong * 3)()
     _lib.call("attn_key_split_plan", int(n_items), int(sms), int(key_tiles), int(max_parts), ctypes.addressof(out))
     return tuple(int(x) for x in out)
+
+
+def split_workspace_bytes(B, Hq, S, D, causal=False):
+    """Bytes of workspace attn_fwd_split needs for this shape on the current device (0: no split)."""
+    return int(_lib.load().attn_fwd_split_workspace_bytes(int(B), int(Hq), int(S), int(D), int(bool(causal))))
+
+
+def attn_fwd_split(q, k, v, q_scale=None, k_scale=None, v_scale=None, causal=False, scale=0.0, out=None,
+                   lse=None, want_lse=True, workspace=None, stream=None):
+    """attn_fwd / attn_fwd_fp8 / attn_fwd_gqa(_fp8) with a workspace for the key-split tail.
+
+    q [B, S, Hq, D], k, v [B, S, Hkv, D]: bf16, or E4M3 codes with all three block-scale arrays
+    (or none: unit scales).  ``workspace``: a CUDA tensor of at least split_workspace_bytes(...)
+    bytes, or None to allocate one here (torch's allocator) when the plan splits; an explicit
+    empty tensor runs unsplit."""
+    dev = _inputs(("q", "k", "v"), (q, k, v), _BF16 + _CODES, 4)
+    B, S, Hq, D = q.shape
+    Hkv = k.shape[2]
+    for n, t in (("k", k), ("v", v)):
+        _arg(t, n, (q.dtype,), shape=(B, S, Hkv, D))
+    fp8 = q.element_size() == 1
+    scales = (q_scale, k_scale, v_scale)
+    if any(s is not None for s in scales):
+        if not fp8 or any(s is None for s in scales):
+            raise ValueError("block scales go with E4M3 inputs, all three or none")
+        _arg(q_scale, "q_scale", _F32, shape=(B, Hq, block_count(S)), device=dev)
+        for n, t in (("k_scale", k_scale), ("v_scale", v_scale)):
+            _arg(t, n, _F32, shape=(B, Hkv, block_count(S)), device=dev)
+    _opt(out, "out", _BF16, shape=(B, S, Hq, D), device=dev)
+    _opt(lse, "lse", _F32, shape=(B, Hq, S), device=dev)
+    if out is None:
+        out = torch.empty((B, S, Hq, D), dtype=torch.bfloat16, device=dev)
+    if lse is None and want_lse:
+        lse = torch.empty((B, Hq, S), dtype=torch.float32, device=dev)
+    if workspace is None:
+        need = split_workspace_bytes(B, Hq, S, D, causal)
+        workspace = torch.empty((need,), dtype=torch.uint8, device=dev) if need else None
+    ws_ptr, ws_bytes = None, 0
+    if workspace is not None:
+        _arg(workspace, "workspace", (workspace.dtype,), device=dev)
+        ws_ptr, ws_bytes = (_ptr(workspace), workspace.numel() * workspace.element_size()) if workspace.numel() else (None, 0)
+    _lib.call("attn_fwd_split", _ptr(q), _ptr(k), _ptr(v), _ptr(q_scale), _ptr(k_scale), _ptr(v_scale),
+              _ptr(out), _ptr(lse), B, Hq, Hkv, S, D, int(bool(causal)), float(scale),
+              ATTN_FP8_E4M3 if fp8 else ATTN_BF16, ws_ptr, ws_bytes, _stream(stream))
+    return out, lse
 
 
 def selftest_bounded_wait(cycles, stream=None):

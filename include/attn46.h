@@ -66,15 +66,11 @@ typedef enum {
  *   causal  : 0 = every query sees every key; 1 = query i sees keys j <= i.
  *   scale   : logit multiplier; 0 selects 1/sqrt(D); negative or non-finite
  *             values are rejected.
- *   Scheduling: one persistent CTA per SM walks the query blocks.  Without
- *   the causal mask, when the blocks do not fill the last round of CTAs, the
- *   blocks of that round are cut into key ranges (attn_key_split_plan) whose
- *   partial results are merged in a fixed order; their scratch comes, per
- *   launch, from a memory pool the library keeps on each device (stream
- *   ordered, returned after the launch; blocks stay cached in the pool).
- *   Under stream capture, or when that memory cannot be had, the launch runs
- *   unsplit.  Split and unsplit results differ only by rounding.  The same
- *   holds for attn_fwd_fp8, attn_fwd_gqa and attn_fwd_gqa_fp8.
+ *   Scheduling: one persistent CTA per SM walks the query blocks.  attn_fwd,
+ *   attn_fwd_fp8, attn_fwd_gqa and attn_fwd_gqa_fp8 allocate nothing and
+ *   always run every block whole; the key-split tail (cutting the blocks of
+ *   a partly filled last round into key ranges) needs scratch and is
+ *   attn_fwd_split's, with a caller workspace.
  */
 int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
              int B, int H, int S, int D, int causal, float scale, int dtype,
@@ -301,9 +297,11 @@ int attn_bwd_gqa(const void* q, const void* k, const void* v, const void* o, con
  *   Limit: attn_bwd_workspace_bytes(B, H, S) <= 16 MiB, i.e.
  *   B * H * (S rounded up to 128) <= 2,097,152; larger problems are rejected
  *   with ATTN_ERR_INVALID_ARG before anything runs.
- *   The first call on a device looks up the scratch's device address
- *   (cudaGetSymbolAddress) with that device current; make that first call
- *   before any stream capture.  All calls on a device share the scratch and
+ *   Every call looks up the scratch's device address (cudaGetSymbolAddress)
+ *   with the caller's device current -- a host-side query, nothing is
+ *   allocated; make the first call on a device before any stream capture, as
+ *   that first lookup loads the library's device code there.  All calls on a
+ *   device share the scratch and
  *   it keeps the last call's contents (every call rewrites what it reads, so
  *   nothing needs clearing); calls whose kernels overlap on the GPU race on
  *   it and may give wrong gradients, so serialise them.
@@ -388,9 +386,54 @@ int attn_check(void* stream);
 void attn_set_spin_limit(long long cycles);
 
 /*
+ * attn_fwd_split -- attn_fwd / attn_fwd_fp8 / attn_fwd_gqa / attn_fwd_gqa_fp8
+ *   with a caller workspace for the key-split tail.  The pages have no
+ *   counterpart ([HADA] "Weitere Optimierungen und künftige Integration"
+ *   names the persistent kernel; how its last round is filled is this
+ *   library's scheduling).
+ *   Without the causal mask, when the B * Hq * ceil(S / (128 * tiles per CTA))
+ *   query blocks do not fill the last round of persistent CTAs (one per SM),
+ *   the blocks of that round may be cut into key ranges (attn_key_split_plan,
+ *   at most attn_set_key_split's ranges); each range writes its normalised
+ *   partial output (fp32) and lse to the workspace, and a second kernel on
+ *   the same stream merges every cut row over its ranges in a fixed order.
+ *   q, k, v, o, lse, B, S, D, causal, scale : as attn_fwd_gqa (Hq query heads,
+ *             Hkv key/value heads, Hq a multiple of Hkv; Hkv = Hq is attn_fwd).
+ *   q_scale, k_scale, v_scale : NULL for bf16 (dtype ATTN_BF16) and for E4M3
+ *             codes with unit scales; all three non-null for E4M3 codes with
+ *             block scales (layouts as attn_fwd_gqa_fp8).  One or two non-null
+ *             is ATTN_ERR_INVALID_ARG.
+ *   dtype   : ATTN_BF16 or ATTN_FP8_E4M3.
+ *   workspace : caller-owned device scratch, 16-byte aligned, overwritten,
+ *             overlapping no input or output; or NULL, which runs every block
+ *             whole (the result of attn_fwd).  With a workspace, a problem the
+ *             plan splits needs workspace_bytes >=
+ *             attn_fwd_split_workspace_bytes(B, Hq, S, D, causal); less is
+ *             ATTN_ERR_INVALID_ARG, never a silent fallback, so the same
+ *             arguments always run the same launches and give the same bits.
+ *   Rows of blocks that run whole are bitwise those of attn_fwd; rows of cut
+ *   blocks differ by rounding only (each range rounds its softmax numerators
+ *   against its own running maximum).
+ */
+int attn_fwd_split(const void* q, const void* k, const void* v, const float* q_scale,
+                   const float* k_scale, const float* v_scale, void* o, float* lse, int B,
+                   int Hq, int Hkv, int S, int D, int causal, float scale, int dtype,
+                   void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * attn_fwd_split_workspace_bytes -- the workspace attn_fwd_split needs for
+ *   this shape on the current device (its SM count sets the plan) under the
+ *   current attn_set_key_split limit: 4 * (D + 1) bytes per row of every cut
+ *   range, 128 * (2, or 1 at D = 256) rows per range.  0 when the plan does
+ *   not split (causal, a full last round, too few key tiles, or the split
+ *   turned off) or for invalid arguments.
+ */
+size_t attn_fwd_split_workspace_bytes(int B, int Hq, int S, int D, int causal);
+
+/*
  * attn_set_key_split -- the most key ranges a query block of the last,
  *   partly filled round of a non-causal forward may be cut into (see
- *   attn_fwd); clamped to [1, 4], 1 turns the split off, 4 is the default.
+ *   attn_fwd_split); clamped to [1, 4], 1 turns the split off, 4 is the default.
  *   Applies to later launches from any host thread.  The pages have no
  *   counterpart: this is a scheduling choice of this library.
  */

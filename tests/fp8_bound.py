@@ -173,7 +173,12 @@ def check(o, lse, ref, lse_tol=LSE_TOL, rms_min_keys=128):
     err = np.abs(o - O)
     worst = ref["worst"] + half_ulp_bf16(np.abs(O) + ref["worst"])
     stat = ref["stat"] + half_ulp_bf16(np.abs(O) + ref["stat"])
-    r_w, r_s = float((err / worst).max()), float((err / stat).max())
+    def ratio(bound):
+        # an exact zero (a zero value, or no error possible) must be met exactly
+        safe = np.where(bound > 0, bound, 1.0)
+        return float(np.where(bound > 0, err / safe, np.where(err > 0, np.inf, 0.0)).max())
+
+    r_w, r_s = ratio(worst), ratio(stat)
     assert r_w <= 1.0, f"worst-case bound exceeded: {int((err > worst).sum())} elements, max ratio {r_w:.3f}"
     assert r_s <= 1.0, f"statistical bound exceeded: {int((err > stat).sum())} elements, max ratio {r_s:.3f}"
     many = np.broadcast_to((ref["n"] >= rms_min_keys)[..., None], err.shape)

@@ -45,11 +45,12 @@ def bf16_stats(gpu, ref):
     return float((err - half_ulp_bf16(ref)).max()), float(np.sqrt(np.mean(err ** 2))), float(err.max())
 
 
-def check_codes(gpu_codes, ref, tie_rtol, tie_atol, max_frac):
-    """E4M3 codes vs the oracle's: equal, except where the oracle's pre-rounding value lies
-    within tie_rtol * |pre| + tie_atol of a rounding midpoint; there the two codes must be the
-    neighbouring grid values around that midpoint.  At most max(3, max_frac * size) differ.
-    Returns the number of differing codes."""
+def check_codes(gpu_codes, ref, tie_rtol, tie_atol):
+    """E4M3 codes vs the oracle's: equal, except where the oracle's pre-rounding quotient lies
+    within tie_rtol * |pre| + tie_atol of a rounding midpoint (the oracle decides midpoints
+    exactly, ties to even; a kernel working in fp32 may land on either side); there the two
+    codes must be the neighbouring grid values around that midpoint.  Returns the number of
+    differing codes."""
     from oracle import e4m3
     diff = gpu_codes != ref["codes"]
     n_diff = int(diff.sum())
@@ -62,7 +63,6 @@ def check_codes(gpu_codes, ref, tie_rtol, tie_atol, max_frac):
         # neighbours on the grid: nothing representable strictly between them
         lo, hi = np.minimum(a, b), np.maximum(a, b)
         assert np.all(e4m3.round_e4m3((lo + mid) / 2) == lo) and np.all(e4m3.round_e4m3((hi + mid) / 2) == hi)
-    assert n_diff <= max(3, max_frac * gpu_codes.size), n_diff
     assert not np.any((gpu_codes & 0x7F) == 0x7F), "NaN code produced"
     return n_diff
 

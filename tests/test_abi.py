@@ -40,7 +40,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_version(lib):
-    assert lib.attn_version() == 110
+    assert lib.attn_version() == 120
 
 
 FAKE = 1 << 20   # 16-byte aligned non-null fake device addresses: never dereferenced
@@ -320,3 +320,28 @@ def test_key_split_plan_is_the_cheapest_last_round(lib):
                     else:
                         assert w % sms == 0 and t == tail and cost[s] == best <= 0.85 * whole
                         assert all(cost[k] > best for k in cost if k < s)
+
+
+def test_split_forward_rejects_bad_arguments_without_a_gpu(lib):
+    # dtype, scale-array combinations and the workspace are checked before any device call
+    bad = [
+        # bf16 with scales
+        (FAKE, FAKE * 2, FAKE * 3, FAKE * 8, FAKE * 9, FAKE * 10, FAKE * 4, None, 1, 2, 2, 128, 128, 0, 0.0, 0),
+        # E4M3 with only two of the three scale arrays
+        (FAKE, FAKE * 2, FAKE * 3, FAKE * 8, None, FAKE * 10, FAKE * 4, None, 1, 2, 2, 128, 128, 0, 0.0, 1),
+        # dtype out of range
+        (FAKE, FAKE * 2, FAKE * 3, None, None, None, FAKE * 4, None, 1, 2, 2, 128, 128, 0, 0.0, 5),
+        # Hq not a multiple of Hkv
+        (FAKE, FAKE * 2, FAKE * 3, None, None, None, FAKE * 4, None, 1, 3, 2, 128, 128, 0, 0.0, 0),
+    ]
+    for a in bad:
+        assert lib.attn_fwd_split(*a, None, 0, None) == 1, a
+    # a misaligned or overlapping workspace
+    base = (FAKE, FAKE * 2, FAKE * 3, None, None, None, FAKE * 4, None, 1, 2, 2, 128, 128, 0, 0.0, 0)
+    assert lib.attn_fwd_split(*base, FAKE * 6 + 8, 4096, None) == 1
+    assert lib.attn_fwd_split(*base, FAKE * 2, 4096, None) == 1
+
+
+def test_split_workspace_bytes_of_invalid_shapes_is_zero(lib):
+    for a in ((0, 16, 8192, 128, 0), (2, 16, 0, 128, 0), (2, 16, 8192, 96, 0), (2, 16, 8192, 128, 3)):
+        assert lib.attn_fwd_split_workspace_bytes(*a) == 0

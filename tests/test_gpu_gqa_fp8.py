@@ -2,15 +2,12 @@
 vs the fp64 oracle, through the C ABI (GPU).
 
 The kernels get the oracle's own E4M3 codes and block scales (Q and K rotated by the same
-random signs, V not rotated), so both sides see the same inputs.  O_deq is exact grouped
-attention on the de-quantised values and O_emul the oracle's FP8 reading, which also rounds
-the softmax numerators to E4M3 (relative to the exact row max; the kernel rounds relative to
-its running max, split by split -- independent roundings of the same size).  The check:
-
-    RMS(O_gpu - O_deq) <= 2 * RMS(O_emul - O_deq) + RMS(half a bf16 ulp of O_deq) + 1e-4
-
-(the middle term is the bf16 rounding of the output, which is all there is for one key),
-and lse, which the numerator rounding does not touch, within 1e-3 of the exact one.
+random signs, V not rotated), so both sides see the same inputs.  Every output element must
+lie within the FP8 bounds of tests/fp8_bound.py against exact grouped attention on the
+de-quantised values (the decoding kernel takes V's largest block scale per key split, which
+only raises the ratios r_j the bound divides by); lse within 1e-3 of the exact one.  The
+bounds' reference is checked against the oracle's grouped attention (oracle/gqa.py, pinned
+against torch in the CPU tests) on every case.
 """
 
 import numpy as np
@@ -20,11 +17,10 @@ import torch
 from exact_attention_46_gb300 import ops, synth
 from oracle import gqa as oracle_gqa
 from oracle import quantise
-from tests.helpers import half_ulp_bf16, to64
+from tests import fp8_bound
+from tests.helpers import check_codes, to64
 
 pytestmark = pytest.mark.gpu
-
-LSE_TOL = 1e-3
 
 
 def raw_inputs(B, Sq, Sk, Hq, Hkv, D, case, block_gain=False):
@@ -55,22 +51,19 @@ def run(B, Sq, Sk, Hq, Hkv, D, causal, case, block_gain=False, rotate=True, fn=N
     t = [torch.from_numpy(np.ascontiguousarray(a)).to(dev) for a in (q8, k8, v8, sq, sk, sv)]
     o, lse = (fn or ops.attn_decode_fp8)(*t, causal=causal)
     ops.check()
-    O_deq, lse_deq = oracle_gqa.attention_gqa(qd, kd, vd, causal=causal)
-    O_emul, _ = oracle_gqa.attention_gqa(qd, kd, vd, causal=causal, round_p=True)
-    return to64(o), to64(lse), O_deq, O_emul, lse_deq
+    return to64(o), to64(lse), reference(qd, kd, vd, sv, D, causal)
 
 
-def rms(x):
-    return float(np.sqrt(np.mean(np.square(x))))
+def reference(qd, kd, vd, sv, D, causal):
+    ref = fp8_bound.reference(qd, kd, vd, sv, 1 / np.sqrt(D), causal)
+    O_gqa, lse_gqa = oracle_gqa.attention_gqa(qd, kd, vd, causal=causal)
+    np.testing.assert_allclose(ref["O"], O_gqa, rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(ref["lse"], lse_gqa, rtol=1e-10, atol=1e-12)
+    return ref
 
 
-def check(o, lse, O_deq, O_emul, lse_deq):
-    assert np.isfinite(o).all()
-    e_gpu, e_emul = rms(o - O_deq), rms(O_emul - O_deq)
-    bound = 2 * e_emul + rms(half_ulp_bf16(O_deq)) + 1e-4
-    assert e_gpu <= bound, (e_gpu, e_emul, bound)
-    lse_err = float(np.abs(lse - lse_deq).max())
-    assert lse_err <= LSE_TOL, lse_err
+def check(o, lse, ref):
+    fp8_bound.check(o, lse, ref)
 
 
 @pytest.mark.parametrize("D", [64, 128, 256])
@@ -121,11 +114,9 @@ def test_decode_fp8_without_rotation():
 
 
 def test_decode_fp8_from_the_quantiser():
-    # the GPU quantiser feeds the decoding kernel.  Rotated Q and K give the logits of the
-    # unrotated inputs, so against exact attention on the original bf16 values the error is
-    # that of the E4M3 inputs (e_in: exact attention on the oracle's quantisation of the same
-    # values) plus the kernel's own bound above (triangle inequality); the GPU quantiser's
-    # codes are the oracle's but for rounding ties
+    # the GPU quantiser feeds the decoding kernel; element by element against exact grouped
+    # attention on the oracle's de-quantised values, the bounds widened by the tie widths of
+    # the codes (the GPU quantiser's codes are the oracle's but for rounding midpoints)
     B, Sq, Sk, Hq, Hkv, D = 2, 1, 5000, 16, 2, 128
     q, k, v = raw_inputs(B, Sq, Sk, Hq, Hkv, D, case=83)
     qb, kb, vb = (torch.from_numpy(a).to(torch.bfloat16) for a in (q, k, v))
@@ -137,15 +128,15 @@ def test_decode_fp8_from_the_quantiser():
     v8, sv = ops.hadamard_rotate_quant_fp8(vb.to(dev), None)
     o, lse = ops.attn_decode_fp8(q8, k8, v8, sq, sk, sv, causal=True)
     ops.check()
-    O_ref, lse_ref = oracle_gqa.attention_gqa(to64(qb), to64(kb), to64(vb), causal=True)
     s64 = s.astype(np.float64)
-    qd, kd, vd = quantised(to64(qb), s64)[2], quantised(to64(kb), s64)[2], quantised(to64(vb), None)[2]
-    O_deq, lse_deq = oracle_gqa.attention_gqa(qd, kd, vd, causal=True)
-    O_emul, _ = oracle_gqa.attention_gqa(qd, kd, vd, causal=True, round_p=True)
-    e_in, e_p = rms(O_deq - O_ref), rms(O_emul - O_deq)
-    bound = e_in + 2 * e_p + rms(half_ulp_bf16(O_deq)) + 1e-4
-    assert rms(to64(o) - O_ref) <= bound, (rms(to64(o) - O_ref), e_in, e_p)
-    assert float(np.abs(to64(lse) - lse_ref).max()) <= float(np.abs(lse_deq - lse_ref).max()) + LSE_TOL
+    res = [quantise.quantise_blocks(to64(qb), s64), quantise.quantise_blocks(to64(kb), s64),
+           quantise.quantise_blocks(to64(vb), None)]
+    for r, g in zip(res, (q8, k8, v8)):
+        check_codes(g.cpu().numpy(), r, 1e-5, 1e-12)
+    deq = [quantise.dequantise(r["q"], r["scale"]) for r in res]
+    widths = [fp8_bound.tie_widths_blocks(r) for r in res]
+    ref = fp8_bound.reference(*deq, res[2]["scale"], 1 / np.sqrt(D), True, dq=widths[0], dk=widths[1], dv=widths[2])
+    fp8_bound.check(to64(o), to64(lse), ref)
 
 
 def test_decode_fp8_without_lse_and_repeatable():
@@ -175,8 +166,6 @@ def test_decode_fp8_zero_value_scales():
     t = [torch.from_numpy(np.ascontiguousarray(a)).to(dev) for a in (q8, k8, v8, sq, sk, sv)]
     o, lse = ops.attn_decode_fp8(*t, causal=True)
     ops.check()
-    O_deq, lse_deq = oracle_gqa.attention_gqa(qd, kd, vd, causal=True)
-    O_emul, _ = oracle_gqa.attention_gqa(qd, kd, vd, causal=True, round_p=True)
     og = to64(o)
     assert np.all(og[1, :, 4:8] == 0.0)                     # query heads of key/value head 1, batch 1
-    check(og, to64(lse), O_deq, O_emul, lse_deq)
+    check(og, to64(lse), reference(qd, kd, vd, sv, D, True))
