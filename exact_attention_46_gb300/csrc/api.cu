@@ -88,7 +88,7 @@ CUtensorMapL2promotion l2_promotion(int row_bytes) {
                           : (row_bytes >= 128 ? CU_TENSOR_MAP_L2_PROMOTION_L2_128B : CU_TENSOR_MAP_L2_PROMOTION_L2_64B);
 }
 
-int make_qkv_map(CUtensorMap* m, const void* ptr, int B, int S, int H, int D, bool fp8) {
+int make_qkv_map(CUtensorMap* m, const void* ptr, int B, int S, int H, int D, bool fp8, int box_rows = 128) {
   EncodeTiledFn enc = encode_fn();
   if (enc == nullptr) return fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled entry point unavailable");
   const int esz = fp8 ? 1 : 2;
@@ -99,7 +99,7 @@ int make_qkv_map(CUtensorMap* m, const void* ptr, int B, int S, int H, int D, bo
   const cuuint64_t strides[3] = {static_cast<cuuint64_t>(D) * esz,
                                  static_cast<cuuint64_t>(H) * D * esz,
                                  static_cast<cuuint64_t>(S) * H * D * esz};
-  const cuuint32_t box[4] = {static_cast<cuuint32_t>(panel_row / esz), 1, 128, 1};
+  const cuuint32_t box[4] = {static_cast<cuuint32_t>(panel_row / esz), 1, static_cast<cuuint32_t>(box_rows), 1};
   const cuuint32_t estr[4] = {1, 1, 1, 1};
   const CUresult r = enc(m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
                          4, const_cast<void*>(ptr), dims, strides, box, estr,
@@ -363,7 +363,8 @@ int run_quant(const void* x, const float* rope_cs, int n_pos, void* out, float* 
   if (rc != ATTN_OK) return rc;
   CUtensorMap tx, tout;
   if ((rc = make_qkv_map(&tx, x, B, S, H, D, false)) != ATTN_OK) return rc;
-  if ((rc = make_qkv_map(&tout, out, B, S, H, D, true)) != ATTN_OK) return rc;
+  // the quantiser stores its codes one warp's rows at a time: 32 rows, 16 at D = 256
+  if ((rc = make_qkv_map(&tout, out, B, S, H, D, true, D == 256 ? 16 : 32)) != ATTN_OK) return rc;
   QuantParams p{B, H, S, nblk, out, scale, signs, rope_cs, spin_limit(), err, err + 1, cu_seqlens, n_seq, n_pos};
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e = D == 64    ? launch_hadamard_quant<64>(tx, tout, p, st)

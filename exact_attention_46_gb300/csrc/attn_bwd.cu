@@ -42,12 +42,6 @@
 
 namespace ea46 {
 
-// Programmatic dependent launch: let the next grid on the stream (launched with programmatic
-// stream serialization) start once every CTA of this grid has issued this; and wait until
-// the grid this one depends on has completed and its memory operations are visible.
-__device__ __forceinline__ void grid_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
-__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-
 namespace {
 
 constexpr float LOG2E = 1.4426950408889634f;

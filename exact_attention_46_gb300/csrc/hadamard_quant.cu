@@ -10,17 +10,20 @@
 //
 // Design: the transform is O(D log D) per row and the kernel is bound by HBM traffic
 // (2 bytes read + 1 byte written per element) once its instruction count is low, so it stays
-// on the FP32 pipes: no tensor cores.  Persistent CTAs stream blocks of 128 rows through a
-// ring of shared-memory stages filled by TMA (the same 128-byte-swizzled box the attention
-// kernel uses), so the loads of the next blocks are in flight while a block is transformed.
-// A thread owns a row (lanes l and l + 16 share one at D = 256), so the butterfly stages run
-// in registers (plus one lane-shuffle stage at D = 256); the 8 lanes of a 128-bit read phase
-// hold 8 rows and read the same 16-byte chunk of each, which the swizzle makes
-// conflict-free.  The random signs are applied as XOR masks on the packed bf16 words, read
-// from a small shared-memory table by broadcast.  Rows beyond S arrive zero-filled.  The
-// codes go back into the consumed stage in the swizzled layout of the E4M3 output map and
-// leave with one tensor store per panel (rows beyond S clipped), so L2 sees whole lines; the
-// stage is refilled once the store has read it.
+// on the FP32 pipes: no tensor cores.  One persistent CTA per SM streams blocks of 128 rows
+// through a ring of NSTAGE shared-memory stages filled by TMA (the same 128-byte-swizzled box
+// the attention kernel uses).  The CTA's threads form G groups of one block's worth of threads;
+// group g takes every G-th block and synchronises on a named barrier of its own.  A stage is
+// refilled with the block NSTAGE further on as soon as its group holds the values in
+// registers -- before the transform -- so about NSTAGE loads stay in flight per SM whatever
+// the groups are doing.  A thread owns a row (lanes l and l + 16 share one at D = 256), so the
+// butterfly stages run in registers (plus one lane-shuffle stage at D = 256); the 8 lanes of
+// a 128-bit read phase hold 8 rows and read the same 16-byte chunk of each, which the swizzle
+// makes conflict-free.  The random signs are applied as XOR masks on the packed bf16 words,
+// read from a small shared-memory table by broadcast.  Rows beyond S arrive zero-filled.  The
+// codes go into the group's own output buffer in the swizzled layout of the E4M3 output map
+// and leave with one tensor store per panel (rows beyond S clipped), so L2 sees whole lines;
+// the buffer is reused once that store has read it.
 //
 // Rotary embedding fused in front (hada.io FA3 summary, same section: the transform is
 // bandwidth-bound and costs nothing extra when fused with a preceding bandwidth-bound op such
@@ -29,7 +32,8 @@
 // transform, with no rounding in between.  A 128-row block would need 128 table rows (4 D
 // bytes each, twice the block's own input), so the kernel rebuilds (cos, sin)(p theta_i) with
 // the angle-addition identity, as the complex product of table row 128 blk + 16 r1 (8 rows per
-// block, bulk-copied with the block) and table row r0 (16 rows, resident), r = 16 r1 + r0.
+// block, bulk-copied into the block's stage after its input) and table row r0 (16 rows,
+// resident), r = 16 r1 + r0.
 //
 // Packed variable-length batches (VARLEN): x is [total, H, D] with sequence offsets cu_seqlens,
 // and a block never straddles two sequences -- sequence s is cut into 128-token blocks from its
@@ -62,40 +66,50 @@ struct QCfg {
   static constexpr int VPT = D < 128 ? D : 128;                            // values per thread
   static constexpr int TPR = D / VPT;                                      // threads per row
   static constexpr int RPW = 32 / TPR;                                     // rows per warp
-  static constexpr int THREADS = QROWS * TPR;
+  static constexpr int GTHREADS = QROWS * TPR;                             // threads of one group
+  static constexpr int GWARPS = GTHREADS / 32;
+  // groups per CTA (one CTA per SM): as many 128-row blocks in registers at once as the
+  // register file holds
+  static constexpr int G = D == 64 ? 4 : (D == 128 ? (ROPE ? 2 : 3) : 1);
+  static constexpr int THREADS = G * GTHREADS;
   static constexpr int ROW_BYTES = D * 2;                                  // bf16 row
   static constexpr int PANEL_BYTES = 128 * 128;                            // 128 rows x 128 B
   static constexpr int NPANEL = ROW_BYTES / 128;                           // 1, 2, 4
-  static constexpr int STAGE_BYTES = QROWS * ROW_BYTES;
-  static constexpr int CTAS_PER_SM = D == 64 ? 4 : (D == 128 ? (ROPE ? 2 : 3) : 1);
-  static constexpr int NSTAGE = D == 256 && !ROPE ? 3 : 2;
-  static constexpr int NWARPS = THREADS / 32;
+  static constexpr int IN_BYTES = QROWS * ROW_BYTES;
   // rotary table rows in shared memory: (cos, sin) pairs, 8 bytes each, a thread's VPT/2 pairs
   // at part * SEG_BYTES; rows padded by 16 bytes so that the 8 rows of one 128-bit read phase
-  // fall in distinct banks
+  // fall in distinct banks.  A block's 8 coarse rows travel in its stage, after the input.
   static constexpr int SEG_BYTES = 4 * VPT;
   static constexpr int TROW = 4 * D + 16;
-  static constexpr int NCSLOT = NSTAGE + 1;                                // coarse-row slots
-  static constexpr int OFF_COARSE = NSTAGE * STAGE_BYTES;
-  static constexpr int OFF_FINE = OFF_COARSE + (ROPE ? NCSLOT * NCOARSE * TROW : 0);
-  static constexpr int OFF_SIGN = OFF_FINE + (ROPE ? NFINE * TROW : 0);
-  // packed-bf16 sign XOR masks [D/2] without RoPE; per-pair masks sign(2i) != sign(2i+1) [D/2]
-  // with it (the even element's sign is folded into the resident rotary rows)
-  static constexpr int SIGN_BYTES = 2 * D;
-  static constexpr int OFF_BAR = OFF_SIGN + SIGN_BYTES;
-  static constexpr int OFF_WMAX = OFF_BAR + 8 * NSTAGE;
-  static constexpr int OFF_ABORT = OFF_WMAX + 2 * NWARPS * 4;
-  static constexpr int OFF_INFO = OFF_ABORT + 16;                          // VARLEN: [NSTAGE] (tok0, rows)
-  static constexpr int SMEM_BYTES = 1024 + OFF_INFO + 8 * NSTAGE;
-  static constexpr uint32_t TX_BYTES = STAGE_BYTES + (ROPE ? NCOARSE * 4 * D : 0);
-  // E4M3 codes of a block, staged in the consumed input stage for one tensor store per
-  // 128-byte panel (64-byte rows, 64-byte swizzle at D = 64)
+  static constexpr int COARSE_OFF = IN_BYTES;
+  static constexpr int STAGE_BYTES = (IN_BYTES + (ROPE ? NCOARSE * TROW : 0) + 1023) / 1024 * 1024;
+  static constexpr int NSTAGE = D == 64 ? (ROPE ? 8 : 10) : (D == 128 ? (ROPE ? 4 : 5) : 2);
+  // E4M3 codes of a block, staged for one tensor store per 128-byte panel (64-byte rows with a
+  // 64-byte swizzle at D = 64), one buffer per group
   static constexpr int CODE_PANEL = D < 128 ? D : 128;                     // bytes per code row
   static constexpr int NCPANEL = D / CODE_PANEL;
+  static constexpr int OUT_BYTES = QROWS * D;
+  static constexpr int OFF_OUT = NSTAGE * STAGE_BYTES;
+  static constexpr int OFF_FINE = OFF_OUT + G * OUT_BYTES;
+  // packed-bf16 sign XOR masks [D/2] without RoPE; per-pair masks sign(2i) != sign(2i+1) [D/2]
+  // with it (the even element's sign is folded into the resident rotary rows)
+  static constexpr int OFF_SIGN = OFF_FINE + (ROPE ? NFINE * TROW : 0);
+  static constexpr int SIGN_BYTES = 2 * D;
+  static constexpr int OFF_BAR = OFF_SIGN + SIGN_BYTES;
+  static constexpr int OFF_WMAX = OFF_BAR + 8 * NSTAGE;                    // [G][2][GWARPS] floats
+  static constexpr int OFF_ISSUED = OFF_WMAX + G * 2 * GWARPS * 4;         // [NSTAGE] loads issued
+  static constexpr int OFF_GEN = OFF_ISSUED + 4 * NSTAGE;                  // [NSTAGE] block in the stage
+  static constexpr int OFF_TAKEN = OFF_GEN + 4 * NSTAGE;                   // [NSTAGE] warps done reading
+  static constexpr int OFF_ABORT = OFF_TAKEN + 4 * NSTAGE;
+  static constexpr int OFF_INFO = (OFF_ABORT + 16 + 7) / 8 * 8;           // VARLEN: [NSTAGE] (tok0, rows)
+  static constexpr int SMEM_BYTES = 1024 + OFF_INFO + 8 * NSTAGE;
+  static constexpr uint32_t TX_BYTES = IN_BYTES + (ROPE ? NCOARSE * 4 * D : 0);
   static_assert(TPR >= 1 && TPR <= 2 && D % VPT == 0, "row split");
-  static_assert(QROWS * D <= STAGE_BYTES, "codes fit the stage");
-  static_assert(SMEM_BYTES * CTAS_PER_SM + 1024 * CTAS_PER_SM <= 228 * 1024, "shared memory budget");
-  static_assert(OFF_COARSE % 16 == 0 && OFF_FINE % 16 == 0 && OFF_SIGN % 16 == 0 && OFF_BAR % 8 == 0,
+  static_assert(G <= 4, "named barriers 1 .. G");
+  static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
+  static_assert(STAGE_BYTES % 1024 == 0 && OFF_OUT % 1024 == 0 && OUT_BYTES % 1024 == 0,
+                "swizzled tiles start on 1024-byte boundaries");
+  static_assert(OFF_FINE % 16 == 0 && OFF_SIGN % 16 == 0 && OFF_BAR % 8 == 0 && (IN_BYTES + TROW) % 16 == 0,
                 "alignment");
 };
 
@@ -116,8 +130,39 @@ __device__ __forceinline__ void rotary_pair(float& v0, float& v1, float ac, floa
   v1 = x0 * s + x1 * c;
 }
 
+__device__ __forceinline__ int ld_acquire_shared(uint32_t addr) {
+  int v;
+  asm volatile("ld.acquire.cta.shared::cta.b32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void st_release_shared(uint32_t addr, int v) {
+  asm volatile("st.release.cta.shared::cta.b32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
+// Count one arrival at a shared counter (acquire + release); returns the count before it.
+__device__ __forceinline__ uint32_t atom_add_acq_rel_shared(uint32_t addr, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.acq_rel.cta.shared::cta.add.u32 %0, [%1], %2;" : "=r"(old) : "r"(addr), "r"(v) : "memory");
+  return old;
+}
+
+// Barrier `id` over the n threads of one group, returning whether any of them passed true.
+__device__ __forceinline__ bool group_bar_or(uint32_t id, uint32_t n, bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, %2, %3, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(v)), "r"(id), "r"(n)
+      : "memory");
+  return r != 0;
+}
+
 template <int D, bool ROTATE, bool ROPE, bool VARLEN>
-__global__ void __launch_bounds__(QCfg<D, ROPE>::THREADS, QCfg<D, ROPE>::CTAS_PER_SM)
+__global__ void __launch_bounds__(QCfg<D, ROPE>::THREADS, 1)
     hadamard_quant_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmOut,
                           const QuantParams p) {
   using C = QCfg<D, ROPE>;
@@ -131,19 +176,34 @@ __global__ void __launch_bounds__(QCfg<D, ROPE>::THREADS, QCfg<D, ROPE>::CTAS_PE
   uint8_t* base = smem_raw + (base_u32 - raw_u32);
   uint32_t* sign_mask = reinterpret_cast<uint32_t*>(base + C::OFF_SIGN);
   const uint32_t bar0 = base_u32 + C::OFF_BAR;
-  float* warp_max = reinterpret_cast<float*>(base + C::OFF_WMAX);          // [2][NWARPS]
   volatile int* abort_flag = reinterpret_cast<volatile int*>(base + C::OFF_ABORT);
+  int* issued = reinterpret_cast<int*>(base + C::OFF_ISSUED);              // loads per stage
+  const uint32_t gen0 = base_u32 + C::OFF_GEN;                             // block each stage holds
+  uint32_t* taken = reinterpret_cast<uint32_t*>(base + C::OFF_TAKEN);    // warps done with each stage
   int2* stage_info = reinterpret_cast<int2*>(base + C::OFF_INFO);         // VARLEN: (tok0, rows)
 
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // Groups of GTHREADS threads each take every G-th block of this CTA; a group synchronises on
+  // its own named barrier (1 + g), never with the other groups.
+  const int g = static_cast<int>(threadIdx.x) / C::GTHREADS;
+  const int gt = static_cast<int>(threadIdx.x) % C::GTHREADS;
+  const bool leader = gt == 0;
+  const uint32_t gbar = 1u + static_cast<uint32_t>(g);
+  const int gwarp = gt >> 5, lane = threadIdx.x & 31;
+  float* warp_max = reinterpret_cast<float*>(base + C::OFF_WMAX) + g * 2 * C::GWARPS;   // [2][GWARPS]
+  const uint32_t outbuf = base_u32 + C::OFF_OUT + g * C::OUT_BYTES;
   // row and the part of it this thread owns: a warp holds RPW rows, lanes l, l + RPW, ... share
   // a row, so the 8 lanes of one 128-bit shared-memory read phase hold 8 different rows
-  const int r = warp * C::RPW + lane % C::RPW;
+  const int r = gwarp * C::RPW + lane % C::RPW;
   const int part = lane / C::RPW;
   const int nblocks = p.nblk * p.H * p.B;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < NSTAGE; ++s) mbar_init(bar0 + 8u * s, 1);
+    for (int s = 0; s < NSTAGE; ++s) {
+      mbar_init(bar0 + 8u * s, 1);
+      issued[s] = 0;
+      taken[s] = 0;
+      st_release_shared(gen0 + 4u * s, -1);
+    }
     *abort_flag = 0;
     fence_barrier_init();
     prefetch_tmap(&tmX);
@@ -178,20 +238,31 @@ __global__ void __launch_bounds__(QCfg<D, ROPE>::THREADS, QCfg<D, ROPE>::CTAS_PE
     }
     if (threadIdx.x == 0) bad |= p.cu_seqlens[0] != 0 || p.cu_seqlens[p.n_seq] != p.S;
     if (__syncthreads_or(bad)) {
+      grid_launch_dependents();
+      grid_dependency_wait();
       if (threadIdx.x == 0 && atomicCAS(p.err_word, 0, 1 /* ATTN_ERR_INVALID_ARG */) == 0) atomicExch(p.err_info, 11);
       return;
     }
   }
   __syncthreads();
-  const WaitCtl ctl{p.spin_limit, abort_flag, p.err_word, p.err_info};
+  // Consecutive quantiser launches on a stream overlap: the next one's CTAs may start on the SMs
+  // this one's CTAs leave (one CTA per SM, so every CTA of this grid is running by now), read
+  // and transform their first blocks, and wait for this grid to complete before they write.
+  grid_launch_dependents();
 
-  int n_issued = 0;                 // thread 0 only: blocks whose load has been issued
-  auto issue = [&](int k) {         // k-th block of this CTA into stage k % NSTAGE
+  // Load of the k-th block of this CTA into stage k % NSTAGE.  Called by thread 0 for the first
+  // NSTAGE blocks, then by lane 0 of the last warp of the group that has just taken block
+  // k - NSTAGE out of that stage: one caller per stage at a time.
+  auto issue = [&](int k) {
     const int bi = static_cast<int>(blockIdx.x) + k * static_cast<int>(gridDim.x);
     const int h = bi % p.H, blk = (bi / p.H) % p.nblk, b = bi / (p.H * p.nblk);
-    const uint32_t st = base_u32 + (k % NSTAGE) * C::STAGE_BYTES;
-    const uint32_t bar = bar0 + 8u * (k % NSTAGE);
+    const int s = k % NSTAGE;
+    const uint32_t st = base_u32 + s * C::STAGE_BYTES;
+    const uint32_t bar = bar0 + 8u * s;
+    issued[s] += 1;
     int tok0 = blk * QROWS, rblk = blk;   // rblk: the block's position block for RoPE
+    // the stage's next phase is block k's; published before the arrival (release), so that a
+    // waiter that sees k here sees the barrier at or past the phase block k's load completes
     if constexpr (VARLEN) {
       // the sequence of index blk: the last s with cu[s] / 128 + s <= blk (cu[0] / 128 + 0 = 0)
       int lo = 0, hi = p.n_seq - 1;
@@ -204,44 +275,64 @@ __global__ void __launch_bounds__(QCfg<D, ROPE>::THREADS, QCfg<D, ROPE>::CTAS_PE
       const int rows = 128 * kb < len ? min(QROWS, len - 128 * kb) : 0;
       tok0 = s0 + 128 * kb;
       rblk = kb;
-      stage_info[k % NSTAGE] = make_int2(tok0, rows);
+      stage_info[s] = make_int2(tok0, rows);
       if (rows == 0) {                // an index no block lives at
+        st_release_shared(gen0 + 4u * s, k);
         mbar_arrive(bar);
-        n_issued = k + 1;
         return;
       }
     }
+    st_release_shared(gen0 + 4u * s, k);
     mbar_arrive_expect_tx(bar, C::TX_BYTES);
 #pragma unroll
     for (int pn = 0; pn < C::NPANEL; ++pn)
       tma_load_4d(st + pn * C::PANEL_BYTES, &tmX, bar, 64 * pn, h, tok0, b,
                   l2_policy_evict_first());
     if (ROPE) {
-      // coarse rows 128 blk + 16 r1 into slot k % NCSLOT.  The slot last held block
-      // k - NSTAGE - 1; issue(k) runs after the CTA-wide barrier of block k - NSTAGE, which
-      // every thread reaches only after finishing block k - NSTAGE - 1.
-      const uint32_t slot = base_u32 + C::OFF_COARSE + (k % C::NCSLOT) * NCOARSE * C::TROW;
+      // coarse rows 128 blk + 16 r1 after the block's input in the same stage
 #pragma unroll
       for (int r1 = 0; r1 < NCOARSE; ++r1)
-        bulk_load(slot + r1 * C::TROW, p.rope_cs + static_cast<size_t>(rblk * QROWS + 16 * r1) * D, 4 * D, bar,
+        bulk_load(st + C::COARSE_OFF + r1 * C::TROW,
+                  p.rope_cs + static_cast<size_t>(rblk * QROWS + 16 * r1) * D, 4 * D, bar,
                   l2_policy_evict_last());
     }
-    n_issued = k + 1;
   };
   const int my_blocks = (nblocks - static_cast<int>(blockIdx.x) + static_cast<int>(gridDim.x) - 1) /
                         static_cast<int>(gridDim.x);
   if (threadIdx.x == 0)
     for (int k = 0; k < NSTAGE && k < my_blocks; ++k) issue(k);
 
-  for (int k = 0; k < my_blocks; ++k) {
-    // Blocks are numbered head-fastest: the CTAs running at one time read all heads of the
+  // Wait for block k in its stage.  The barrier alone tells phases apart only by parity: a group
+  // that runs ahead could find the stage still holding block k - 2 NSTAGE's completed phase,
+  // of the same parity, while block k - NSTAGE has not been taken out yet.  So the stage's
+  // published block number (acquire) must be k first; then the phase test can only see block
+  // k's own phase, complete or not.
+  auto wait_block = [&](int k) -> bool {
+    const int s = k % NSTAGE;
+    const uint32_t bar = bar0 + 8u * s, par = (k / NSTAGE) & 1;
+    const long long t0 = clock64();
+    while (true) {
+      if (ld_acquire_shared(gen0 + 4u * s) == k && mbar_try_wait(bar, par)) return true;
+      if (*abort_flag) return false;
+      if (clock64() - t0 > p.spin_limit) {
+        *abort_flag = 1;
+        if (atomicCAS(p.err_word, 0, 4 /* ATTN_ERR_TIMEOUT */) == 0) atomicExch(p.err_info, 10);
+        return false;
+      }
+    }
+  };
+
+  int n_stores = 0;                  // lane 0: tensor stores this warp has issued from its rows of the buffer
+  bool may_write = false;            // this thread has waited for the previous grid on the stream
+  for (int k = g, it = 0; k < my_blocks; k += C::G, ++it) {
+    // Blocks are numbered head-fastest: the groups running at one time read all heads of the
     // same tokens, i.e. contiguous memory.
     const int bi = static_cast<int>(blockIdx.x) + k * static_cast<int>(gridDim.x);
     const int h = bi % p.H, blk = (bi / p.H) % p.nblk, b = bi / (p.H * p.nblk);
     const int hb = b * p.H + h;
     const int stage = k % NSTAGE;
     const uint32_t st = base_u32 + stage * C::STAGE_BYTES;
-    const bool ok = wait_bounded(bar0 + 8u * stage, (k / NSTAGE) & 1, ctl, 10);
+    const bool ok = wait_block(k);
     int tok0 = blk * QROWS, rows = QROWS;
     if constexpr (VARLEN) {
       const int2 inf = stage_info[stage];
@@ -249,8 +340,8 @@ __global__ void __launch_bounds__(QCfg<D, ROPE>::THREADS, QCfg<D, ROPE>::CTAS_PE
       rows = inf.y;
       if (rows == 0) {
         // nothing at this index: pass the stage on once every thread has read its info
-        if (__syncthreads_or(!ok)) break;
-        if (threadIdx.x == 0 && k + NSTAGE < my_blocks) issue(k + NSTAGE);
+        if (group_bar_or(gbar, C::GTHREADS, !ok)) break;
+        if (leader && k + NSTAGE < my_blocks) issue(k + NSTAGE);
         continue;
       }
     }
@@ -280,12 +371,8 @@ __global__ void __launch_bounds__(QCfg<D, ROPE>::THREADS, QCfg<D, ROPE>::CTAS_PE
       for (int e = 0; e < VPT; ++e) v[e] = 0.f;
     }
 
-    // Every thread has its values in registers; the stage now takes this block's codes.
-    if (__syncthreads_or(!ok)) break;
-
     if (ROPE) {
-      const uint32_t crow = base_u32 + C::OFF_COARSE + (k % C::NCSLOT) * NCOARSE * C::TROW +
-                            (r >> 4) * C::TROW + part * C::SEG_BYTES;
+      const uint32_t crow = st + C::COARSE_OFF + (r >> 4) * C::TROW + part * C::SEG_BYTES;
       const uint32_t frow = base_u32 + C::OFF_FINE + (r & 15) * C::TROW + part * C::SEG_BYTES;
 #pragma unroll
       for (int j = 0; j < VPT / 2; j += 2) {               // two pairs per 16-byte read
@@ -293,15 +380,26 @@ __global__ void __launch_bounds__(QCfg<D, ROPE>::THREADS, QCfg<D, ROPE>::CTAS_PE
         rotary_pair(v[2 * j], v[2 * j + 1], a.x, a.y, f.x, f.y);
         rotary_pair(v[2 * j + 2], v[2 * j + 3], a.z, a.w, f.z, f.w);
       }
-      if (ROTATE) {
+    }
+
+    // This warp has read what it needs of the stage.  The group's last warp to get here refills
+    // the stage with the block NSTAGE blocks on, while this one is transformed; no warp waits.
+    // (A warp whose wait failed does not count: the stage then never refills, later waits run
+    // out, and the group stops together at its next barrier.)
+    if (__all_sync(0xffffffffu, ok)) {
+      if (lane == 0 && atom_add_acq_rel_shared(smem_u32(taken + stage), 1u) % C::GWARPS == C::GWARPS - 1 &&
+          k + NSTAGE < my_blocks)
+        issue(k + NSTAGE);
+    }
+
+    if (ROPE && ROTATE) {
 #pragma unroll
-        for (int j = 0; j < VPT / 2; j += 4) {
-          const uint4 m = reinterpret_cast<const uint4*>(sign_mask)[(part * VPT / 2 + j) / 4];
-          v[2 * j + 1] = __uint_as_float(__float_as_uint(v[2 * j + 1]) ^ m.x);
-          v[2 * j + 3] = __uint_as_float(__float_as_uint(v[2 * j + 3]) ^ m.y);
-          v[2 * j + 5] = __uint_as_float(__float_as_uint(v[2 * j + 5]) ^ m.z);
-          v[2 * j + 7] = __uint_as_float(__float_as_uint(v[2 * j + 7]) ^ m.w);
-        }
+      for (int j = 0; j < VPT / 2; j += 4) {
+        const uint4 m = reinterpret_cast<const uint4*>(sign_mask)[(part * VPT / 2 + j) / 4];
+        v[2 * j + 1] = __uint_as_float(__float_as_uint(v[2 * j + 1]) ^ m.x);
+        v[2 * j + 3] = __uint_as_float(__float_as_uint(v[2 * j + 3]) ^ m.y);
+        v[2 * j + 5] = __uint_as_float(__float_as_uint(v[2 * j + 5]) ^ m.z);
+        v[2 * j + 7] = __uint_as_float(__float_as_uint(v[2 * j + 7]) ^ m.w);
       }
     }
 
@@ -343,21 +441,29 @@ __global__ void __launch_bounds__(QCfg<D, ROPE>::THREADS, QCfg<D, ROPE>::CTAS_PE
     for (int e = 0; e < VPT; e += 2) amax = max3(amax, fabsf(v[e]), fabsf(v[e + 1]));
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-    float* wm = warp_max + C::NWARPS * (k & 1);
-    if (lane == 0) wm[warp] = amax;
-    __syncthreads();
+    float* wm = warp_max + C::GWARPS * (it & 1);
+    if (lane == 0) wm[gwarp] = amax;
+    if (!may_write) {                 // nothing is written to global memory before this
+      grid_dependency_wait();
+      may_write = true;
+    }
+    // the block's one group-wide step: the maximum over its rows (and whether any wait failed)
+    if (group_bar_or(gbar, C::GTHREADS, !ok)) break;
     amax = wm[0];
 #pragma unroll
-    for (int w = 1; w < C::NWARPS; ++w) amax = fmaxf(amax, wm[w]);
+    for (int w = 1; w < C::GWARPS; ++w) amax = fmaxf(amax, wm[w]);
 
     const float inv = amax > 0.f ? 448.f / amax : 0.f;
-    if (threadIdx.x == 0) {
+    if (leader) {
       const float norm = ROTATE ? rsqrtf(static_cast<float>(D)) : 1.f;
       p.scale[static_cast<size_t>(hb) * p.nblk + blk] = amax > 0.f ? (amax * norm) / 448.f : 1.f;
     }
-    // Codes into the stage in the output map's swizzled layout, then one tensor store per
-    // panel: whole 128-byte lines reach L2 instead of 16-byte pieces of 32-byte sectors, and
-    // rows beyond S are clipped by the store.
+    // Codes into the group's buffer in the output map's swizzled layout, then one tensor store
+    // per panel of this warp's rows: whole 128-byte lines reach L2 instead of 16-byte pieces of
+    // 32-byte sectors, and rows beyond S are clipped by the store.  The warp's rows of the
+    // buffer are free once its previous store has read them.
+    if (lane == 0 && n_stores > 0) bulk_wait_read_all();
+    __syncwarp();
     {
       const uint64_t inv2 = f2_pack(inv, inv);
 #pragma unroll
@@ -382,36 +488,36 @@ __global__ void __launch_bounds__(QCfg<D, ROPE>::THREADS, QCfg<D, ROPE>::CTAS_PE
         }
         const int pn = idx / C::CODE_PANEL, cc = (idx % C::CODE_PANEL) / 16;
         const int sw = C::CODE_PANEL == 128 ? (r & 7) : ((r >> 1) & 3);
-        const uint32_t addr = st + pn * (QROWS * C::CODE_PANEL) + r * C::CODE_PANEL + ((cc ^ sw) << 4);
+        const uint32_t addr = outbuf + pn * (QROWS * C::CODE_PANEL) + r * C::CODE_PANEL + ((cc ^ sw) << 4);
         asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(wq[0]), "r"(wq[1]),
                      "r"(wq[2]), "r"(wq[3])
                      : "memory");
       }
     }
-    fence_proxy_async_smem();
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      if (rows == QROWS) {
+    if (!VARLEN || rows == QROWS) {
+      fence_proxy_async_smem();
+      __syncwarp();
+      const int row0 = C::RPW * gwarp;              // this warp's first row of the block
+      if (lane == 0 && tok0 + row0 < p.S) {
 #pragma unroll
         for (int pn = 0; pn < C::NCPANEL; ++pn)
-          tma_store_4d(&tmOut, st + pn * (QROWS * C::CODE_PANEL), pn * C::CODE_PANEL, h, tok0, b);
+          tma_store_4d(&tmOut, outbuf + pn * (QROWS * C::CODE_PANEL) + row0 * C::CODE_PANEL, pn * C::CODE_PANEL,
+                       h, tok0 + row0, b);
         bulk_commit_group();
-        // the stage is free once the store has read it: refill it for block k + NSTAGE
-        bulk_wait_read_all();
+        ++n_stores;
       }
-      if (k + NSTAGE < my_blocks) issue(k + NSTAGE);
     }
   }
-  if (threadIdx.x == 0) bulk_wait_all();
+  if (lane == 0) bulk_wait_all();
+  __syncthreads();
 
   // On an abort, copies still in flight must land before the CTA exits.
   if (threadIdx.x == 0 && *abort_flag) {
     for (int s = 0; s < NSTAGE; ++s) {
-      int last = -1;
-      for (int k = s; k < n_issued; k += NSTAGE) last = k;
-      if (last >= 0) {
+      const int n = issued[s];
+      if (n > 0) {
         const long long t0 = clock64();
-        while (!mbar_try_wait(bar0 + 8u * s, (last / NSTAGE) & 1))
+        while (!mbar_try_wait(bar0 + 8u * s, (n - 1) & 1))
           if (clock64() - t0 > p.spin_limit) break;
       }
     }
@@ -423,9 +529,21 @@ cudaError_t launch_variant(const CUtensorMap& tx, const CUtensorMap& tout, const
                            cudaStream_t stream) {
   using C = QCfg<D, ROPE>;
   const long long nblocks = static_cast<long long>(p.nblk) * p.H * p.B;
-  const long long cap = static_cast<long long>(sm_count) * C::CTAS_PER_SM;
-  const unsigned grid = static_cast<unsigned>(nblocks < cap ? nblocks : cap);
-  hadamard_quant_kernel<D, ROTATE, ROPE, VARLEN><<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(tx, tout, p);
+  // one CTA per SM (a small problem spreads over as many SMs as it has blocks; groups without
+  // a block idle)
+  const unsigned grid = static_cast<unsigned>(nblocks < sm_count ? nblocks : sm_count);
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(C::THREADS);
+  cfg.dynamicSmemBytes = C::SMEM_BYTES;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, hadamard_quant_kernel<D, ROTATE, ROPE, VARLEN>, tx, tout, p);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

@@ -136,7 +136,8 @@ struct QuantParams {
 };
 
 // x is read through `tx`, the same [B, S, H, D] bf16 tensor map the attention kernel uses;
-// codes are written through `tout`, the E4M3 map of the attention kernel's FP8 inputs.
+// codes are written through `tout`, an E4M3 map of the same tensor whose box is one warp's
+// rows (32, or 16 at D = 256).
 template <int D>
 cudaError_t launch_hadamard_quant(const CUtensorMap& tx, const CUtensorMap& tout, const QuantParams& p,
                                   cudaStream_t stream);

@@ -326,6 +326,12 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
 }
 
 // Named barrier `id` (1 .. 15) over `n` threads (a multiple of 32).
+// Programmatic dependent launch: let the next grid on the stream (launched with programmatic
+// stream serialization) start once every CTA of this grid has issued this; and wait until
+// the grid this one depends on has completed and its memory operations are visible.
+__device__ __forceinline__ void grid_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t n) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
 }

@@ -326,6 +326,13 @@ int attn_bwd_noalloc(const void* q, const void* k, const void* v, const void* o,
  *            x' = (x * signs) H_D / sqrt(D), H_D the Sylvester Hadamard
  *            matrix; use the same signs for Q and K.
  *   out[e] = E4M3_round_nearest_even_saturating(x'[e] / scale).
+ *   Overlap: consecutive quantiser launches on one stream (this function, its
+ *   RoPE and packed forms) may run concurrently -- a launch reads its inputs
+ *   and transforms its first blocks while the quantiser launch before it is
+ *   finishing, and writes nothing until that launch has completed.  So the
+ *   input (x, signs, the rotary table, cu_seqlens) of a quantiser call must
+ *   not be an output of the quantiser call just before it on the stream.
+ *   Any other kernel before it completes first, as usual.
  */
 int hadamard_rotate_quant_fp8(const void* x, void* out, float* scale, const float* signs,
                               int B, int H, int S, int D, void* stream);

@@ -25,9 +25,9 @@ input is the sum of the copies' gradients): ``attention_backward_gqa``.
 
 import numpy as np
 
-from .attention import attention_weights, default_scale
+from .attention import attention, attention_weights, default_scale
 
-__all__ = ["attention_backward", "attention_backward_gqa"]
+__all__ = ["attention_backward", "attention_backward_gqa", "attention_backward_rows"]
 
 
 def attention_backward(q, k, v, do, scale=None, causal=False):
@@ -66,3 +66,47 @@ def attention_backward_gqa(q, k, v, do, scale=None, causal=False):
     dq, dk_rep, dv_rep = attention_backward(q, np.repeat(k, G, axis=2), np.repeat(v, G, axis=2), do, scale, causal)
     B, S, _, D = k.shape
     return dq, dk_rep.reshape(B, S, Hkv, G, D).sum(axis=3), dv_rep.reshape(B, S, Hkv, G, D).sum(axis=3)
+
+
+def attention_backward_rows(q, k, v, do, q_rows, k_rows, scale=None, causal=False):
+    """The same gradients on sampled rows only, for sequences too long for an S x S matrix.
+
+    Returns (dQ [B, len(q_rows), H, D], dK and dV [B, len(k_rows), H, D]).  Every entry is the
+    formula above evaluated for one row or one column: O and lse of all query rows first
+    (``attention``, row blocks), then, for query row i, P_i = exp(S_i - lse_i), dP_i = dO_i V^T,
+    dS_i = P_i * (dP_i - Delta_i), dQ_i = scale * dS_i K; and for key j the column
+    P_:j = exp(S_:j - lse), dV_j = P_:j^T dO, dS_:j = P_:j * (dO v_j - Delta),
+    dK_j = scale * dS_:j^T Q."""
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    do = np.asarray(do, dtype=np.float64)
+    B, S, H, D = q.shape
+    if scale is None:
+        scale = default_scale(D)
+    q_rows = np.asarray(q_rows, dtype=np.int64)
+    k_rows = np.asarray(k_rows, dtype=np.int64)
+    O, lse = attention(q, k, v, scale, causal)
+    delta = (do * O).sum(axis=3)                                   # [B, S, H]
+    dq = np.zeros((B, len(q_rows), H, D))
+    dk = np.zeros((B, len(k_rows), H, D))
+    dv = np.zeros((B, len(k_rows), H, D))
+    keys = np.arange(S)
+    for b in range(B):
+        for h in range(H):
+            Q, K, V, G = q[b, :, h], k[b, :, h], v[b, :, h], do[b, :, h]
+            L, dl = lse[b, h], delta[b, :, h]
+            # query rows
+            s = scale * (Q[q_rows] @ K.T)
+            vis = (keys[None, :] <= q_rows[:, None]) if causal else np.ones(s.shape, dtype=bool)
+            P = np.where(vis, np.exp(s - L[q_rows, None]), 0.0)
+            dS = P * (G[q_rows] @ V.T - dl[q_rows, None])
+            dq[b, :, h] = scale * dS @ K
+            # key columns
+            sc = scale * (Q @ K[k_rows].T)                         # [S, n_k]
+            visc = (keys[:, None] >= k_rows[None, :]) if causal else np.ones(sc.shape, dtype=bool)
+            Pc = np.where(visc, np.exp(sc - L[:, None]), 0.0)
+            dv[b, :, h] = Pc.T @ G
+            dSc = Pc * (G @ V[k_rows].T - dl[:, None])
+            dk[b, :, h] = scale * dSc.T @ Q
+    return dq, dk, dv

@@ -61,7 +61,7 @@ def test_benchmark_sizes_d128(S):
 
 
 @pytest.mark.parametrize("D", [64, 128, 256])
-@pytest.mark.parametrize("S", [1024, 4096, 16384])
+@pytest.mark.parametrize("S", [1024, 2048, 4096, 8192, 16384])
 def test_causal_head_dims(S, D):
     run_and_check(16384 // S, S, 2048 // D, D, True, case=3, rows=sample_rows(S))
 

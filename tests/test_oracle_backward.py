@@ -106,3 +106,16 @@ def test_gqa_with_one_group_per_head_is_the_plain_backward():
     b = backward.attention_backward(q, k, v, do, causal=True)
     for x, y in zip(a, b):
         np.testing.assert_array_equal(x, y)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_sampled_rows_equal_the_full_gradients(causal):
+    B, S, H, D = 2, 300, 2, 32
+    rng = np.random.default_rng(31)
+    q, k, v, do = (rng.standard_normal((B, S, H, D)) for _ in range(4))
+    full = backward.attention_backward(q, k, v, do, causal=causal)
+    qr, kr = np.array([0, 1, 127, 128, 299]), np.array([0, 5, 150, 298, 299])
+    dq, dk, dv = backward.attention_backward_rows(q, k, v, do, qr, kr, causal=causal)
+    np.testing.assert_allclose(dq, full[0][:, qr], rtol=1e-11, atol=1e-12)
+    np.testing.assert_allclose(dk, full[1][:, kr], rtol=1e-11, atol=1e-12)
+    np.testing.assert_allclose(dv, full[2][:, kr], rtol=1e-11, atol=1e-12)

@@ -42,3 +42,28 @@ def test_two_calls_in_a_row_match_attn_bwd(first, second):
         ops.check()
         for name, got, want in zip(("dq", "dk", "dv"), (dq, dk, dv), ref):
             assert torch.equal(got, want), name
+
+
+def test_the_largest_problem_that_fits():
+    # B * H * (S rounded up to 128) = 8 * 16 * 16384 = 2,097,152 rows: exactly the 16 MiB the
+    # built-in scratch holds; the last padded rows land on its last bytes
+    lib = _lib.load()
+    B, S, H, D, causal = 8, 16384, 16, 64, False
+    assert lib.attn_bwd_workspace_bytes(B, H, S) == 16 * 1024 * 1024
+    dev = torch.device("cuda")
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    q, k, v = (t.to(dev) for t in synth.make_qkv(B, S, H, D, 62))
+    do = torch.from_numpy(synth.normal((B, S, H, D), synth.seed_for(62, synth.STREAM_OUT_VAL))).to(torch.bfloat16).to(dev)
+    o, lse = ops.attn_fwd(q, k, v, causal=causal)
+    ref = ops.attn_bwd(q, k, v, o, lse, do, causal=causal)
+    ops.check()
+    dq, dk, dv = (torch.full_like(q, float("nan")) for _ in range(3))
+    rc = lib.attn_bwd_noalloc(_p(q), _p(k), _p(v), _p(o), _p(do), _p(lse), _p(dq), _p(dk), _p(dv),
+                              B, H, S, D, int(causal), 0.0, stream)
+    assert rc == 0, lib.attn_get_last_error()
+    ops.check()
+    for name, got, want in zip(("dq", "dk", "dv"), (dq, dk, dv), ref):
+        assert torch.equal(got, want), name
+    # one more 128-row block does not fit, and is refused before anything runs
+    assert lib.attn_bwd_noalloc(_p(q), _p(k), _p(v), _p(o), _p(do), _p(lse), _p(dq), _p(dk), _p(dv),
+                                B, H, S + 1, D, int(causal), 0.0, stream) == 1
