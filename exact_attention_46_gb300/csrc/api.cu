@@ -88,7 +88,27 @@ CUtensorMapL2promotion l2_promotion(int row_bytes) {
                           : (row_bytes >= 128 ? CU_TENSOR_MAP_L2_PROMOTION_L2_128B : CU_TENSOR_MAP_L2_PROMOTION_L2_64B);
 }
 
-int make_qkv_map(CUtensorMap* m, const void* ptr, int B, int S, int H, int D, bool fp8, int box_rows = 128) {
+int make_qkv_map(CUtensorMap* m, const void* ptr, int B, int S, int H, int D, bool fp8, int box_rows = 128);
+
+// O [B, S, H, D] bf16 for the forward's epilogue: a box of 32 columns x 32 rows (one softmax
+// warp's rows, one 32-column chunk), 64-byte swizzle.
+int make_o_map(CUtensorMap* m, const void* ptr, int B, int S, int H, int D) {
+  EncodeTiledFn enc = encode_fn();
+  if (enc == nullptr) return fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled entry point unavailable");
+  const cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H),
+                              static_cast<cuuint64_t>(S), static_cast<cuuint64_t>(B)};
+  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(H) * D * 2,
+                                 static_cast<cuuint64_t>(S) * H * D * 2};
+  const cuuint32_t box[4] = {32, 1, 32, 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptr), dims, strides, box, estr,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled failed for O (%d)", int(r));
+  return ATTN_OK;
+}
+
+int make_qkv_map(CUtensorMap* m, const void* ptr, int B, int S, int H, int D, bool fp8, int box_rows) {
   EncodeTiledFn enc = encode_fn();
   if (enc == nullptr) return fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled entry point unavailable");
   const int esz = fp8 ? 1 : 2;
@@ -248,16 +268,16 @@ int check_attn_args(const void* q, const void* k, const void* v, const void* o, 
 }
 
 template <bool FP8>
-int dispatch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+int dispatch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& to,
              const AttnParams& p, int D, int causal, cudaStream_t st, const SplitParams* sp) {
   cudaError_t e = cudaErrorInvalidValue;
   switch (D * 2 + causal) {
-    case 64 * 2 + 0: e = launch_attn<64, FP8, false>(tq, tk, tv, p, st, sp); break;
-    case 64 * 2 + 1: e = launch_attn<64, FP8, true>(tq, tk, tv, p, st, nullptr); break;
-    case 128 * 2 + 0: e = launch_attn<128, FP8, false>(tq, tk, tv, p, st, sp); break;
-    case 128 * 2 + 1: e = launch_attn<128, FP8, true>(tq, tk, tv, p, st, nullptr); break;
-    case 256 * 2 + 0: e = launch_attn<256, FP8, false>(tq, tk, tv, p, st, sp); break;
-    case 256 * 2 + 1: e = launch_attn<256, FP8, true>(tq, tk, tv, p, st, nullptr); break;
+    case 64 * 2 + 0: e = launch_attn<64, FP8, false>(tq, tk, tv, to, p, st, sp); break;
+    case 64 * 2 + 1: e = launch_attn<64, FP8, true>(tq, tk, tv, to, p, st, nullptr); break;
+    case 128 * 2 + 0: e = launch_attn<128, FP8, false>(tq, tk, tv, to, p, st, sp); break;
+    case 128 * 2 + 1: e = launch_attn<128, FP8, true>(tq, tk, tv, to, p, st, nullptr); break;
+    case 256 * 2 + 0: e = launch_attn<256, FP8, false>(tq, tk, tv, to, p, st, sp); break;
+    case 256 * 2 + 1: e = launch_attn<256, FP8, true>(tq, tk, tv, to, p, st, nullptr); break;
     default: break;
   }
   if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "attention launch failed: %s", cudaGetErrorString(e));
@@ -275,6 +295,8 @@ int run_attn(const void* q, const void* k, const void* v, const float* qs, const
   if ((rc = make_qkv_map(&tq, q, B, S, H, D, fp8)) != ATTN_OK) return rc;
   if ((rc = make_qkv_map(&tk, k, B, S, H, D, fp8)) != ATTN_OK) return rc;
   if ((rc = make_qkv_map(&tv, v, B, S, H, D, fp8)) != ATTN_OK) return rc;
+  CUtensorMap to;
+  if ((rc = make_o_map(&to, o, B, S, H, D)) != ATTN_OK) return rc;
   AttnParams p{};
   p.B = B;
   p.H = H;
@@ -294,16 +316,17 @@ int run_attn(const void* q, const void* k, const void* v, const float* qs, const
   p.err_info = err + 1;
   p.kv_group = 1;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  return fp8 ? dispatch<true>(tq, tk, tv, p, D, causal, st, nullptr)
-             : dispatch<false>(tq, tk, tv, p, D, causal, st, nullptr);
+  return fp8 ? dispatch<true>(tq, tk, tv, to, p, D, causal, st, nullptr)
+             : dispatch<false>(tq, tk, tv, to, p, D, causal, st, nullptr);
 }
 
 template <bool FP8, bool CAUSAL>
 cudaError_t launch_varlen(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                           const AttnParams& p, int D, cudaStream_t st) {
-  return D == 64    ? launch_attn<64, FP8, CAUSAL, true>(tq, tk, tv, p, st, nullptr)
-         : D == 128 ? launch_attn<128, FP8, CAUSAL, true>(tq, tk, tv, p, st, nullptr)
-                    : launch_attn<256, FP8, CAUSAL, true>(tq, tk, tv, p, st, nullptr);
+  // the packed-batch kernels store O from registers: the O map is not read
+  return D == 64    ? launch_attn<64, FP8, CAUSAL, true>(tq, tk, tv, tq, p, st, nullptr)
+         : D == 128 ? launch_attn<128, FP8, CAUSAL, true>(tq, tk, tv, tq, p, st, nullptr)
+                    : launch_attn<256, FP8, CAUSAL, true>(tq, tk, tv, tq, p, st, nullptr);
 }
 
 // Scale entries per head of a packed batch's block scales.
@@ -520,6 +543,8 @@ int run_gqa(const void* q, const void* k, const void* v, const float* qs, const 
   if ((rc = make_qkv_map(&tq, q, B, S, Hq, D, fp8)) != ATTN_OK) return rc;
   if ((rc = make_qkv_map(&tk, k, B, S, Hkv, D, fp8)) != ATTN_OK) return rc;
   if ((rc = make_qkv_map(&tv, v, B, S, Hkv, D, fp8)) != ATTN_OK) return rc;
+  CUtensorMap to;
+  if ((rc = make_o_map(&to, o, B, S, Hq, D)) != ATTN_OK) return rc;
   AttnParams p{};
   p.B = B;
   p.H = Hq;
@@ -542,8 +567,8 @@ int run_gqa(const void* q, const void* k, const void* v, const float* qs, const 
   SplitParams sp{};
   bool split = false;
   if ((rc = key_split_params(p, D, causal, ws, ws_bytes, &sp, &split)) != ATTN_OK) return rc;
-  return fp8 ? dispatch<true>(tq, tk, tv, p, D, causal, st, split ? &sp : nullptr)
-             : dispatch<false>(tq, tk, tv, p, D, causal, st, split ? &sp : nullptr);
+  return fp8 ? dispatch<true>(tq, tk, tv, to, p, D, causal, st, split ? &sp : nullptr)
+             : dispatch<false>(tq, tk, tv, to, p, D, causal, st, split ? &sp : nullptr);
 }
 
 }  // namespace

@@ -101,6 +101,10 @@ struct AttnCfg {
   static constexpr int SMEM_BYTES =
       (SMEM_BYTES_RAW > 120 * 1024 ? SMEM_BYTES_RAW : 120 * 1024) + 1024;
   static constexpr int NUM_SOFTMAX_WARPS = 4 * NT;
+  // O leaves through shared memory: per softmax warp two 2 KB buffers, each 32 rows x 32
+  // columns of bf16 (64-byte swizzle), stored to O by one tensor store per 32-column chunk
+  static constexpr int OST_WARP_BYTES = 2 * 32 * 64;
+  static constexpr int OST_BYTES = NUM_SOFTMAX_WARPS * OST_WARP_BYTES;
   static constexpr int LOAD_WARP = NUM_SOFTMAX_WARPS;
   static constexpr int MMA_WARP = NUM_SOFTMAX_WARPS + 1;
   static constexpr int THREADS = 32 * (NUM_SOFTMAX_WARPS + 2);
@@ -243,7 +247,8 @@ constexpr int VARLEN_SMEM_BYTES = ((VARLEN_MAX_SEQ + 1) + 2 * (VARLEN_MAX_LEVELS
 template <int D, bool FP8, bool CAUSAL, bool VARLEN, bool SPLIT>
 __global__ void __launch_bounds__(AttnCfg<D, FP8>::THREADS, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                    const __grid_constant__ CUtensorMap tmV, const AttnParams p, const SplitParams sp) {
+                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+                    const AttnParams p, const SplitParams sp) {
   using C = AttnCfg<D, FP8>;
   constexpr int NT = C::NT;
   constexpr int NSLOT = C::NSLOT;
@@ -253,9 +258,13 @@ __global__ void __launch_bounds__(AttnCfg<D, FP8>::THREADS, 1)
   const uint32_t raw_u32 = smem_u32(smem_raw);
   const uint32_t base_u32 = (raw_u32 + 1023u) & ~1023u;
   uint8_t* base = smem_raw + (base_u32 - raw_u32);
+  // Fixed-length launches stage O in shared memory for tensor stores; packed batches store rows
+  // from registers (a tensor store of a partial tile would write the next sequence's rows).
+  constexpr bool STAGE_O = !VARLEN;
   const uint32_t sQ = base_u32;                                  // NT tiles
   const uint32_t sKV = base_u32 + NT * C::TILE_BYTES;            // NSLOT tiles
-  const uint32_t bar0 = sKV + NSLOT * C::TILE_BYTES;             // barriers (8 B each)
+  const uint32_t sOst = sKV + NSLOT * C::TILE_BYTES;             // STAGE_O: O staging
+  const uint32_t bar0 = sOst + (STAGE_O ? C::OST_BYTES : 0);     // barriers (8 B each)
   uint8_t* bar_ptr = base + (bar0 - base_u32);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_ptr + C::NBAR * 8);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -386,6 +395,7 @@ __global__ void __launch_bounds__(AttnCfg<D, FP8>::THREADS, 1)
     prefetch_tmap(&tmQ);
     prefetch_tmap(&tmK);
     prefetch_tmap(&tmV);
+    if (STAGE_O) prefetch_tmap(&tmO);
   }
   tc_fence_before();
   __syncthreads();
@@ -866,6 +876,9 @@ __global__ void __launch_bounds__(AttnCfg<D, FP8>::THREADS, 1)
           continue;
         }
       }
+      // this warp's 32 rows of the tile: the first one, and its staging buffers
+      const int row0 = it.q0 + 128 * t + 32 * wq;
+      const uint32_t ost = sOst + static_cast<uint32_t>(warp) * C::OST_WARP_BYTES;
 #pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {
         uint32_t o[32];
@@ -878,7 +891,27 @@ __global__ void __launch_bounds__(AttnCfg<D, FP8>::THREADS, 1)
           reg_fence(o[2 * i + 1]);
           pk[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
         }
-        if (valid) {
+        if constexpr (STAGE_O) {
+          // buffer c & 1 is free once at most one store (chunk c - 1's) still reads its buffer
+          if (lane == 0 && c >= 2) bulk_wait_read_1();
+          __syncwarp();
+          const uint32_t buf = ost + (c & 1) * (32 * 64);
+#pragma unroll
+          for (int v4 = 0; v4 < 4; ++v4) {
+            // row = lane (64 bytes), 16-byte chunk v4, 64-byte swizzle: chunk ^ ((row >> 1) & 3)
+            const uint32_t addr = buf + lane * 64 + ((v4 ^ ((lane >> 1) & 3)) << 4);
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(pk[4 * v4]),
+                         "r"(pk[4 * v4 + 1]), "r"(pk[4 * v4 + 2]), "r"(pk[4 * v4 + 3])
+                         : "memory");
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          // rows beyond S are clipped by the store; a warp whose rows all lie beyond S stores none
+          if (lane == 0 && row0 < seq_len(it)) {
+            tma_store_4d(&tmO, buf, 32 * c, it.h, row0, it.b);
+            bulk_commit_group();
+          }
+        } else if (valid) {
           uint4* dst = reinterpret_cast<uint4*>(orow + 32 * c);
 #pragma unroll
           for (int v4 = 0; v4 < 4; ++v4)
@@ -893,6 +926,9 @@ __global__ void __launch_bounds__(AttnCfg<D, FP8>::THREADS, 1)
     }
   }
 
+  // the epilogue's tensor stores have read their staging buffers (and written O) before the
+  // CTA's shared memory goes away
+  if (STAGE_O && warp < C::NUM_SOFTMAX_WARPS && lane == 0) bulk_wait_all();
   __syncwarp();
   tc_fence_before();
   __syncthreads();
@@ -904,9 +940,10 @@ __global__ void __launch_bounds__(AttnCfg<D, FP8>::THREADS, 1)
 
 template <int D, bool FP8, bool CAUSAL, bool VARLEN>
 cudaError_t launch_attn(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                        const AttnParams& p, cudaStream_t stream, const SplitParams* split_plan) {
+                        const CUtensorMap& to, const AttnParams& p, cudaStream_t stream,
+                        const SplitParams* split_plan) {
   using C = AttnCfg<D, FP8>;
-  constexpr int SMEM = C::SMEM_BYTES + (VARLEN ? VARLEN_SMEM_BYTES : 0);
+  constexpr int SMEM = C::SMEM_BYTES + (VARLEN ? VARLEN_SMEM_BYTES : C::OST_BYTES);
   static_assert(SMEM <= 227 * 1024, "shared memory budget");
   constexpr bool CAN_SPLIT = !CAUSAL && !VARLEN;
   const bool split = CAN_SPLIT && split_plan != nullptr && split_plan->n_parts > 1;
@@ -942,7 +979,7 @@ cudaError_t launch_attn(const CUtensorMap& tq, const CUtensorMap& tk, const CUte
   if constexpr (CAN_SPLIT) {
     if (split) {
       attn_fwd_kernel<D, FP8, CAUSAL, VARLEN, true>
-          <<<static_cast<unsigned>(grid), C::THREADS, SMEM, stream>>>(tq, tk, tv, p, sp);
+          <<<static_cast<unsigned>(grid), C::THREADS, SMEM, stream>>>(tq, tk, tv, to, p, sp);
       if ((e = cudaGetLastError()) != cudaSuccess) return e;
       const long long warps = static_cast<long long>(sp.n_tail) * 128 * C::NT;
       split_merge_kernel<D, C::NT><<<static_cast<unsigned>((warps + 7) / 8), 256, 0, stream>>>(p, sp);
@@ -950,7 +987,7 @@ cudaError_t launch_attn(const CUtensorMap& tq, const CUtensorMap& tk, const CUte
     }
   }
   attn_fwd_kernel<D, FP8, CAUSAL, VARLEN, false>
-      <<<static_cast<unsigned>(grid), C::THREADS, SMEM, stream>>>(tq, tk, tv, p, sp);
+      <<<static_cast<unsigned>(grid), C::THREADS, SMEM, stream>>>(tq, tk, tv, to, p, sp);
   return cudaGetLastError();
 }
 

@@ -6,7 +6,7 @@
 namespace ea46 {
 #define EA46_INST(D, CAUSAL)                                                                        \
   template cudaError_t launch_attn<D, false, CAUSAL, true>(const CUtensorMap&, const CUtensorMap&, \
-                                                           const CUtensorMap&, const AttnParams&,  \
+                                                           const CUtensorMap&, const CUtensorMap&, const AttnParams&,  \
                                                            cudaStream_t, const SplitParams*);
 EA46_INST(64, false)
 EA46_INST(64, true)

@@ -61,7 +61,7 @@ constexpr int QROWS = 128;            // tokens per scale block
 constexpr int NCOARSE = 8;            // rotary rows 128 blk + 16 r1 per block
 constexpr int NFINE = 16;             // rotary rows r0 = 0..15, resident
 
-template <int D, bool ROPE>
+template <int D, bool ROPE, bool ROTATE = true, bool VARLEN = false>
 struct QCfg {
   static constexpr int VPT = D < 128 ? D : 128;                            // values per thread
   static constexpr int TPR = D / VPT;                                      // threads per row
@@ -70,7 +70,9 @@ struct QCfg {
   static constexpr int GWARPS = GTHREADS / 32;
   // groups per CTA (one CTA per SM): as many 128-row blocks in registers at once as the
   // register file holds
-  static constexpr int G = D == 64 ? 4 : (D == 128 ? (ROPE ? 2 : 3) : 1);
+  // (three groups of the rotary forms at D = 128 fit 170 registers only for the rotated,
+  // fixed-length one; the others keep two)
+  static constexpr int G = D == 64 ? 4 : (D == 128 ? (ROPE && (!ROTATE || VARLEN) ? 2 : 3) : 1);
   static constexpr int THREADS = G * GTHREADS;
   static constexpr int ROW_BYTES = D * 2;                                  // bf16 row
   static constexpr int PANEL_BYTES = 128 * 128;                            // 128 rows x 128 B
@@ -162,10 +164,10 @@ __device__ __forceinline__ bool group_bar_or(uint32_t id, uint32_t n, bool v) {
 }
 
 template <int D, bool ROTATE, bool ROPE, bool VARLEN>
-__global__ void __launch_bounds__(QCfg<D, ROPE>::THREADS, 1)
+__global__ void __launch_bounds__(QCfg<D, ROPE, ROTATE, VARLEN>::THREADS, 1)
     hadamard_quant_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmOut,
                           const QuantParams p) {
-  using C = QCfg<D, ROPE>;
+  using C = QCfg<D, ROPE, ROTATE, VARLEN>;
   constexpr int VPT = C::VPT;
   constexpr int NSTAGE = C::NSTAGE;
   constexpr int NW = VPT / 8;         // 16-byte input chunks per thread
@@ -527,7 +529,7 @@ __global__ void __launch_bounds__(QCfg<D, ROPE>::THREADS, 1)
 template <int D, bool ROTATE, bool ROPE, bool VARLEN = false>
 cudaError_t launch_variant(const CUtensorMap& tx, const CUtensorMap& tout, const QuantParams& p, int sm_count,
                            cudaStream_t stream) {
-  using C = QCfg<D, ROPE>;
+  using C = QCfg<D, ROPE, ROTATE, VARLEN>;
   const long long nblocks = static_cast<long long>(p.nblk) * p.H * p.B;
   // one CTA per SM (a small problem spreads over as many SMs as it has blocks; groups without
   // a block idle)
@@ -550,7 +552,7 @@ cudaError_t launch_variant(const CUtensorMap& tx, const CUtensorMap& tout, const
 template <int D, bool ROTATE, bool ROPE, bool VARLEN = false>
 cudaError_t set_smem() {
   return cudaFuncSetAttribute(hadamard_quant_kernel<D, ROTATE, ROPE, VARLEN>,
-                              cudaFuncAttributeMaxDynamicSharedMemorySize, QCfg<D, ROPE>::SMEM_BYTES);
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, QCfg<D, ROPE, ROTATE, VARLEN>::SMEM_BYTES);
 }
 
 }  // namespace

@@ -56,10 +56,13 @@ constexpr int VARLEN_MAX_SEQ = 4096;
 constexpr int VARLEN_MAX_LEVELS = 1024;
 
 // Launch one attention forward.  Returns the cudaError_t of the launch.
-// `split` (fixed length, not causal; may be null) plans a key-split tail.
+// `to` is O's bf16 map with a box of 32 columns x 32 rows and a 64-byte swizzle (the epilogue's
+// tensor stores; unused by the packed-batch kernels).  `split` (fixed length, not causal; may be
+// null) plans a key-split tail.
 template <int D, bool FP8, bool CAUSAL, bool VARLEN = false>
 cudaError_t launch_attn(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                        const AttnParams& p, cudaStream_t stream, const SplitParams* split);
+                        const CUtensorMap& to, const AttnParams& p, cudaStream_t stream,
+                        const SplitParams* split);
 
 // Query-tile count per CTA (two Q tiles share K/V loads; one at D = 256 where
 // two tiles' S and O would not fit the 512 Tensor-Memory columns).
