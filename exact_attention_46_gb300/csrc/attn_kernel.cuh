@@ -95,16 +95,24 @@ struct AttnCfg {
   static constexpr int SMEM_TILES_BUDGET = 200 * 1024;
   static constexpr int NSLOT_RAW = (SMEM_TILES_BUDGET - NT * TILE_BYTES) / TILE_BYTES;
   static constexpr int NSLOT = NSLOT_RAW > 8 ? 8 : NSLOT_RAW;
-  static constexpr int NBAR = 2 + 2 * NSLOT + 5 * NT + 1;
-  static constexpr int SMEM_BYTES_RAW = (NT + NSLOT) * TILE_BYTES + NBAR * 8 + 16;
-  // Request at least ~120 KB so that one CTA (and its 512 TMEM columns) owns the SM.
-  static constexpr int SMEM_BYTES =
-      (SMEM_BYTES_RAW > 120 * 1024 ? SMEM_BYTES_RAW : 120 * 1024) + 1024;
+  static constexpr int NBAR = 2 + 2 * NSLOT + 5 * NT + 1 + 2;   // the last pair: second Q buffer
   static constexpr int NUM_SOFTMAX_WARPS = 4 * NT;
   // O leaves through shared memory: per softmax warp two 2 KB buffers, each 32 rows x 32
   // columns of bf16 (64-byte swizzle), stored to O by one tensor store per 32-column chunk
   static constexpr int OST_WARP_BYTES = 2 * 32 * 64;
   static constexpr int OST_BYTES = NUM_SOFTMAX_WARPS * OST_WARP_BYTES;
+  // what the launch adds after the tiles and barriers: O staging, or the packed-batch tables
+  static constexpr int VARLEN_TABLE_BYTES =
+      ((VARLEN_MAX_SEQ + 1) + 2 * (VARLEN_MAX_LEVELS + 1) + 4) * 4 + VARLEN_MAX_SEQ * 2;
+  static constexpr int EXTRA_MAX = OST_BYTES > VARLEN_TABLE_BYTES ? OST_BYTES : VARLEN_TABLE_BYTES;
+  // Q tiles double-buffered where shared memory has room, so the next item's Q loads while this
+  // item runs instead of after its last QK^T (at D = 128 bf16 and D = 256 it has none)
+  static constexpr int QBUF =
+      (2 * NT + NSLOT) * TILE_BYTES + NBAR * 8 + 16 + 1024 + EXTRA_MAX <= 227 * 1024 ? 2 : 1;
+  static constexpr int SMEM_BYTES_RAW = (QBUF * NT + NSLOT) * TILE_BYTES + NBAR * 8 + 16;
+  // Request at least ~120 KB so that one CTA (and its 512 TMEM columns) owns the SM.
+  static constexpr int SMEM_BYTES =
+      (SMEM_BYTES_RAW > 120 * 1024 ? SMEM_BYTES_RAW : 120 * 1024) + 1024;
   static constexpr int LOAD_WARP = NUM_SOFTMAX_WARPS;
   static constexpr int MMA_WARP = NUM_SOFTMAX_WARPS + 1;
   static constexpr int THREADS = 32 * (NUM_SOFTMAX_WARPS + 2);
@@ -261,8 +269,8 @@ __global__ void __launch_bounds__(AttnCfg<D, FP8>::THREADS, 1)
   // Fixed-length launches stage O in shared memory for tensor stores; packed batches store rows
   // from registers (a tensor store of a partial tile would write the next sequence's rows).
   constexpr bool STAGE_O = !VARLEN;
-  const uint32_t sQ = base_u32;                                  // NT tiles
-  const uint32_t sKV = base_u32 + NT * C::TILE_BYTES;            // NSLOT tiles
+  const uint32_t sQ = base_u32;                                  // QBUF x NT tiles
+  const uint32_t sKV = base_u32 + C::QBUF * NT * C::TILE_BYTES;  // NSLOT tiles
   const uint32_t sOst = sKV + NSLOT * C::TILE_BYTES;             // STAGE_O: O staging
   const uint32_t bar0 = sOst + (STAGE_O ? C::OST_BYTES : 0);     // barriers (8 B each)
   uint8_t* bar_ptr = base + (bar0 - base_u32);
@@ -275,8 +283,9 @@ __global__ void __launch_bounds__(AttnCfg<D, FP8>::THREADS, 1)
   int* s_nitems = s_off + VARLEN_MAX_LEVELS + 1;
   int16_t* s_perm = reinterpret_cast<int16_t*>(s_nitems + 4);
 
-  auto BAR_Q_FULL = [&]() { return bar0; };
-  auto BAR_Q_EMPTY = [&]() { return bar0 + 8u; };
+  // Q buffer qb: the first pair of barriers, or the pair after everything else
+  auto BAR_Q_FULL = [&](int qb) { return qb == 0 ? bar0 : bar0 + 8u * (2 + 2 * NSLOT + 5 * NT + 1); };
+  auto BAR_Q_EMPTY = [&](int qb) { return qb == 0 ? bar0 + 8u : bar0 + 8u * (2 + 2 * NSLOT + 5 * NT + 2); };
   auto BAR_KV_FULL = [&](int s) { return bar0 + 8u * (2 + s); };
   auto BAR_KV_EMPTY = [&](int s) { return bar0 + 8u * (2 + NSLOT + s); };
   auto BAR_S_FULL = [&](int t) { return bar0 + 8u * (2 + 2 * NSLOT + t); };
@@ -291,8 +300,10 @@ __global__ void __launch_bounds__(AttnCfg<D, FP8>::THREADS, 1)
   const uint32_t lane = lane_id();
 
   if (threadIdx.x == 0) {
-    mbar_init(BAR_Q_FULL(), 1);
-    mbar_init(BAR_Q_EMPTY(), 1);
+    for (int qb = 0; qb < 2; ++qb) {
+      mbar_init(BAR_Q_FULL(qb), 1);
+      mbar_init(BAR_Q_EMPTY(qb), 1);
+    }
     for (int s = 0; s < NSLOT; ++s) {
       mbar_init(BAR_KV_FULL(s), 1);
       mbar_init(BAR_KV_EMPTY(s), 1);
@@ -513,18 +524,20 @@ __global__ void __launch_bounds__(AttnCfg<D, FP8>::THREADS, 1)
         Item it;
         decode(item, it);
         const int kvh = it.h / p.kv_group;     // grouped-query attention: the shared K/V head
-        // The Q buffer is released by the MMA warp after the previous item's last S MMA.
-        if (!wait_bounded(BAR_Q_EMPTY(), (q_issued & 1) ^ 1u, ctl, WHERE_LOAD)) break;
+        // Q buffer qb is released by the MMA warp after the last S MMA of the item that used it
+        // (QBUF items ago).
+        const int qb = q_issued % C::QBUF;
+        if (!wait_bounded(BAR_Q_EMPTY(qb), ((q_issued / C::QBUF) & 1) ^ 1u, ctl, WHERE_LOAD)) break;
         uint32_t qbytes = 0;
 #pragma unroll
         for (int t = 0; t < NT; ++t) qbytes += it.n[t] > 0 ? C::TILE_BYTES : 0;
-        mbar_arrive_expect_tx(BAR_Q_FULL(), qbytes);
+        mbar_arrive_expect_tx(BAR_Q_FULL(qb), qbytes);
 #pragma unroll
         for (int t = 0; t < NT; ++t) {
           if (it.n[t] == 0) continue;
 #pragma unroll
           for (int pn = 0; pn < C::NPANEL; ++pn)
-            tma_load_4d(sQ + t * C::TILE_BYTES + pn * C::PANEL_BYTES, &tmQ, BAR_Q_FULL(),
+            tma_load_4d(sQ + (qb * NT + t) * C::TILE_BYTES + pn * C::PANEL_BYTES, &tmQ, BAR_Q_FULL(qb),
                         pn * C::PANEL_ELEMS, it.h, tma_row(it, it.q0 + 128 * t), it.b, pol_q);
         }
         ++q_issued;
@@ -545,7 +558,8 @@ __global__ void __launch_bounds__(AttnCfg<D, FP8>::THREADS, 1)
       }
       if (*abort_flag) {
         // Drain: every copy still in flight must land before the CTA may exit.
-        if (q_issued > 0) wait_drain(BAR_Q_FULL(), (q_issued - 1) & 1, p.spin_limit);
+        for (int i = q_issued > C::QBUF ? q_issued - C::QBUF : 0; i < q_issued; ++i)
+          wait_drain(BAR_Q_FULL(i % C::QBUF), (i / C::QBUF) & 1, p.spin_limit);
         const int first = issued > NSLOT ? issued - NSLOT : 0;
         for (int i = first; i < issued; ++i)
           wait_drain(BAR_KV_FULL(i % NSLOT), (i / NSLOT) & 1, p.spin_limit);
@@ -559,9 +573,10 @@ __global__ void __launch_bounds__(AttnCfg<D, FP8>::THREADS, 1)
       const uint64_t dq0 = smem_desc(sQ, 16, C::SBO, C::LAYOUT);
       const uint64_t dkv0 = smem_desc(sKV, 16, C::SBO, C::LAYOUT);
       const uint64_t dv0 = smem_desc(sKV, C::PANEL_BYTES, C::SBO, C::LAYOUT);
+      int qsel = 0;              // the Q buffer of the current item
       auto gemm_qk = [&](int t, int slot) {
         const uint32_t d = tmem + 128u * t;
-        const uint64_t a0 = dq0 + ((t * C::TILE_BYTES) >> 4);
+        const uint64_t a0 = dq0 + (((qsel * NT + t) * C::TILE_BYTES) >> 4);
         const uint64_t b0 = dkv0 + ((slot * C::TILE_BYTES) >> 4);
 #pragma unroll
         for (int kk = 0; kk < C::KSTEPS_QK; ++kk) {
@@ -593,7 +608,8 @@ __global__ void __launch_bounds__(AttnCfg<D, FP8>::THREADS, 1)
         if (item >= n_items) break;
         Item it;
         decode(item, it);
-        ok = wait_bounded(BAR_Q_FULL(), n & 1, ctl, WHERE_MMA);
+        qsel = n % C::QBUF;
+        ok = wait_bounded(BAR_Q_FULL(qsel), (n / C::QBUF) & 1, ctl, WHERE_MMA);
         if (!ok) break;
         {
           const int ks = consumed % NSLOT;
@@ -608,7 +624,7 @@ __global__ void __launch_bounds__(AttnCfg<D, FP8>::THREADS, 1)
               mma_commit(BAR_S_FULL(t));
             }
           }
-          if (it.nmax == 1) mma_commit(BAR_Q_EMPTY());
+          if (it.nmax == 1) mma_commit(BAR_Q_EMPTY(qsel));
           mma_commit(BAR_KV_EMPTY(ks));
         }
         for (int j = 1; ok && j <= it.nmax; ++j) {
@@ -652,7 +668,7 @@ __global__ void __launch_bounds__(AttnCfg<D, FP8>::THREADS, 1)
             }
           }
           if (ok && ks >= 0) {
-            if (j == it.nmax - 1) mma_commit(BAR_Q_EMPTY());
+            if (j == it.nmax - 1) mma_commit(BAR_Q_EMPTY(qsel));
             mma_commit(BAR_KV_EMPTY(ks));
           }
         }
