@@ -92,10 +92,18 @@ struct AttnCfg {
   static constexpr int TILE_BYTES = 128 * ROW_BYTES;
   static constexpr uint32_t LAYOUT = PANEL_ROW == 128 ? 2u : 4u;   // SW128 / SW64
   static constexpr uint32_t SBO = 8 * PANEL_ROW;               // stride of 8-row groups
+  // E4M3 numerators with two query tiles go through shared memory (one 128 x 128-byte tile per
+  // query tile, K-major, 128-byte swizzle) instead of over S in Tensor Memory, so the next
+  // QK^T may overwrite S as soon as the softmax warps have read it
+  static constexpr bool P_SMEM = FP8 && NT == 2;
+  static constexpr int P_BYTES = P_SMEM ? NT * 128 * 128 : 0;
   static constexpr int SMEM_TILES_BUDGET = 200 * 1024;
-  static constexpr int NSLOT_RAW = (SMEM_TILES_BUDGET - NT * TILE_BYTES) / TILE_BYTES;
-  static constexpr int NSLOT = NSLOT_RAW > 8 ? 8 : NSLOT_RAW;
-  static constexpr int NBAR = 2 + 2 * NSLOT + 5 * NT + 1 + 2;   // the last pair: second Q buffer
+  static constexpr int NSLOT_RAW = (SMEM_TILES_BUDGET - NT * TILE_BYTES - P_BYTES) / TILE_BYTES;
+  static constexpr int NSLOT_CAP = P_SMEM ? 6 : 8;
+  static constexpr int NSLOT = NSLOT_RAW > NSLOT_CAP ? NSLOT_CAP : NSLOT_RAW;
+  // K/V ring pairs, per tile S/P/O barriers, the second Q buffer's pair, and (P_SMEM) the
+  // S-read and PV-done barrier of each tile
+  static constexpr int NBAR = 2 + 2 * NSLOT + 5 * NT + 1 + 2 + 2 * NT;
   static constexpr int NUM_SOFTMAX_WARPS = 4 * NT;
   // O leaves through shared memory: per softmax warp two 2 KB buffers, each 32 rows x 32
   // columns of bf16 (64-byte swizzle), stored to O by one tensor store per 32-column chunk
@@ -108,14 +116,18 @@ struct AttnCfg {
   // Q tiles double-buffered where shared memory has room, so the next item's Q loads while this
   // item runs instead of after its last QK^T (at D = 128 bf16 and D = 256 it has none)
   static constexpr int QBUF =
-      (2 * NT + NSLOT) * TILE_BYTES + NBAR * 8 + 16 + 1024 + EXTRA_MAX <= 227 * 1024 ? 2 : 1;
-  static constexpr int SMEM_BYTES_RAW = (QBUF * NT + NSLOT) * TILE_BYTES + NBAR * 8 + 16;
+      (2 * NT + NSLOT) * TILE_BYTES + P_BYTES + NBAR * 8 + 16 + 1024 + EXTRA_MAX <= 227 * 1024 ? 2 : 1;
+  static constexpr int SMEM_BYTES_RAW = (QBUF * NT + NSLOT) * TILE_BYTES + P_BYTES + NBAR * 8 + 16;
   // Request at least ~120 KB so that one CTA (and its 512 TMEM columns) owns the SM.
   static constexpr int SMEM_BYTES =
       (SMEM_BYTES_RAW > 120 * 1024 ? SMEM_BYTES_RAW : 120 * 1024) + 1024;
   static constexpr int LOAD_WARP = NUM_SOFTMAX_WARPS;
+  // MMA issuers: with P in shared memory one thread per query tile, each in a warp of its own
+  // (MMA_WARP + t), so that one tile's waits never hold back the other's MMAs; otherwise one
+  // thread issues both tiles' MMAs in a fixed interleave
+  static constexpr int ISSUERS = P_SMEM ? NT : 1;
   static constexpr int MMA_WARP = NUM_SOFTMAX_WARPS + 1;
-  static constexpr int THREADS = 32 * (NUM_SOFTMAX_WARPS + 2);
+  static constexpr int THREADS = 32 * (NUM_SOFTMAX_WARPS + 1 + ISSUERS);
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr int UMMA_K = FP8 ? 32 : 16;                 // K per MMA instruction
   static constexpr int KSTEPS_QK = ROW_BYTES / 32;             // 32 bytes of K per step
@@ -128,6 +140,7 @@ struct AttnCfg {
   static_assert(128 * NT + D * NT <= 512, "Tensor Memory budget");
   static_assert(NSLOT >= 2, "need a K and a V slot");
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
+  static_assert(SMEM_BYTES + EXTRA_MAX <= 227 * 1024, "shared memory budget with O staging");
 };
 
 // Where a bounded wait gave up (reported in the error info word).
@@ -271,7 +284,8 @@ __global__ void __launch_bounds__(AttnCfg<D, FP8>::THREADS, 1)
   constexpr bool STAGE_O = !VARLEN;
   const uint32_t sQ = base_u32;                                  // QBUF x NT tiles
   const uint32_t sKV = base_u32 + C::QBUF * NT * C::TILE_BYTES;  // NSLOT tiles
-  const uint32_t sOst = sKV + NSLOT * C::TILE_BYTES;             // STAGE_O: O staging
+  const uint32_t sP = sKV + NSLOT * C::TILE_BYTES;               // P_SMEM: NT numerator tiles
+  const uint32_t sOst = sP + C::P_BYTES;                         // STAGE_O: O staging
   const uint32_t bar0 = sOst + (STAGE_O ? C::OST_BYTES : 0);     // barriers (8 B each)
   uint8_t* bar_ptr = base + (bar0 - base_u32);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_ptr + C::NBAR * 8);
@@ -295,6 +309,9 @@ __global__ void __launch_bounds__(AttnCfg<D, FP8>::THREADS, 1)
   auto BAR_MMA_DONE = [&]() { return bar0 + 8u * (2 + 2 * NSLOT + 4 * NT); };
   // the first half of P_t (keys 0..63 of the tile) is in Tensor Memory
   auto BAR_P_HALF = [&](int t) { return bar0 + 8u * (2 + 2 * NSLOT + 4 * NT + 1 + t); };
+  // P_SMEM: the softmax warps of tile t have read S_t (4 arrivals), and PV_t has completed
+  auto BAR_S_READ = [&](int t) { return bar0 + 8u * (2 + 2 * NSLOT + 5 * NT + 3 + t); };
+  auto BAR_PV_DONE = [&](int t) { return bar0 + 8u * (2 + 2 * NSLOT + 6 * NT + 3 + t); };
 
   const uint32_t warp = warp_id();
   const uint32_t lane = lane_id();
@@ -302,11 +319,11 @@ __global__ void __launch_bounds__(AttnCfg<D, FP8>::THREADS, 1)
   if (threadIdx.x == 0) {
     for (int qb = 0; qb < 2; ++qb) {
       mbar_init(BAR_Q_FULL(qb), 1);
-      mbar_init(BAR_Q_EMPTY(qb), 1);
+      mbar_init(BAR_Q_EMPTY(qb), C::ISSUERS);      // one release per issuer
     }
     for (int s = 0; s < NSLOT; ++s) {
       mbar_init(BAR_KV_FULL(s), 1);
-      mbar_init(BAR_KV_EMPTY(s), 1);
+      mbar_init(BAR_KV_EMPTY(s), C::ISSUERS);
     }
     for (int t = 0; t < NT; ++t) {
       mbar_init(BAR_S_FULL(t), 1);
@@ -314,8 +331,10 @@ __global__ void __launch_bounds__(AttnCfg<D, FP8>::THREADS, 1)
       mbar_init(BAR_P_HALF(t), 4);
       mbar_init(BAR_O_FULL(t), 1);
       mbar_init(BAR_O_EMPTY(t), 4);
+      mbar_init(BAR_S_READ(t), 4);
+      mbar_init(BAR_PV_DONE(t), 1);
     }
-    mbar_init(BAR_MMA_DONE(), 1);
+    mbar_init(BAR_MMA_DONE(), C::ISSUERS);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -565,7 +584,7 @@ __global__ void __launch_bounds__(AttnCfg<D, FP8>::THREADS, 1)
           wait_drain(BAR_KV_FULL(i % NSLOT), (i / NSLOT) & 1, p.spin_limit);
       }
     }
-  } else if (warp == C::MMA_WARP) {
+  } else if (warp >= C::MMA_WARP && warp < C::MMA_WARP + C::ISSUERS) {
     // ========================================================== MMA issuer ==
     if (lane == 0) {
       // Descriptors are built once; a K-step advances the start address field (bits 0-13,
@@ -573,6 +592,7 @@ __global__ void __launch_bounds__(AttnCfg<D, FP8>::THREADS, 1)
       const uint64_t dq0 = smem_desc(sQ, 16, C::SBO, C::LAYOUT);
       const uint64_t dkv0 = smem_desc(sKV, 16, C::SBO, C::LAYOUT);
       const uint64_t dv0 = smem_desc(sKV, C::PANEL_BYTES, C::SBO, C::LAYOUT);
+      const uint64_t dp0 = smem_desc(sP, 16, 1024, 2);            // P_SMEM: 128-byte rows
       int qsel = 0;              // the Q buffer of the current item
       auto gemm_qk = [&](int t, int slot) {
         const uint32_t d = tmem + 128u * t;
@@ -598,78 +618,164 @@ __global__ void __launch_bounds__(AttnCfg<D, FP8>::THREADS, 1)
           else     mma_f16_ts(d, a, b0 + off, C::IDESC_PV, (acc || kk > 0) ? 1u : 0u);
         }
       };
-      int consumed = 0;          // K/V ring position
-      int pc[NT], ouse[NT];      // P phases consumed, and O uses completed, per query tile
+      // P_SMEM: O_t += P_t V with P_t from shared memory, 32 keys per K-step
+      auto gemm_pv_smem = [&](int t, int slot, bool acc) {
+        const uint32_t d = tmem + 128u * NT + static_cast<uint32_t>(D) * t;
+        const uint64_t a0 = dp0 + ((t * 128 * 128) >> 4);
+        const uint64_t b0 = dv0 + ((slot * C::TILE_BYTES) >> 4);
 #pragma unroll
-      for (int t = 0; t < NT; ++t) pc[t] = ouse[t] = 0;
-      bool ok = true;
-      for (int n = 0; ok && n * G < n_items; ++n) {
-        const int item = item_of(n);
-        if (item >= n_items) break;
-        Item it;
-        decode(item, it);
-        qsel = n % C::QBUF;
-        ok = wait_bounded(BAR_Q_FULL(qsel), (n / C::QBUF) & 1, ctl, WHERE_MMA);
-        if (!ok) break;
-        {
-          const int ks = consumed % NSLOT;
-          ok = wait_bounded(BAR_KV_FULL(ks), (consumed / NSLOT) & 1, ctl, WHERE_MMA);
-          ++consumed;
+        for (int kk = 0; kk < C::KSTEPS_PV; ++kk)
+          mma_f8_ss(d, a0 + 2 * kk, b0 + ((kk * C::UMMA_K * C::PANEL_ROW) >> 4), C::IDESC_PV,
+                    (acc || kk > 0) ? 1u : 0u);
+      };
+      if constexpr (!C::P_SMEM) {
+        // A single issuer: per key step PV_0, S_0, PV_1, S_1 (P_t lies over S_t in Tensor Memory,
+        // so S_t(j) follows PV_t(j-1)); with one query tile P is handed over in two halves.
+        int consumed = 0;          // K/V ring position
+        int pc[NT], ouse[NT];      // P phases consumed, and O uses completed, per query tile
+#pragma unroll
+        for (int t = 0; t < NT; ++t) pc[t] = ouse[t] = 0;
+        bool ok = true;
+        for (int n = 0; ok && n * G < n_items; ++n) {
+          const int item = item_of(n);
+          if (item >= n_items) break;
+          Item it;
+          decode(item, it);
+          qsel = n % C::QBUF;
+          ok = wait_bounded(BAR_Q_FULL(qsel), (n / C::QBUF) & 1, ctl, WHERE_MMA);
           if (!ok) break;
-          tc_fence_after();
+          {
+            const int ks = consumed % NSLOT;
+            ok = wait_bounded(BAR_KV_FULL(ks), (consumed / NSLOT) & 1, ctl, WHERE_MMA);
+            ++consumed;
+            if (!ok) break;
+            tc_fence_after();
 #pragma unroll
-          for (int t = 0; t < NT; ++t) {
-            if (it.n[t] > 0) {
-              gemm_qk(t, ks);
-              mma_commit(BAR_S_FULL(t));
-            }
-          }
-          if (it.nmax == 1) mma_commit(BAR_Q_EMPTY(qsel));
-          mma_commit(BAR_KV_EMPTY(ks));
-        }
-        for (int j = 1; ok && j <= it.nmax; ++j) {
-          const int vs = consumed % NSLOT;
-          ok = wait_bounded(BAR_KV_FULL(vs), (consumed / NSLOT) & 1, ctl, WHERE_MMA);
-          ++consumed;
-          if (!ok) break;
-          tc_fence_after();
-          int ks = -1;   // K_j is waited for only right before the first S(j) that needs it
-#pragma unroll
-          for (int t = 0; t < NT; ++t) {
-            if (j - 1 < it.n[t]) {
-              if (j - 1 == 0) {
-                // O_t is free once the softmax warps have read the previous item's O_t.
-                if (!wait_bounded(BAR_O_EMPTY(t), (ouse[t] & 1) ^ 1, ctl, WHERE_MMA)) { ok = false; break; }
-              }
-              if constexpr (SPLIT_P) {
-                if (!wait_bounded(BAR_P_HALF(t), pc[t] & 1, ctl, WHERE_MMA)) { ok = false; break; }
-                tc_fence_after();
-                gemm_pv(t, vs, j - 1 > 0, 0, C::KSTEPS_PV / 2);
-              }
-              if (!wait_bounded(BAR_P_FULL(t), pc[t] & 1, ctl, WHERE_MMA)) { ok = false; break; }
-              ++pc[t];
-              tc_fence_after();
-              gemm_pv(t, vs, SPLIT_P || j - 1 > 0, SPLIT_P ? C::KSTEPS_PV / 2 : 0, C::KSTEPS_PV);
-              if (j - 1 == it.n[t] - 1) {
-                mma_commit(BAR_O_FULL(t));
-                ++ouse[t];
+            for (int t = 0; t < NT; ++t) {
+              if (it.n[t] > 0) {
+                gemm_qk(t, ks);
+                mma_commit(BAR_S_FULL(t));
               }
             }
-            if (t == NT - 1) mma_commit(BAR_KV_EMPTY(vs));
-            if (j < it.n[t]) {
-              if (ks < 0) {
-                ks = consumed % NSLOT;
-                if (!wait_bounded(BAR_KV_FULL(ks), (consumed / NSLOT) & 1, ctl, WHERE_MMA)) { ok = false; break; }
-                ++consumed;
-                tc_fence_after();
-              }
-              gemm_qk(t, ks);
-              mma_commit(BAR_S_FULL(t));
-            }
-          }
-          if (ok && ks >= 0) {
-            if (j == it.nmax - 1) mma_commit(BAR_Q_EMPTY(qsel));
+            if (it.nmax == 1) mma_commit(BAR_Q_EMPTY(qsel));
             mma_commit(BAR_KV_EMPTY(ks));
+          }
+          for (int j = 1; ok && j <= it.nmax; ++j) {
+            const int vs = consumed % NSLOT;
+            ok = wait_bounded(BAR_KV_FULL(vs), (consumed / NSLOT) & 1, ctl, WHERE_MMA);
+            ++consumed;
+            if (!ok) break;
+            tc_fence_after();
+            int ks = -1;   // K_j is waited for only right before the first S(j) that needs it
+#pragma unroll
+            for (int t = 0; t < NT; ++t) {
+              if (j - 1 < it.n[t]) {
+                if (j - 1 == 0) {
+                  // O_t is free once the softmax warps have read the previous item's O_t.
+                  if (!wait_bounded(BAR_O_EMPTY(t), (ouse[t] & 1) ^ 1, ctl, WHERE_MMA)) { ok = false; break; }
+                }
+                if constexpr (SPLIT_P) {
+                  if (!wait_bounded(BAR_P_HALF(t), pc[t] & 1, ctl, WHERE_MMA)) { ok = false; break; }
+                  tc_fence_after();
+                  gemm_pv(t, vs, j - 1 > 0, 0, C::KSTEPS_PV / 2);
+                }
+                if (!wait_bounded(BAR_P_FULL(t), pc[t] & 1, ctl, WHERE_MMA)) { ok = false; break; }
+                ++pc[t];
+                tc_fence_after();
+                gemm_pv(t, vs, SPLIT_P || j - 1 > 0, SPLIT_P ? C::KSTEPS_PV / 2 : 0, C::KSTEPS_PV);
+                if (j - 1 == it.n[t] - 1) {
+                  mma_commit(BAR_O_FULL(t));
+                  ++ouse[t];
+                }
+              }
+              if (t == NT - 1) mma_commit(BAR_KV_EMPTY(vs));
+              if (j < it.n[t]) {
+                if (ks < 0) {
+                  ks = consumed % NSLOT;
+                  if (!wait_bounded(BAR_KV_FULL(ks), (consumed / NSLOT) & 1, ctl, WHERE_MMA)) { ok = false; break; }
+                  ++consumed;
+                  tc_fence_after();
+                }
+                gemm_qk(t, ks);
+                mma_commit(BAR_S_FULL(t));
+              }
+            }
+            if (ok && ks >= 0) {
+              if (j == it.nmax - 1) mma_commit(BAR_Q_EMPTY(qsel));
+              mma_commit(BAR_KV_EMPTY(ks));
+            }
+          }
+        }
+      } else {
+        // P in shared memory: query tile t's issuer.  Every ring position (K_j, V_j of each item, in load order) is
+        // released once by each issuer: by a commit after its MMAs that read it, or, where its
+        // tile does not need it (causal items, rows past the sequence), by an arrival once the
+        // copy has landed, so that the slot's phases stay in step.
+        const int t = static_cast<int>(warp) - C::MMA_WARP;
+        int consumed = 0;          // K/V ring position
+        int pc = 0, ouse = 0;      // P phases consumed, O uses completed
+        int qkc = 0;               // QK^T products issued
+        bool ok = true;
+        auto release = [&](int pos, bool used) -> bool {
+          if (used) {
+            mma_commit(BAR_KV_EMPTY(pos % NSLOT));
+            return true;
+          }
+          if (!wait_bounded(BAR_KV_FULL(pos % NSLOT), (pos / NSLOT) & 1, ctl, WHERE_MMA)) return false;
+          mbar_arrive(BAR_KV_EMPTY(pos % NSLOT));
+          return true;
+        };
+        for (int n = 0; ok && n * G < n_items; ++n) {
+          const int item = item_of(n);
+          if (item >= n_items) break;
+          Item it;
+          decode(item, it);
+          const int nt = it.n[t];
+          qsel = n % C::QBUF;
+          if (!wait_bounded(BAR_Q_FULL(qsel), (n / C::QBUF) & 1, ctl, WHERE_MMA)) { ok = false; break; }
+          if (nt == 0) mbar_arrive(BAR_Q_EMPTY(qsel));
+          // S_t(j) = Q_t K_j^T from ring position kpos; the last one releases the Q buffer.
+          auto issue_qk = [&](int j, int kpos) -> bool {
+            if (!wait_bounded(BAR_KV_FULL(kpos % NSLOT), (kpos / NSLOT) & 1, ctl, WHERE_MMA)) return false;
+            // S_t is free once the softmax warps have read the previous one
+            if (qkc > 0 && !wait_bounded(BAR_S_READ(t), (qkc - 1) & 1, ctl, WHERE_MMA)) return false;
+            tc_fence_after();
+            gemm_qk(t, kpos % NSLOT);
+            mma_commit(BAR_S_FULL(t));
+            ++qkc;
+            if (j == nt - 1) mma_commit(BAR_Q_EMPTY(qsel));
+            return true;
+          };
+          // O_t += P_t(j) V_j from ring position vpos.
+          auto issue_pv = [&](int j, int vpos) -> bool {
+            if (!wait_bounded(BAR_KV_FULL(vpos % NSLOT), (vpos / NSLOT) & 1, ctl, WHERE_MMA)) return false;
+            // O_t is free once the softmax warps have read the previous item's O_t.
+            if (j == 0 && !wait_bounded(BAR_O_EMPTY(t), (ouse & 1) ^ 1, ctl, WHERE_MMA)) return false;
+            if (!wait_bounded(BAR_P_FULL(t), pc & 1, ctl, WHERE_MMA)) return false;
+            ++pc;
+            tc_fence_after();
+            gemm_pv_smem(t, vpos % NSLOT, j > 0);
+            mma_commit(BAR_PV_DONE(t));
+            if (j == nt - 1) {
+              mma_commit(BAR_O_FULL(t));
+              ++ouse;
+            }
+            return true;
+          };
+          {
+            const int kpos = consumed++;
+            if (nt > 0 && !issue_qk(0, kpos)) { ok = false; break; }
+            if (!release(kpos, nt > 0)) { ok = false; break; }
+          }
+          for (int j = 1; ok && j <= it.nmax; ++j) {
+            const int vpos = consumed++;
+            const int kpos = j < it.nmax ? consumed++ : -1;
+            const bool do_qk = j < nt, do_pv = j - 1 < nt;
+            // S_t(j) first: it needs only the softmax warps to have read S_t(j-1)
+            if (do_qk && !issue_qk(j, kpos)) { ok = false; break; }
+            if (do_pv && !issue_pv(j - 1, vpos)) { ok = false; break; }
+            if (!release(vpos, do_pv)) { ok = false; break; }
+            if (kpos >= 0 && !release(kpos, do_qk)) { ok = false; break; }
           }
         }
       }
@@ -686,6 +792,11 @@ __global__ void __launch_bounds__(AttnCfg<D, FP8>::THREADS, 1)
     const uint32_t s_addr = tl + 128u * t;
     const uint32_t o_addr = tl + 128u * NT + static_cast<uint32_t>(D) * t;
     int sc = 0, ouse = 0;      // S phases consumed, O uses completed (this tile)
+    int pcnt = 0;              // P_SMEM: numerator tiles handed over (this tile)
+    // P_SMEM: this thread's row of P_t, 128 bytes in the 128-byte swizzle (16-byte chunk c of
+    // row r at chunk c ^ (r & 7) of its row)
+    const uint32_t p_row = sP + static_cast<uint32_t>(t) * (128u * 128u) +
+                           static_cast<uint32_t>((row_local >> 3) * 1024 + (row_local & 7) * 128);
     bool ok = true;
     for (int n = 0; ok && n * G < n_items; ++n) {
       const int item = item_of(n);
@@ -747,6 +858,12 @@ __global__ void __launch_bounds__(AttnCfg<D, FP8>::THREADS, 1)
         for (int c = 0; c < 4; ++c)
 #pragma unroll
           for (int i = 0; i < 32; ++i) reg_fence(sr[c][i]);
+        if constexpr (C::P_SMEM) {
+          // S_t is in registers: the MMA warp may compute the next S_t over it
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(BAR_S_READ(t));
+        }
 
         // masks: causal diagonal tile, or the ragged last key tile
         if (SPLIT ? (j == nt - 1 && ragged_end)
@@ -854,9 +971,22 @@ __global__ void __launch_bounds__(AttnCfg<D, FP8>::THREADS, 1)
               }
               pk[i] = pack_e4m3x4(pv[0], pv[1], pv[2], pv[3]);
             }
-            tmem_st16(s_addr + 16u * h2, pk);
-            if (SPLIT_P && h2 == 0) hand_off_first_half();
+            if constexpr (C::P_SMEM) {
+              // P_t and O_t are free once the previous PV_t has completed
+              if (h2 == 0 && pcnt > 0 && !warp_wait(BAR_PV_DONE(t), (pcnt - 1) & 1, ctl, WHERE_SOFTMAX)) ok = false;
+              if (ok) {
+#pragma unroll
+                for (int c4 = 0; c4 < 4; ++c4) {
+                  const uint32_t chunk = static_cast<uint32_t>((4 * h2 + c4) ^ (row_local & 7));
+                  st_shared_v4(p_row + 16u * chunk, pk[4 * c4], pk[4 * c4 + 1], pk[4 * c4 + 2], pk[4 * c4 + 3]);
+                }
+              }
+            } else {
+              tmem_st16(s_addr + 16u * h2, pk);
+              if (SPLIT_P && h2 == 0) hand_off_first_half();
+            }
           }
+          if (!ok) break;
         }
         {
           const uint64_t t2 = f2_add(f2_add(ls2[0], ls2[1]), f2_add(ls2[2], ls2[3]));
@@ -866,6 +996,10 @@ __global__ void __launch_bounds__(AttnCfg<D, FP8>::THREADS, 1)
         }
         if (!SPLIT_P) rescale_o();
         tmem_wait_st();
+        if constexpr (C::P_SMEM) {
+          fence_proxy_async_smem();      // P_t's shared-memory writes, for the tensor core
+          ++pcnt;
+        }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(BAR_P_FULL(t));
