@@ -834,12 +834,22 @@ __global__ void __launch_bounds__(AttnCfg<D, FP8>::THREADS, 1)
 
       float m_run = -INFINITY;
       float l_run = 0.f;
+      // Per-tile FP8 scales are read one key tile ahead, so the loads' latency hides behind a
+      // whole step (S is often ready at once, with nothing else to wait for).
+      float sk_next = 1.f, sv_next = 1.f;
+      if (FP8) {
+        if (p.k_scale != nullptr) sk_next = p.k_scale[kv_tile0];
+        if (p.v_scale != nullptr) sv_next = p.v_scale[kv_tile0];
+      }
       for (int j = 0; j < nt; ++j) {
-        // Per-tile FP8 scales are read before waiting for S, so the loads overlap the wait.
         float cmul = p.c_log2, bias = 0.f, inv_r = 1.f;
         if (FP8) {
-          const float sk = p.k_scale != nullptr ? p.k_scale[kv_tile0 + j] : 1.f;
-          const float sv_raw = p.v_scale != nullptr ? p.v_scale[kv_tile0 + j] : 1.f;
+          const float sk = sk_next;
+          const float sv_raw = sv_next;
+          if (j + 1 < nt) {
+            if (p.k_scale != nullptr) sk_next = p.k_scale[kv_tile0 + j + 1];
+            if (p.v_scale != nullptr) sv_next = p.v_scale[kv_tile0 + j + 1];
+          }
           // a zero scale (a block of zeros) as 2^-30 of the largest: its numerators vanish in E4M3,
           // the row sum still takes them at full weight
           const float sv = fmaxf(sv_raw, sv_max * 0x1p-30f);
