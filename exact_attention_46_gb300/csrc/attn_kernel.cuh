@@ -92,11 +92,11 @@ struct AttnCfg {
   static constexpr int TILE_BYTES = 128 * ROW_BYTES;
   static constexpr uint32_t LAYOUT = PANEL_ROW == 128 ? 2u : 4u;   // SW128 / SW64
   static constexpr uint32_t SBO = 8 * PANEL_ROW;               // stride of 8-row groups
-  // E4M3 numerators with two query tiles go through shared memory (one 128 x 128-byte tile per
-  // query tile, K-major, 128-byte swizzle) instead of over S in Tensor Memory, so the next
+  // E4M3 numerators with two query tiles go through shared memory (two 128 x 128-byte buffers
+  // per query tile, K-major, 128-byte swizzle) instead of over S in Tensor Memory, so the next
   // QK^T may overwrite S as soon as the softmax warps have read it
   static constexpr bool P_SMEM = FP8 && NT == 2;
-  static constexpr int P_BYTES = P_SMEM ? NT * 128 * 128 : 0;
+  static constexpr int P_BYTES = P_SMEM ? NT * 2 * 128 * 128 : 0;
   static constexpr int SMEM_TILES_BUDGET = 200 * 1024;
   static constexpr int NSLOT_RAW = (SMEM_TILES_BUDGET - NT * TILE_BYTES - P_BYTES) / TILE_BYTES;
   static constexpr int NSLOT_CAP = P_SMEM ? 6 : 8;
@@ -618,10 +618,10 @@ __global__ void __launch_bounds__(AttnCfg<D, FP8>::THREADS, 1)
           else     mma_f16_ts(d, a, b0 + off, C::IDESC_PV, (acc || kk > 0) ? 1u : 0u);
         }
       };
-      // P_SMEM: O_t += P_t V with P_t from shared memory, 32 keys per K-step
-      auto gemm_pv_smem = [&](int t, int slot, bool acc) {
+      // P_SMEM: O_t += P_t V with P_t from its shared-memory buffer pb, 32 keys per K-step
+      auto gemm_pv_smem = [&](int t, int pb, int slot, bool acc) {
         const uint32_t d = tmem + 128u * NT + static_cast<uint32_t>(D) * t;
-        const uint64_t a0 = dp0 + ((t * 128 * 128) >> 4);
+        const uint64_t a0 = dp0 + (((2 * t + pb) * 128 * 128) >> 4);
         const uint64_t b0 = dv0 + ((slot * C::TILE_BYTES) >> 4);
 #pragma unroll
         for (int kk = 0; kk < C::KSTEPS_PV; ++kk)
@@ -752,9 +752,9 @@ __global__ void __launch_bounds__(AttnCfg<D, FP8>::THREADS, 1)
             // O_t is free once the softmax warps have read the previous item's O_t.
             if (j == 0 && !wait_bounded(BAR_O_EMPTY(t), (ouse & 1) ^ 1, ctl, WHERE_MMA)) return false;
             if (!wait_bounded(BAR_P_FULL(t), pc & 1, ctl, WHERE_MMA)) return false;
-            ++pc;
             tc_fence_after();
-            gemm_pv_smem(t, vpos % NSLOT, j > 0);
+            gemm_pv_smem(t, pc & 1, vpos % NSLOT, j > 0);
+            ++pc;
             mma_commit(BAR_PV_DONE(t));
             if (j == nt - 1) {
               mma_commit(BAR_O_FULL(t));
@@ -793,9 +793,9 @@ __global__ void __launch_bounds__(AttnCfg<D, FP8>::THREADS, 1)
     const uint32_t o_addr = tl + 128u * NT + static_cast<uint32_t>(D) * t;
     int sc = 0, ouse = 0;      // S phases consumed, O uses completed (this tile)
     int pcnt = 0;              // P_SMEM: numerator tiles handed over (this tile)
-    // P_SMEM: this thread's row of P_t, 128 bytes in the 128-byte swizzle (16-byte chunk c of
-    // row r at chunk c ^ (r & 7) of its row)
-    const uint32_t p_row = sP + static_cast<uint32_t>(t) * (128u * 128u) +
+    // P_SMEM: this thread's row of P_t in buffer 0, 128 bytes in the 128-byte swizzle (16-byte
+    // chunk c of row r at chunk c ^ (r & 7) of its row); P_t number k goes to buffer k & 1
+    const uint32_t p_row = sP + static_cast<uint32_t>(2 * t) * (128u * 128u) +
                            static_cast<uint32_t>((row_local >> 3) * 1024 + (row_local & 7) * 128);
     bool ok = true;
     for (int n = 0; ok && n * G < n_items; ++n) {
@@ -917,13 +917,17 @@ __global__ void __launch_bounds__(AttnCfg<D, FP8>::THREADS, 1)
         uint64_t ls2[4];
 #pragma unroll
         for (int k = 0; k < 4; ++k) ls2[k] = f2_pack(0.f, 0.f);
-        // O_t holds PV_t(j-1) complete (it preceded S_t(j)) and PV_t(j) waits for this warp's
-        // arrival, so O_t is rescaled in place before that arrival.  With one query tile
+        // O_t holds PV_t(j-1) complete (it preceded S_t(j), or P_SMEM: PV-done) and PV_t(j) waits
+        // for this warp's arrival, so O_t is rescaled in place before that arrival.  With one query tile
         // (SPLIT_P) the first 64 keys' numerators are handed over on their own, so PV over them
         // overlaps the exponentials of the second half; with two tiles the other tile's MMAs
         // already fill that time and the extra hand-off only costs.
-        auto rescale_o = [&]() {
+        auto rescale_o = [&]() -> bool {
           if (__any_sync(0xffffffffu, rescale)) {
+            // P_SMEM: S_t(j) does not follow PV_t(j-1), so O_t waits for it here
+            if (C::P_SMEM && pcnt > 0 && !warp_wait(BAR_PV_DONE(t), (pcnt - 1) & 1, ctl, WHERE_SOFTMAX))
+              return false;
+            tc_fence_after();
 #pragma unroll 1
             for (int c = 0; c < D / 32; ++c) {
               uint32_t o[32];
@@ -937,9 +941,10 @@ __global__ void __launch_bounds__(AttnCfg<D, FP8>::THREADS, 1)
               tmem_st32(o_addr + 32u * c, o);
             }
           }
+          return true;
         };
         auto hand_off_first_half = [&]() {
-          rescale_o();
+          (void)rescale_o();
           tmem_wait_st();
           tc_fence_before();
           __syncwarp();
@@ -982,21 +987,19 @@ __global__ void __launch_bounds__(AttnCfg<D, FP8>::THREADS, 1)
               pk[i] = pack_e4m3x4(pv[0], pv[1], pv[2], pv[3]);
             }
             if constexpr (C::P_SMEM) {
-              // P_t and O_t are free once the previous PV_t has completed
-              if (h2 == 0 && pcnt > 0 && !warp_wait(BAR_PV_DONE(t), (pcnt - 1) & 1, ctl, WHERE_SOFTMAX)) ok = false;
-              if (ok) {
+              // The buffer's previous numerators (two tiles back) have been read: the MMA warp
+              // issued S_t(j), whose completion this warp has seen, after PV_t(j - 2).
+              const uint32_t prow = p_row + static_cast<uint32_t>(pcnt & 1) * (128u * 128u);
 #pragma unroll
-                for (int c4 = 0; c4 < 4; ++c4) {
-                  const uint32_t chunk = static_cast<uint32_t>((4 * h2 + c4) ^ (row_local & 7));
-                  st_shared_v4(p_row + 16u * chunk, pk[4 * c4], pk[4 * c4 + 1], pk[4 * c4 + 2], pk[4 * c4 + 3]);
-                }
+              for (int c4 = 0; c4 < 4; ++c4) {
+                const uint32_t chunk = static_cast<uint32_t>((4 * h2 + c4) ^ (row_local & 7));
+                st_shared_v4(prow + 16u * chunk, pk[4 * c4], pk[4 * c4 + 1], pk[4 * c4 + 2], pk[4 * c4 + 3]);
               }
             } else {
               tmem_st16(s_addr + 16u * h2, pk);
               if (SPLIT_P && h2 == 0) hand_off_first_half();
             }
           }
-          if (!ok) break;
         }
         {
           const uint64_t t2 = f2_add(f2_add(ls2[0], ls2[1]), f2_add(ls2[2], ls2[3]));
@@ -1004,7 +1007,7 @@ __global__ void __launch_bounds__(AttnCfg<D, FP8>::THREADS, 1)
           f2_unpack(t2, a0, a1);
           l_run += (a0 + a1) * inv_r;
         }
-        if (!SPLIT_P) rescale_o();
+        if (!SPLIT_P && !rescale_o()) { ok = false; break; }
         tmem_wait_st();
         if constexpr (C::P_SMEM) {
           fence_proxy_async_smem();      // P_t's shared-memory writes, for the tensor core
