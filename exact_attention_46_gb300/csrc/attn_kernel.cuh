@@ -309,6 +309,11 @@ __global__ void __launch_bounds__(AttnCfg<D, FP8>::THREADS, 1)
   auto BAR_MMA_DONE = [&]() { return bar0 + 8u * (2 + 2 * NSLOT + 4 * NT); };
   // the first half of P_t (keys 0..63 of the tile) is in Tensor Memory
   auto BAR_P_HALF = [&](int t) { return bar0 + 8u * (2 + 2 * NSLOT + 4 * NT + 1 + t); };
+  // P_SMEM: numerators of tile t in buffer b are in shared memory (4 arrivals).  One barrier
+  // per buffer: the softmax warps may run a whole tile ahead of the issuer, and a single
+  // barrier could then complete two phases before the issuer looks at it.  A buffer is
+  // refilled only after PV_t has read it, so its barrier is never more than one phase ahead.
+  auto BAR_P_SM = [&](int t, int b) { return b == 0 ? BAR_P_FULL(t) : BAR_P_HALF(t); };
   // P_SMEM: the softmax warps of tile t have read S_t (4 arrivals), and PV_t has completed
   auto BAR_S_READ = [&](int t) { return bar0 + 8u * (2 + 2 * NSLOT + 5 * NT + 3 + t); };
   auto BAR_PV_DONE = [&](int t) { return bar0 + 8u * (2 + 2 * NSLOT + 6 * NT + 3 + t); };
@@ -751,7 +756,7 @@ __global__ void __launch_bounds__(AttnCfg<D, FP8>::THREADS, 1)
             if (!wait_bounded(BAR_KV_FULL(vpos % NSLOT), (vpos / NSLOT) & 1, ctl, WHERE_MMA)) return false;
             // O_t is free once the softmax warps have read the previous item's O_t.
             if (j == 0 && !wait_bounded(BAR_O_EMPTY(t), (ouse & 1) ^ 1, ctl, WHERE_MMA)) return false;
-            if (!wait_bounded(BAR_P_FULL(t), pc & 1, ctl, WHERE_MMA)) return false;
+            if (!wait_bounded(BAR_P_SM(t, pc & 1), (pc >> 1) & 1, ctl, WHERE_MMA)) return false;
             tc_fence_after();
             gemm_pv_smem(t, pc & 1, vpos % NSLOT, j > 0);
             ++pc;
@@ -1009,13 +1014,14 @@ __global__ void __launch_bounds__(AttnCfg<D, FP8>::THREADS, 1)
         }
         if (!SPLIT_P && !rescale_o()) { ok = false; break; }
         tmem_wait_st();
+        const uint32_t bar_p = C::P_SMEM ? BAR_P_SM(t, pcnt & 1) : BAR_P_FULL(t);
         if constexpr (C::P_SMEM) {
           fence_proxy_async_smem();      // P_t's shared-memory writes, for the tensor core
           ++pcnt;
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(BAR_P_FULL(t));
+        if (lane == 0) mbar_arrive(bar_p);
       }
       if (!ok) break;
 
