@@ -35,6 +35,7 @@ SIGNATURES = {
     "attn_bwd_gqa": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _I, _I, _I, _I, _I, _I, _F, _P]),
     "attn_bwd_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _P]),
     "hadamard_rotate_quant_fp8": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _P]),
+    "hadamard_rotate_quant_fp8_qkv": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P]),
     "rope_cos_sin_table": (_I, [_P, _I, _I, _D, _P]),
     "rope_hadamard_rotate_quant_fp8": (_I, [_P, _P, _I, _P, _P, _P, _I, _I, _I, _I, _P]),
     "attn_get_last_error": (ctypes.c_char_p, []),

@@ -384,15 +384,66 @@ int run_quant(const void* x, const float* rope_cs, int n_pos, void* out, float* 
   int* err = nullptr;
   int rc = err_words(&err);
   if (rc != ATTN_OK) return rc;
-  CUtensorMap tx, tout;
-  if ((rc = make_qkv_map(&tx, x, B, S, H, D, false)) != ATTN_OK) return rc;
+  QuantMaps m;
+  if ((rc = make_qkv_map(&m.x[0], x, B, S, H, D, false)) != ATTN_OK) return rc;
   // the quantiser stores its codes one warp's rows at a time: 32 rows, 16 at D = 256
-  if ((rc = make_qkv_map(&tout, out, B, S, H, D, true, D == 256 ? 16 : 32)) != ATTN_OK) return rc;
+  if ((rc = make_qkv_map(&m.out[0], out, B, S, H, D, true, D == 256 ? 16 : 32)) != ATTN_OK) return rc;
   QuantParams p{B, H, S, nblk, out, scale, signs, rope_cs, spin_limit(), err, err + 1, cu_seqlens, n_seq, n_pos};
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  cudaError_t e = D == 64    ? launch_hadamard_quant<64>(tx, tout, p, st)
-                  : D == 128 ? launch_hadamard_quant<128>(tx, tout, p, st)
-                             : launch_hadamard_quant<256>(tx, tout, p, st);
+  cudaError_t e = D == 64    ? launch_hadamard_quant<64>(m, p, st)
+                  : D == 128 ? launch_hadamard_quant<128>(m, p, st)
+                             : launch_hadamard_quant<256>(m, p, st);
+  if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "quantiser launch failed: %s", cudaGetErrorString(e));
+  return ok();
+}
+
+// Q, K and V in one quantiser launch: Q and K rotated (when signs is given), V not.
+int run_quant_qkv(const void* const x[3], void* const out[3], float* const scale[3], const float* signs, int B,
+                  int H, int S, int D, void* stream) {
+  for (int t = 0; t < 3; ++t)
+    if (x[t] == nullptr || out[t] == nullptr || scale[t] == nullptr)
+      return fail(ATTN_ERR_INVALID_ARG, "q, k, v, their codes and their scales must be non-null device pointers");
+  if (B < 1 || H < 1 || S < 1)
+    return fail(ATTN_ERR_INVALID_ARG, "B, H, S must be >= 1 (got %d, %d, %d)", B, H, S);
+  if (D != 64 && D != 128 && D != 256)
+    return fail(D > 0 ? ATTN_ERR_UNSUPPORTED : ATTN_ERR_INVALID_ARG,
+                "head dimension D = %d not supported (64, 128, 256)", D);
+  for (int t = 0; t < 3; ++t)
+    if (!aligned16(x[t]) || !aligned16(out[t]) || (reinterpret_cast<uintptr_t>(scale[t]) & 3u))
+      return fail(ATTN_ERR_INVALID_ARG, "inputs and codes must be 16-byte and scales 4-byte aligned");
+  if (signs != nullptr && !aligned16(signs)) return fail(ATTN_ERR_INVALID_ARG, "signs must be 16-byte aligned");
+  const unsigned long long n = 1ull * B * S * H * D;
+  const long long nblk_ll = (S + 127) / 128;
+  if (n > (1ull << 40) / 2 || 3 * nblk_ll * H * B >= 0x7fffffffll || H > 65535 || B > 65535)
+    return fail(ATTN_ERR_INVALID_ARG, "tensors too large for the grid");
+  const int nblk = static_cast<int>(nblk_ll);
+  const size_t sbytes = 4ull * B * H * nblk;
+  // the six outputs overlap neither each other nor the three inputs
+  const void* obuf[6] = {out[0], out[1], out[2], scale[0], scale[1], scale[2]};
+  const size_t olen[6] = {n, n, n, sbytes, sbytes, sbytes};
+  for (int i = 0; i < 6; ++i) {
+    for (int t = 0; t < 3; ++t)
+      if (overlap(obuf[i], olen[i], x[t], 2 * n)) return fail(ATTN_ERR_INVALID_ARG, "outputs overlap an input");
+    for (int j = i + 1; j < 6; ++j)
+      if (overlap(obuf[i], olen[i], obuf[j], olen[j])) return fail(ATTN_ERR_INVALID_ARG, "outputs overlap each other");
+  }
+  int* err = nullptr;
+  int rc = err_words(&err);
+  if (rc != ATTN_OK) return rc;
+  QuantMaps m;
+  for (int t = 0; t < 3; ++t) {
+    if ((rc = make_qkv_map(&m.x[t], x[t], B, S, H, D, false)) != ATTN_OK) return rc;
+    if ((rc = make_qkv_map(&m.out[t], out[t], B, S, H, D, true, D == 256 ? 16 : 32)) != ATTN_OK) return rc;
+  }
+  QuantParams p{B, H, S, nblk, out[0], scale[0], signs, nullptr, spin_limit(), err, err + 1, nullptr, 0, 0};
+  p.n_tensors = 3;
+  p.rot_tensors = signs != nullptr ? 2 : 0;
+  p.scale1 = scale[1];
+  p.scale2 = scale[2];
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = D == 64    ? launch_hadamard_quant<64>(m, p, st)
+                  : D == 128 ? launch_hadamard_quant<128>(m, p, st)
+                             : launch_hadamard_quant<256>(m, p, st);
   if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "quantiser launch failed: %s", cudaGetErrorString(e));
   return ok();
 }
@@ -598,6 +649,15 @@ int attn_fwd_fp8(const void* q8, const void* k8, const void* v8, const float* q_
 int hadamard_rotate_quant_fp8(const void* x, void* out, float* scale, const float* signs, int B,
                               int H, int S, int D, void* stream) {
   return run_quant(x, nullptr, 0, out, scale, signs, B, H, S, D, stream);
+}
+
+int hadamard_rotate_quant_fp8_qkv(const void* q, const void* k, const void* v, void* q8, void* k8, void* v8,
+                                  float* q_scale, float* k_scale, float* v_scale, const float* signs, int B,
+                                  int H, int S, int D, void* stream) {
+  const void* x[3] = {q, k, v};
+  void* out[3] = {q8, k8, v8};
+  float* scale[3] = {q_scale, k_scale, v_scale};
+  return run_quant_qkv(x, out, scale, signs, B, H, S, D, stream);
 }
 
 int rope_hadamard_rotate_quant_fp8(const void* x, const float* rope_cs, int n_pos, void* out, float* scale,

@@ -163,11 +163,13 @@ __device__ __forceinline__ bool group_bar_or(uint32_t id, uint32_t n, bool v) {
   return r != 0;
 }
 
-template <int D, bool ROTATE, bool ROPE, bool VARLEN>
+// QKV: the three tensors Q, K, V in one launch (blocks of tensor t numbered after tensor t-1's),
+// the first p.rot_tensors of them rotated: one ramp and one tail instead of three.
+template <int D, bool ROTATE, bool ROPE, bool VARLEN, bool QKV>
 __global__ void __launch_bounds__(QCfg<D, ROPE, ROTATE, VARLEN>::THREADS, 1)
-    hadamard_quant_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmOut,
-                          const QuantParams p) {
+    hadamard_quant_kernel(const __grid_constant__ QuantMaps m, const QuantParams p) {
   using C = QCfg<D, ROPE, ROTATE, VARLEN>;
+  static_assert(!QKV || (ROTATE && !ROPE && !VARLEN), "the three-tensor form is fixed-length, without RoPE");
   constexpr int VPT = C::VPT;
   constexpr int NSTAGE = C::NSTAGE;
   constexpr int NW = VPT / 8;         // 16-byte input chunks per thread
@@ -197,7 +199,8 @@ __global__ void __launch_bounds__(QCfg<D, ROPE, ROTATE, VARLEN>::THREADS, 1)
   // a row, so the 8 lanes of one 128-bit shared-memory read phase hold 8 different rows
   const int r = gwarp * C::RPW + lane % C::RPW;
   const int part = lane / C::RPW;
-  const int nblocks = p.nblk * p.H * p.B;
+  const int nb1 = p.nblk * p.H * p.B;                 // blocks of one tensor
+  const int nblocks = nb1 * (QKV ? 3 : 1);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < NSTAGE; ++s) {
@@ -208,15 +211,72 @@ __global__ void __launch_bounds__(QCfg<D, ROPE, ROTATE, VARLEN>::THREADS, 1)
     }
     *abort_flag = 0;
     fence_barrier_init();
-    prefetch_tmap(&tmX);
-    prefetch_tmap(&tmOut);
+    for (int t = 0; t < (QKV ? 3 : 1); ++t) {
+      prefetch_tmap(&m.x[t]);
+      prefetch_tmap(&m.out[t]);
+    }
   }
+
+  // Load of the k-th block of this CTA into stage k % NSTAGE.  Called by thread 0 for the first
+  // NSTAGE blocks, then by lane 0 of the last warp of the group that has just taken block
+  // k - NSTAGE out of that stage: one caller per stage at a time.
+  auto issue = [&](int k) {
+    const int bt = static_cast<int>(blockIdx.x) + k * static_cast<int>(gridDim.x);
+    const int tsr = QKV ? bt / nb1 : 0, bi = bt - tsr * nb1;
+    const int h = bi % p.H, blk = (bi / p.H) % p.nblk, b = bi / (p.H * p.nblk);
+    const int s = k % NSTAGE;
+    const uint32_t st = base_u32 + s * C::STAGE_BYTES;
+    const uint32_t bar = bar0 + 8u * s;
+    issued[s] += 1;
+    int tok0 = blk * QROWS, rblk = blk;   // rblk: the block's position block for RoPE
+    // the stage's next phase is block k's; published before the arrival (release), so that a
+    // waiter that sees k here sees the barrier at or past the phase block k's load completes
+    if constexpr (VARLEN) {
+      // the sequence of index blk: the last s with cu[s] / 128 + s <= blk (cu[0] / 128 + 0 = 0)
+      int lo = 0, hi = p.n_seq - 1;
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if ((p.cu_seqlens[mid] >> 7) + mid <= blk) lo = mid; else hi = mid - 1;
+      }
+      const int s0 = p.cu_seqlens[lo], len = p.cu_seqlens[lo + 1] - s0;
+      const int kb = blk - ((s0 >> 7) + lo);
+      const int rows = 128 * kb < len ? min(QROWS, len - 128 * kb) : 0;
+      tok0 = s0 + 128 * kb;
+      rblk = kb;
+      stage_info[s] = make_int2(tok0, rows);
+      if (rows == 0) {                // an index no block lives at
+        st_release_shared(gen0 + 4u * s, k);
+        mbar_arrive(bar);
+        return;
+      }
+    }
+    st_release_shared(gen0 + 4u * s, k);
+    mbar_arrive_expect_tx(bar, C::TX_BYTES);
+#pragma unroll
+    for (int pn = 0; pn < C::NPANEL; ++pn)
+      tma_load_4d(st + pn * C::PANEL_BYTES, &m.x[tsr], bar, 64 * pn, h, tok0, b,
+                  l2_policy_evict_first());
+    if (ROPE) {
+      // coarse rows 128 blk + 16 r1 after the block's input in the same stage
+#pragma unroll
+      for (int r1 = 0; r1 < NCOARSE; ++r1)
+        bulk_load(st + C::COARSE_OFF + r1 * C::TROW,
+                  p.rope_cs + static_cast<size_t>(rblk * QROWS + 16 * r1) * D, 4 * D, bar,
+                  l2_policy_evict_last());
+    }
+  };
+  const int my_blocks = (nblocks - static_cast<int>(blockIdx.x) + static_cast<int>(gridDim.x) - 1) /
+                        static_cast<int>(gridDim.x);
+  // Fixed-length launches start their first loads at once, before the tables below (whose
+  // global reads would otherwise delay them); packed batches check their offsets first.
+  if (!VARLEN && threadIdx.x == 0)
+    for (int k = 0; k < NSTAGE && k < my_blocks; ++k) issue(k);
   if (!ROPE) {
     // bit 15 flips the even element of a packed bf16 pair, bit 31 the odd one
     for (int w = static_cast<int>(threadIdx.x); w < D / 2; w += C::THREADS)
-      sign_mask[w] = ROTATE ? ((p.signs[2 * w] < 0.f ? 0x00008000u : 0u) |
-                               (p.signs[2 * w + 1] < 0.f ? 0x80000000u : 0u))
-                            : 0u;
+      sign_mask[w] = ROTATE && p.signs != nullptr ? ((p.signs[2 * w] < 0.f ? 0x00008000u : 0u) |
+                                                     (p.signs[2 * w + 1] < 0.f ? 0x80000000u : 0u))
+                                                  : 0u;
   } else {
     // The rotary step comes before the signs: the even element's sign is folded into the
     // resident rows below, the odd element then needs sign(2i) * sign(2i+1).
@@ -251,58 +311,9 @@ __global__ void __launch_bounds__(QCfg<D, ROPE, ROTATE, VARLEN>::THREADS, 1)
   // this one's CTAs leave (one CTA per SM, so every CTA of this grid is running by now), read
   // and transform their first blocks, and wait for this grid to complete before they write.
   grid_launch_dependents();
-
-  // Load of the k-th block of this CTA into stage k % NSTAGE.  Called by thread 0 for the first
-  // NSTAGE blocks, then by lane 0 of the last warp of the group that has just taken block
-  // k - NSTAGE out of that stage: one caller per stage at a time.
-  auto issue = [&](int k) {
-    const int bi = static_cast<int>(blockIdx.x) + k * static_cast<int>(gridDim.x);
-    const int h = bi % p.H, blk = (bi / p.H) % p.nblk, b = bi / (p.H * p.nblk);
-    const int s = k % NSTAGE;
-    const uint32_t st = base_u32 + s * C::STAGE_BYTES;
-    const uint32_t bar = bar0 + 8u * s;
-    issued[s] += 1;
-    int tok0 = blk * QROWS, rblk = blk;   // rblk: the block's position block for RoPE
-    // the stage's next phase is block k's; published before the arrival (release), so that a
-    // waiter that sees k here sees the barrier at or past the phase block k's load completes
-    if constexpr (VARLEN) {
-      // the sequence of index blk: the last s with cu[s] / 128 + s <= blk (cu[0] / 128 + 0 = 0)
-      int lo = 0, hi = p.n_seq - 1;
-      while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if ((p.cu_seqlens[mid] >> 7) + mid <= blk) lo = mid; else hi = mid - 1;
-      }
-      const int s0 = p.cu_seqlens[lo], len = p.cu_seqlens[lo + 1] - s0;
-      const int kb = blk - ((s0 >> 7) + lo);
-      const int rows = 128 * kb < len ? min(QROWS, len - 128 * kb) : 0;
-      tok0 = s0 + 128 * kb;
-      rblk = kb;
-      stage_info[s] = make_int2(tok0, rows);
-      if (rows == 0) {                // an index no block lives at
-        st_release_shared(gen0 + 4u * s, k);
-        mbar_arrive(bar);
-        return;
-      }
-    }
-    st_release_shared(gen0 + 4u * s, k);
-    mbar_arrive_expect_tx(bar, C::TX_BYTES);
-#pragma unroll
-    for (int pn = 0; pn < C::NPANEL; ++pn)
-      tma_load_4d(st + pn * C::PANEL_BYTES, &tmX, bar, 64 * pn, h, tok0, b,
-                  l2_policy_evict_first());
-    if (ROPE) {
-      // coarse rows 128 blk + 16 r1 after the block's input in the same stage
-#pragma unroll
-      for (int r1 = 0; r1 < NCOARSE; ++r1)
-        bulk_load(st + C::COARSE_OFF + r1 * C::TROW,
-                  p.rope_cs + static_cast<size_t>(rblk * QROWS + 16 * r1) * D, 4 * D, bar,
-                  l2_policy_evict_last());
-    }
-  };
-  const int my_blocks = (nblocks - static_cast<int>(blockIdx.x) + static_cast<int>(gridDim.x) - 1) /
-                        static_cast<int>(gridDim.x);
-  if (threadIdx.x == 0)
+  if (VARLEN && threadIdx.x == 0)
     for (int k = 0; k < NSTAGE && k < my_blocks; ++k) issue(k);
+
 
   // Wait for block k in its stage.  The barrier alone tells phases apart only by parity: a group
   // that runs ahead could find the stage still holding block k - 2 NSTAGE's completed phase,
@@ -329,9 +340,12 @@ __global__ void __launch_bounds__(QCfg<D, ROPE, ROTATE, VARLEN>::THREADS, 1)
   for (int k = g, it = 0; k < my_blocks; k += C::G, ++it) {
     // Blocks are numbered head-fastest: the groups running at one time read all heads of the
     // same tokens, i.e. contiguous memory.
-    const int bi = static_cast<int>(blockIdx.x) + k * static_cast<int>(gridDim.x);
+    const int bt = static_cast<int>(blockIdx.x) + k * static_cast<int>(gridDim.x);
+    const int tsr = QKV ? bt / nb1 : 0, bi = bt - tsr * nb1;
     const int h = bi % p.H, blk = (bi / p.H) % p.nblk, b = bi / (p.H * p.nblk);
     const int hb = b * p.H + h;
+    // whether this block is rotated (the same for the whole group: a uniform branch)
+    const bool rot = ROTATE && (!QKV || tsr < p.rot_tensors);
     const int stage = k % NSTAGE;
     const uint32_t st = base_u32 + stage * C::STAGE_BYTES;
     const bool ok = wait_block(k);
@@ -357,9 +371,9 @@ __global__ void __launch_bounds__(QCfg<D, ROPE, ROTATE, VARLEN>::THREADS, 1)
       uint32_t w[4];
       asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
                    : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]) : "r"(addr));
-      if (ROTATE && !ROPE) {
-        const uint4 m = reinterpret_cast<const uint4*>(sign_mask)[idx / 8];
-        w[0] ^= m.x; w[1] ^= m.y; w[2] ^= m.z; w[3] ^= m.w;
+      if (ROTATE && !ROPE && rot) {
+        const uint4 sm = reinterpret_cast<const uint4*>(sign_mask)[idx / 8];
+        w[0] ^= sm.x; w[1] ^= sm.y; w[2] ^= sm.z; w[3] ^= sm.w;
       }
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
@@ -397,15 +411,15 @@ __global__ void __launch_bounds__(QCfg<D, ROPE, ROTATE, VARLEN>::THREADS, 1)
     if (ROPE && ROTATE) {
 #pragma unroll
       for (int j = 0; j < VPT / 2; j += 4) {
-        const uint4 m = reinterpret_cast<const uint4*>(sign_mask)[(part * VPT / 2 + j) / 4];
-        v[2 * j + 1] = __uint_as_float(__float_as_uint(v[2 * j + 1]) ^ m.x);
-        v[2 * j + 3] = __uint_as_float(__float_as_uint(v[2 * j + 3]) ^ m.y);
-        v[2 * j + 5] = __uint_as_float(__float_as_uint(v[2 * j + 5]) ^ m.z);
-        v[2 * j + 7] = __uint_as_float(__float_as_uint(v[2 * j + 7]) ^ m.w);
+        const uint4 sm = reinterpret_cast<const uint4*>(sign_mask)[(part * VPT / 2 + j) / 4];
+        v[2 * j + 1] = __uint_as_float(__float_as_uint(v[2 * j + 1]) ^ sm.x);
+        v[2 * j + 3] = __uint_as_float(__float_as_uint(v[2 * j + 3]) ^ sm.y);
+        v[2 * j + 5] = __uint_as_float(__float_as_uint(v[2 * j + 5]) ^ sm.z);
+        v[2 * j + 7] = __uint_as_float(__float_as_uint(v[2 * j + 7]) ^ sm.w);
       }
     }
 
-    if (ROTATE) {
+    if (ROTATE && rot) {
       // butterflies over the index bits held by this thread: bit 0 pairs the two halves of a
       // packed pair, every higher bit pairs whole pairs, done with f32x2 add/sub
 #pragma unroll
@@ -457,8 +471,9 @@ __global__ void __launch_bounds__(QCfg<D, ROPE, ROTATE, VARLEN>::THREADS, 1)
 
     const float inv = amax > 0.f ? 448.f / amax : 0.f;
     if (leader) {
-      const float norm = ROTATE ? rsqrtf(static_cast<float>(D)) : 1.f;
-      p.scale[static_cast<size_t>(hb) * p.nblk + blk] = amax > 0.f ? (amax * norm) / 448.f : 1.f;
+      const float norm = rot ? rsqrtf(static_cast<float>(D)) : 1.f;
+      float* sc = !QKV ? p.scale : (tsr == 0 ? p.scale : (tsr == 1 ? p.scale1 : p.scale2));
+      sc[static_cast<size_t>(hb) * p.nblk + blk] = amax > 0.f ? (amax * norm) / 448.f : 1.f;
     }
     // Codes into the group's buffer in the output map's swizzled layout, then one tensor store
     // per panel of this warp's rows: whole 128-byte lines reach L2 instead of 16-byte pieces of
@@ -503,7 +518,7 @@ __global__ void __launch_bounds__(QCfg<D, ROPE, ROTATE, VARLEN>::THREADS, 1)
       if (lane == 0 && tok0 + row0 < p.S) {
 #pragma unroll
         for (int pn = 0; pn < C::NCPANEL; ++pn)
-          tma_store_4d(&tmOut, outbuf + pn * (QROWS * C::CODE_PANEL) + row0 * C::CODE_PANEL, pn * C::CODE_PANEL,
+          tma_store_4d(&m.out[tsr], outbuf + pn * (QROWS * C::CODE_PANEL) + row0 * C::CODE_PANEL, pn * C::CODE_PANEL,
                        h, tok0 + row0, b);
         bulk_commit_group();
         ++n_stores;
@@ -526,11 +541,10 @@ __global__ void __launch_bounds__(QCfg<D, ROPE, ROTATE, VARLEN>::THREADS, 1)
   }
 }
 
-template <int D, bool ROTATE, bool ROPE, bool VARLEN = false>
-cudaError_t launch_variant(const CUtensorMap& tx, const CUtensorMap& tout, const QuantParams& p, int sm_count,
-                           cudaStream_t stream) {
+template <int D, bool ROTATE, bool ROPE, bool VARLEN = false, bool QKV = false>
+cudaError_t launch_variant(const QuantMaps& m, const QuantParams& p, int sm_count, cudaStream_t stream) {
   using C = QCfg<D, ROPE, ROTATE, VARLEN>;
-  const long long nblocks = static_cast<long long>(p.nblk) * p.H * p.B;
+  const long long nblocks = static_cast<long long>(p.nblk) * p.H * p.B * (QKV ? 3 : 1);
   // one CTA per SM (a small problem spreads over as many SMs as it has blocks; groups without
   // a block idle)
   const unsigned grid = static_cast<unsigned>(nblocks < sm_count ? nblocks : sm_count);
@@ -544,22 +558,21 @@ cudaError_t launch_variant(const CUtensorMap& tx, const CUtensorMap& tout, const
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, hadamard_quant_kernel<D, ROTATE, ROPE, VARLEN>, tx, tout, p);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, hadamard_quant_kernel<D, ROTATE, ROPE, VARLEN, QKV>, m, p);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
-template <int D, bool ROTATE, bool ROPE, bool VARLEN = false>
+template <int D, bool ROTATE, bool ROPE, bool VARLEN = false, bool QKV = false>
 cudaError_t set_smem() {
-  return cudaFuncSetAttribute(hadamard_quant_kernel<D, ROTATE, ROPE, VARLEN>,
+  return cudaFuncSetAttribute(hadamard_quant_kernel<D, ROTATE, ROPE, VARLEN, QKV>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize, QCfg<D, ROPE, ROTATE, VARLEN>::SMEM_BYTES);
 }
 
 }  // namespace
 
 template <int D>
-cudaError_t launch_hadamard_quant(const CUtensorMap& tx, const CUtensorMap& tout, const QuantParams& p,
-                                  cudaStream_t stream) {
+cudaError_t launch_hadamard_quant(const QuantMaps& m, const QuantParams& p, cudaStream_t stream) {
   static std::atomic<unsigned long long> configured{0};
   static int sm_count[64] = {0};
   int dev = 0;
@@ -575,6 +588,7 @@ cudaError_t launch_hadamard_quant(const CUtensorMap& tx, const CUtensorMap& tout
     if ((e = set_smem<D, false, false, true>()) != cudaSuccess) return e;
     if ((e = set_smem<D, true, true, true>()) != cudaSuccess) return e;
     if ((e = set_smem<D, false, true, true>()) != cudaSuccess) return e;
+    if ((e = set_smem<D, true, false, false, true>()) != cudaSuccess) return e;
     int n = 0;
     e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
@@ -583,25 +597,23 @@ cudaError_t launch_hadamard_quant(const CUtensorMap& tx, const CUtensorMap& tout
   }
   const int sms = sm_count[dev & 63];
   const bool rot = p.signs != nullptr, rope = p.rope_cs != nullptr;
+  if (p.n_tensors == 3) return launch_variant<D, true, false, false, true>(m, p, sms, stream);
   if (p.cu_seqlens != nullptr) {
     if (rope)
-      return rot ? launch_variant<D, true, true, true>(tx, tout, p, sms, stream)
-                 : launch_variant<D, false, true, true>(tx, tout, p, sms, stream);
-    return rot ? launch_variant<D, true, false, true>(tx, tout, p, sms, stream)
-               : launch_variant<D, false, false, true>(tx, tout, p, sms, stream);
+      return rot ? launch_variant<D, true, true, true>(m, p, sms, stream)
+                 : launch_variant<D, false, true, true>(m, p, sms, stream);
+    return rot ? launch_variant<D, true, false, true>(m, p, sms, stream)
+               : launch_variant<D, false, false, true>(m, p, sms, stream);
   }
   if (rope)
-    return rot ? launch_variant<D, true, true>(tx, tout, p, sms, stream)
-               : launch_variant<D, false, true>(tx, tout, p, sms, stream);
-  return rot ? launch_variant<D, true, false>(tx, tout, p, sms, stream)
-             : launch_variant<D, false, false>(tx, tout, p, sms, stream);
+    return rot ? launch_variant<D, true, true>(m, p, sms, stream)
+               : launch_variant<D, false, true>(m, p, sms, stream);
+  return rot ? launch_variant<D, true, false>(m, p, sms, stream)
+             : launch_variant<D, false, false>(m, p, sms, stream);
 }
 
-template cudaError_t launch_hadamard_quant<64>(const CUtensorMap&, const CUtensorMap&, const QuantParams&,
-                                               cudaStream_t);
-template cudaError_t launch_hadamard_quant<128>(const CUtensorMap&, const CUtensorMap&, const QuantParams&,
-                                                cudaStream_t);
-template cudaError_t launch_hadamard_quant<256>(const CUtensorMap&, const CUtensorMap&, const QuantParams&,
-                                                cudaStream_t);
+template cudaError_t launch_hadamard_quant<64>(const QuantMaps&, const QuantParams&, cudaStream_t);
+template cudaError_t launch_hadamard_quant<128>(const QuantMaps&, const QuantParams&, cudaStream_t);
+template cudaError_t launch_hadamard_quant<256>(const QuantMaps&, const QuantParams&, cudaStream_t);
 
 }  // namespace ea46

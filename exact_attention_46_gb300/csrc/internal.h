@@ -136,13 +136,25 @@ struct QuantParams {
   const int* cu_seqlens;
   int n_seq;
   int n_pos;            // rows of rope_cs (VARLEN: checked against every sequence on the device)
+  // Q, K and V in one launch (fixed length, no RoPE): tensor t's blocks follow tensor t-1's,
+  // its scales go to scale (t = 0), scale1, scale2, and the first rot_tensors are rotated
+  int n_tensors = 1;
+  int rot_tensors = 1;
+  float* scale1 = nullptr;
+  float* scale2 = nullptr;
+};
+
+// Tensor maps of the quantiser's inputs and outputs: [0] only, or Q, K, V.
+struct QuantMaps {
+  CUtensorMap x[3];
+  CUtensorMap out[3];
 };
 
 // x is read through `tx`, the same [B, S, H, D] bf16 tensor map the attention kernel uses;
 // codes are written through `tout`, an E4M3 map of the same tensor whose box is one warp's
 // rows (32, or 16 at D = 256).
 template <int D>
-cudaError_t launch_hadamard_quant(const CUtensorMap& tx, const CUtensorMap& tout, const QuantParams& p,
+cudaError_t launch_hadamard_quant(const QuantMaps& m, const QuantParams& p,
                                   cudaStream_t stream);
 
 // cs[p, i] = (cos, sin)(p * base^(-2i/D)) for p < n_pos, i < D/2, in fp64 rounded to fp32.

@@ -380,6 +380,32 @@ def hadamard_rotate_quant_fp8(x, signs=None, out=None, scale=None, stream=None):
     return out, scale
 
 
+def hadamard_rotate_quant_fp8_qkv(q, k, v, signs=None, out=None, scale=None, stream=None):
+    """``hadamard_rotate_quant_fp8`` of q and k (rotated by ``signs``) and of v (not rotated), in one
+    launch.  Returns (q8, q_scale, k8, k_scale, v8, v_scale); bitwise what three separate calls give.
+    ``out`` / ``scale``: optional sequences of three preallocated code / scale tensors (q, k, v).
+    """
+    dev = _arg(q, "q", _BF16, dim=4).device
+    B, S, H, D = q.shape
+    _arg(k, "k", _BF16, shape=(B, S, H, D), device=dev)
+    _arg(v, "v", _BF16, shape=(B, S, H, D), device=dev)
+    _opt(signs, "signs", _F32, shape=(D,), device=dev)
+    codes = list(out) if out is not None else [None] * 3
+    scales = list(scale) if scale is not None else [None] * 3
+    if len(codes) != 3 or len(scales) != 3:
+        raise ValueError("out and scale take three tensors each (q, k, v)")
+    for i, n in enumerate("qkv"):
+        _opt(codes[i], n + "8", _CODES, shape=(B, S, H, D), device=dev)
+        _opt(scales[i], n + "_scale", _F32, shape=(B, H, block_count(S)), device=dev)
+        if codes[i] is None:
+            codes[i] = torch.empty((B, S, H, D), dtype=torch.uint8, device=dev)
+        if scales[i] is None:
+            scales[i] = torch.empty((B, H, block_count(S)), dtype=torch.float32, device=dev)
+    _lib.call("hadamard_rotate_quant_fp8_qkv", _ptr(q), _ptr(k), _ptr(v), *[_ptr(c) for c in codes],
+              *[_ptr(s_) for s_ in scales], _ptr(signs), B, H, S, D, _stream(stream))
+    return codes[0], scales[0], codes[1], scales[1], codes[2], scales[2]
+
+
 def rope_cos_sin_table(n_pos, D, base=10000.0, device="cuda", out=None, stream=None):
     """Rotary table fp32 [n_pos, D/2, 2]: (cos, sin) of p * base^(-2i/D), built on the GPU."""
     _opt(out, "out", _F32, shape=(n_pos, D // 2, 2))

@@ -338,6 +338,29 @@ int hadamard_rotate_quant_fp8(const void* x, void* out, float* scale, const floa
                               int B, int H, int S, int D, void* stream);
 
 /*
+ * hadamard_rotate_quant_fp8_qkv -- hadamard_rotate_quant_fp8 of Q and K
+ * (rotated by the same signs) and of V (not rotated), in one launch.
+ *   [NL] "Technische innovaties", item 3, and [HADA] "Niedrige FP8-Präzision
+ *   und incoherent processing", as for hadamard_rotate_quant_fp8: the
+ *   rotation is applied to the two operands of Q K^T, whose product it
+ *   leaves unchanged; V is quantised as it is.
+ *   q, k, v        : [B, S, H, D] bf16 inputs (16-byte aligned).
+ *   q8, k8, v8     : [B, S, H, D] E4M3 outputs (16-byte aligned).
+ *   q_scale, k_scale, v_scale : [B, H, ceil(S/128)] fp32 outputs.
+ *   signs          : D fp32 values +1 / -1 for Q and K, or NULL (then none
+ *                    of the three is rotated).
+ *   Every output holds exactly what hadamard_rotate_quant_fp8 writes for
+ *   its tensor (the same arithmetic); the three tensors' blocks are one
+ *   grid's work list, so the launch has one start-up and one tail instead of
+ *   three.  The six outputs must overlap neither each other nor the inputs.
+ *   Overlap with neighbouring quantiser launches and errors as
+ *   hadamard_rotate_quant_fp8.
+ */
+int hadamard_rotate_quant_fp8_qkv(const void* q, const void* k, const void* v, void* q8, void* k8,
+                                  void* v8, float* q_scale, float* k_scale, float* v_scale,
+                                  const float* signs, int B, int H, int S, int D, void* stream);
+
+/*
  * rope_cos_sin_table -- the rotary-embedding table.
  *   [HADA] "Niedrige FP8-Präzision und incoherent processing" names rotary
  *   embedding as the bandwidth-bound op to fuse the rotation with but does
