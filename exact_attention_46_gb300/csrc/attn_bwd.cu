@@ -12,9 +12,10 @@
 //              (bandwidth-bound, plain loads).
 //   2. dK/dV:  CTA = 128 keys of one (b, h); K, V stay in shared memory while Q_j, dO_j and
 //              the rows' Delta / lse stream through a TMA ring.  Per query tile the tensor core
-//              forms S^T = K Q_j^T and dP^T = V dO_j^T in Tensor Memory; the four compute
-//              warps (thread = key row = TMEM lane) turn them into P^T and dS^T (bf16, written
-//              back over S^T and dP^T); then dV += P^T dO_j and dK += dS^T Q_j accumulate in
+//              forms S^T = K Q_j^T and dP^T = V dO_j^T in Tensor Memory; the eight compute
+//              warps (thread = key row = TMEM lane; two warps per row, each half the columns)
+//              turn them into P^T and dS^T (bf16, written back over S^T and dP^T); then
+//              dV += P^T dO_j and dK += dS^T Q_j accumulate in
 //              Tensor Memory (A operand from Tensor Memory, B = dO_j / Q_j read N-major).
 //   3. dQ:     CTA = 128 queries; Q, dO resident, K_j, V_j stream; S = Q K_j^T and
 //              dP = dO V_j^T, dS by the compute warps (thread = query row), dQ += dS K_j.
@@ -27,8 +28,9 @@
 // dK/dV CTA therefore belongs to (key tile, b, key/value head) and streams the query tiles of
 // every head of the group through the same ring, so the sum stays in Tensor Memory.
 //
-// Tensor Memory (512 columns): S (P over its first 64 columns) at 0, dP (dS over its first 64)
-// at 128, then the accumulators (dV, dK at 256 and 256 + D; dQ at 256).  D = 64 or 128.
+// Tensor Memory (512 columns): S at 0 (P over columns 0-31 and 64-95: each half of the compute
+// warps over its own half of S), dP at 128 (dS likewise), then the accumulators (dV, dK at 256
+// and 256 + D; dQ at 256).  D = 64 or 128.
 //
 // Every mbarrier wait is bounded (ptx.cuh); a wait that runs out records ATTN_ERR_TIMEOUT and
 // every role leaves through the common exit, which frees Tensor Memory.
@@ -64,10 +66,13 @@ struct BwdCfg {
   static constexpr int KSTEPS_TS = 128 / 16;
   static constexpr uint32_t IDESC_SS = instr_desc(1, 0, 128, 128);
   static constexpr uint32_t IDESC_TS = instr_desc(1, 1, 128, D);
-  static constexpr int NBAR = 4 + 2 * NSTAGE + 2;
+  static constexpr int NBAR = 4 + 2 * NSTAGE + 3;     // ..., done, dP ready, dS ready
   static constexpr int SMEM_BYTES = 1024 + 2 * TILE_BYTES + NSTAGE * STAGE_BYTES + NBAR * 8 + 16;
-  static constexpr int THREADS = 32 * 6;                       // 4 compute, 1 load, 1 MMA
-  static constexpr int LOAD_WARP = 4, MMA_WARP = 5;
+  // 8 compute warps: two per Tensor-Memory lane quarter, each taking 64 of a tile's 128
+  // columns (the compute is elementwise, so the halves never meet), then 1 load, 1 MMA
+  static constexpr int COMPUTE_WARPS = 8;
+  static constexpr int THREADS = 32 * (COMPUTE_WARPS + 2);
+  static constexpr int LOAD_WARP = COMPUTE_WARPS, MMA_WARP = COMPUTE_WARPS + 1;
   static_assert(D == 64 || D == 128, "head dimension");
   static_assert(256 + 2 * D <= 512, "Tensor Memory budget");
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
@@ -151,6 +156,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
   auto BAR_FULL = [&](int s) { return bar0 + 32 + 8u * s; };
   auto BAR_EMPTY = [&](int s) { return bar0 + 32 + 8u * (NSTAGE + s); };
   const uint32_t BAR_DONE = bar0 + 32 + 8u * (2 * NSTAGE);
+  // dP^T ready (its own commit, after S^T's), and dS^T written (after P^T's hand-off)
+  const uint32_t BAR_DP = BAR_DONE + 8, BAR_DS = BAR_DONE + 16;
 
   const uint32_t warp = warp_id(), lane = lane_id();
   // CTA -> (key tile, b, key/value head): key tile slowest, so the causal key tiles with the
@@ -174,13 +181,15 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
   if (threadIdx.x == 0) {
     mbar_init(BAR_KV, 1);
     mbar_init(BAR_S, 1);
-    mbar_init(BAR_P, 4);
+    mbar_init(BAR_P, C::COMPUTE_WARPS);
     mbar_init(BAR_ACC, 1);
     for (int s = 0; s < NSTAGE; ++s) {
       mbar_init(BAR_FULL(s), 1);
       mbar_init(BAR_EMPTY(s), 1);
     }
     mbar_init(BAR_DONE, 1);
+    mbar_init(BAR_DP, 1);
+    mbar_init(BAR_DS, C::COMPUTE_WARPS);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -235,22 +244,34 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
           const uint32_t off = ((kk / C::STEPS_PER_PANEL) * C::PANEL_BYTES + (kk % C::STEPS_PER_PANEL) * 32) >> 4;
           mma_f16_ss(tmem, dK + off, dQk + off, C::IDESC_SS, kk > 0);
         }
+        mma_commit(BAR_S);                                // the exponentials start on S^T ...
 #pragma unroll
-        for (int kk = 0; kk < C::KSTEPS_SS; ++kk) {      // dP^T = V dO^T
+        for (int kk = 0; kk < C::KSTEPS_SS; ++kk) {      // ... while dP^T = V dO^T forms
           const uint32_t off = ((kk / C::STEPS_PER_PANEL) * C::PANEL_BYTES + (kk % C::STEPS_PER_PANEL) * 32) >> 4;
           mma_f16_ss(tmem + 128, dV + off, dDOk + off, C::IDESC_SS, kk > 0);
         }
-        mma_commit(BAR_S);
+        mma_commit(BAR_DP);
+        const uint64_t dDOn = smem_desc(sDO(s), C::PANEL_BYTES, C::SBO, C::LAYOUT);
+        const uint64_t dQn = smem_desc(sQ(s), C::PANEL_BYTES, C::SBO, C::LAYOUT);
+        // P^T / dS^T of queries 16kk .. 16kk + 15 sit at 8kk + 32 (kk / 4) (the second half of
+        // the queries was written by the second half of the compute warps, over its own S^T)
         ok = wait_bounded(BAR_P, i & 1, ctl, WHERE_BWD_MMA);
         if (!ok) break;
         tc_fence_after();
-        const uint64_t dDOn = smem_desc(sDO(s), C::PANEL_BYTES, C::SBO, C::LAYOUT);
-        const uint64_t dQn = smem_desc(sQ(s), C::PANEL_BYTES, C::SBO, C::LAYOUT);
 #pragma unroll
-        for (int kk = 0; kk < C::KSTEPS_TS; ++kk) {      // dV += P^T dO, dK += dS^T Q
+        for (int kk = 0; kk < C::KSTEPS_TS; ++kk) {      // dV += P^T dO, while dS^T forms
           const uint32_t off = (kk * 16 * C::PANEL_ROW) >> 4;
-          mma_f16_ts(tmem + 256, tmem + 8u * kk, dDOn + off, C::IDESC_TS, (i > 0 || kk > 0) ? 1u : 0u);
-          mma_f16_ts(tmem + 256 + D, tmem + 128 + 8u * kk, dQn + off, C::IDESC_TS, (i > 0 || kk > 0) ? 1u : 0u);
+          mma_f16_ts(tmem + 256, tmem + 8u * kk + 32u * (kk / 4), dDOn + off, C::IDESC_TS,
+                     (i > 0 || kk > 0) ? 1u : 0u);
+        }
+        ok = wait_bounded(BAR_DS, i & 1, ctl, WHERE_BWD_MMA);
+        if (!ok) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < C::KSTEPS_TS; ++kk) {      // dK += dS^T Q
+          const uint32_t off = (kk * 16 * C::PANEL_ROW) >> 4;
+          mma_f16_ts(tmem + 256 + D, tmem + 128 + 8u * kk + 32u * (kk / 4), dQn + off, C::IDESC_TS,
+                     (i > 0 || kk > 0) ? 1u : 0u);
         }
         mma_commit(BAR_EMPTY(s));
       }
@@ -259,9 +280,10 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       wait_drain(BAR_DONE, 0, p.spin_limit);
     }
   } else {
-    // compute warps: thread = key row k0 + r
-    const int r = static_cast<int>(warp) * 32 + static_cast<int>(lane);
-    const uint32_t tl = tmem + ((warp * 32u) << 16);
+    // compute warps: thread = key row k0 + r of lane quarter wq, query columns 64 hc .. 64 hc + 63
+    const int wq = static_cast<int>(warp) % 4, hc = static_cast<int>(warp) / 4;
+    const int r = wq * 32 + static_cast<int>(lane);
+    const uint32_t tl = tmem + ((static_cast<uint32_t>(wq) * 32u) << 16);
     const int key = k0 + r;
     bool ok = true;
     for (int i = 0; ok && i < ntile; ++i) {
@@ -276,51 +298,77 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       tc_fence_after();
       // masks are needed only on the diagonal tile (causal) and the ragged last query tile
       const bool masked = (CAUSAL && q_tile(i) == kt) || q0 + 128 > p.S;
-#pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
-        uint32_t sv[32], pv[32];
+      // P^T of this warp's 64 queries (kept for dS^T), stored as bf16 over its own half of S^T
+      // (already read): queries 32c .. 32c + 31 at columns 16c + 32hc, so the two halves'
+      // stores never touch each other's S.  dV's MMAs start on them while dP^T is used below.
+      float pkeep[2][32];
+#pragma unroll
+      for (int cc = 0; cc < 2; ++cc) {
+        const int c = 2 * hc + cc;
+        uint32_t sv[32];
         tmem_ld32(tl + 32u * c, sv);
-        tmem_ld32(tl + 128u + 32u * c, pv);
         tmem_wait_ld();
-        uint32_t pk[16], dk[16];
+        uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 32; e += 4) {
-          // the columns' Delta and lse*log2e, four at a time (broadcast reads)
+          // the columns' lse*log2e, four at a time (broadcast reads)
           const float4 l4 = *reinterpret_cast<const float4*>(l2 + 32 * c + e);
-          const float4 d4 = *reinterpret_cast<const float4*>(dlt + 32 * c + e);
-          const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, dv4[4] = {d4.x, d4.y, d4.z, d4.w};
-          float pp[4], dd[4];
+          const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
             reg_fence(sv[e + u]);
-            reg_fence(pv[e + u]);
             float x = fmaf(__uint_as_float(sv[e + u]), p.c_log2, -lv[u]);
             if (masked) {
               const int q = q0 + 32 * c + e + u;
               if (!(q < p.S && (!CAUSAL || key <= q))) x = -INFINITY;
             }
-            pp[u] = ex2(x);
-            dd[u] = pp[u] * (__uint_as_float(pv[e + u]) - dv4[u]);
+            pkeep[cc][e + u] = ex2(x);
           }
-          pk[e / 2] = pack_bf16x2(pp[0], pp[1]);
-          pk[e / 2 + 1] = pack_bf16x2(pp[2], pp[3]);
-          dk[e / 2] = pack_bf16x2(dd[0], dd[1]);
-          dk[e / 2 + 1] = pack_bf16x2(dd[2], dd[3]);
+          pk[e / 2] = pack_bf16x2(pkeep[cc][e], pkeep[cc][e + 1]);
+          pk[e / 2 + 1] = pack_bf16x2(pkeep[cc][e + 2], pkeep[cc][e + 3]);
         }
-        tmem_st16(tl + 16u * c, pk);
-        tmem_st16(tl + 128u + 16u * c, dk);
+        tmem_st16(tl + static_cast<uint32_t>(16 * c + 32 * hc), pk);
       }
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(BAR_P);
+      // dS^T = P^T * (dP^T - Delta) over this warp's own half of dP^T, the same way
+      if (!warp_wait(BAR_DP, i & 1, ctl, WHERE_BWD_COMPUTE)) { ok = false; break; }
+      tc_fence_after();
+#pragma unroll
+      for (int cc = 0; cc < 2; ++cc) {
+        const int c = 2 * hc + cc;
+        uint32_t pv[32];
+        tmem_ld32(tl + 128u + 32u * c, pv);
+        tmem_wait_ld();
+        uint32_t dk[16];
+#pragma unroll
+        for (int e = 0; e < 32; e += 4) {
+          const float4 d4 = *reinterpret_cast<const float4*>(dlt + 32 * c + e);
+          const float dv4[4] = {d4.x, d4.y, d4.z, d4.w};
+          float dd[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            reg_fence(pv[e + u]);
+            dd[u] = pkeep[cc][e + u] * (__uint_as_float(pv[e + u]) - dv4[u]);
+          }
+          dk[e / 2] = pack_bf16x2(dd[0], dd[1]);
+          dk[e / 2 + 1] = pack_bf16x2(dd[2], dd[3]);
+        }
+        tmem_st16(tl + 128u + static_cast<uint32_t>(16 * c + 32 * hc), dk);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(BAR_DS);
     }
     if (ok && warp_wait(BAR_ACC, 0, ctl, WHERE_BWD_COMPUTE)) {
       tc_fence_after();
       const bool valid = key < p.S;
       const size_t row = ((static_cast<size_t>(b) * p.S + (valid ? key : 0)) * p.Hkv + hkv) * D;
-#pragma unroll 1
-      for (int part = 0; part < 2; ++part) {           // dV, then dK (times the softmax scale)
+      {
+        const int part = hc;                           // dV (first half of the warps), dK (times the softmax scale)
         __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(part ? p.dk : p.dv) + row;
         const float mul = part ? p.scale : 1.f;
 #pragma unroll 1
@@ -377,6 +425,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
   auto BAR_FULL = [&](int s) { return bar0 + 32 + 8u * s; };
   auto BAR_EMPTY = [&](int s) { return bar0 + 32 + 8u * (NSTAGE + s); };
   const uint32_t BAR_DONE = bar0 + 32 + 8u * (2 * NSTAGE);
+  // dP ready (its own commit, after S's), and dS written over S (BAR_P is not used here)
+  const uint32_t BAR_DP = BAR_DONE + 8, BAR_DS = BAR_DONE + 16;
 
   const uint32_t warp = warp_id(), lane = lane_id();
   // CTA -> (query tile, b, h): causal query tiles with the most key tiles start first
@@ -392,13 +442,15 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
   if (threadIdx.x == 0) {
     mbar_init(BAR_QD, 1);
     mbar_init(BAR_S, 1);
-    mbar_init(BAR_P, 4);
+    mbar_init(BAR_P, C::COMPUTE_WARPS);
     mbar_init(BAR_ACC, 1);
     for (int s = 0; s < NSTAGE; ++s) {
       mbar_init(BAR_FULL(s), 1);
       mbar_init(BAR_EMPTY(s), 1);
     }
     mbar_init(BAR_DONE, 1);
+    mbar_init(BAR_DP, 1);
+    mbar_init(BAR_DS, C::COMPUTE_WARPS);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -449,20 +501,23 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
           const uint32_t off = ((kk / C::STEPS_PER_PANEL) * C::PANEL_BYTES + (kk % C::STEPS_PER_PANEL) * 32) >> 4;
           mma_f16_ss(tmem, dQ + off, dKk + off, C::IDESC_SS, kk > 0);
         }
+        mma_commit(BAR_S);                                // the exponentials start on S ...
 #pragma unroll
-        for (int kk = 0; kk < C::KSTEPS_SS; ++kk) {      // dP = dO V^T
+        for (int kk = 0; kk < C::KSTEPS_SS; ++kk) {      // ... while dP = dO V^T forms
           const uint32_t off = ((kk / C::STEPS_PER_PANEL) * C::PANEL_BYTES + (kk % C::STEPS_PER_PANEL) * 32) >> 4;
           mma_f16_ss(tmem + 128, dDO + off, dVk + off, C::IDESC_SS, kk > 0);
         }
-        mma_commit(BAR_S);
-        ok = wait_bounded(BAR_P, i & 1, ctl, WHERE_BWD_MMA);
+        mma_commit(BAR_DP);
+        ok = wait_bounded(BAR_DS, i & 1, ctl, WHERE_BWD_MMA);
         if (!ok) break;
         tc_fence_after();
         const uint64_t dKn = smem_desc(sK(s), C::PANEL_BYTES, C::SBO, C::LAYOUT);
 #pragma unroll
         for (int kk = 0; kk < C::KSTEPS_TS; ++kk) {      // dQ += dS K
           const uint32_t off = (kk * 16 * C::PANEL_ROW) >> 4;
-          mma_f16_ts(tmem + 256, tmem + 8u * kk, dKn + off, C::IDESC_TS, (i > 0 || kk > 0) ? 1u : 0u);
+          // dS of keys 16kk .. 16kk + 15 at 8kk + 32 (kk / 4) (see the compute warps' stores)
+          mma_f16_ts(tmem + 256, tmem + 8u * kk + 32u * (kk / 4), dKn + off, C::IDESC_TS,
+                     (i > 0 || kk > 0) ? 1u : 0u);
         }
         mma_commit(BAR_EMPTY(s));
       }
@@ -471,9 +526,10 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       wait_drain(BAR_DONE, 0, p.spin_limit);
     }
   } else {
-    // compute warps: thread = query row q0 + r
-    const int r = static_cast<int>(warp) * 32 + static_cast<int>(lane);
-    const uint32_t tl = tmem + ((warp * 32u) << 16);
+    // compute warps: thread = query row q0 + r of lane quarter wq, key columns 64 hc .. 64 hc + 63
+    const int wq = static_cast<int>(warp) % 4, hc = static_cast<int>(warp) / 4;
+    const int r = wq * 32 + static_cast<int>(lane);
+    const uint32_t tl = tmem + ((static_cast<uint32_t>(wq) * 32u) << 16);
     const int qrow = q0 + r;
     const bool valid = qrow < p.S;
     const float dlt = valid ? p.ws[static_cast<size_t>(2 * bh) * p.Sp + qrow] : 0.f;
@@ -484,42 +540,55 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       const bool masked = (CAUSAL && i == qt) || kb + 128 > p.S;
       if (!warp_wait(BAR_S, i & 1, ctl, WHERE_BWD_COMPUTE)) { ok = false; break; }
       tc_fence_after();
-#pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
-        uint32_t sv[32], pv[32];
+      // P of this warp's 64 keys, while the tensor core forms dP
+      float pkeep[2][32];
+#pragma unroll
+      for (int cc = 0; cc < 2; ++cc) {
+        const int c = 2 * hc + cc;
+        uint32_t sv[32];
         tmem_ld32(tl + 32u * c, sv);
+        tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          reg_fence(sv[e]);
+          float x = fmaf(__uint_as_float(sv[e]), p.c_log2, -l2);
+          if (masked) {
+            const int kcol = kb + 32 * c + e;
+            if (!(kcol < p.S && (!CAUSAL || kcol <= qrow))) x = -INFINITY;
+          }
+          pkeep[cc][e] = ex2(x);
+        }
+      }
+      if (!warp_wait(BAR_DP, i & 1, ctl, WHERE_BWD_COMPUTE)) { ok = false; break; }
+      tc_fence_after();
+#pragma unroll
+      for (int cc = 0; cc < 2; ++cc) {
+        const int c = 2 * hc + cc;
+        uint32_t pv[32];
         tmem_ld32(tl + 128u + 32u * c, pv);
         tmem_wait_ld();
         uint32_t dk[16];
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
-          float dd[2];
-#pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            reg_fence(sv[e + u]);
-            reg_fence(pv[e + u]);
-            float x = fmaf(__uint_as_float(sv[e + u]), p.c_log2, -l2);
-            if (masked) {
-              const int kcol = kb + 32 * c + e + u;
-              if (!(kcol < p.S && (!CAUSAL || kcol <= qrow))) x = -INFINITY;
-            }
-            dd[u] = ex2(x) * (__uint_as_float(pv[e + u]) - dlt);
-          }
-          dk[e / 2] = pack_bf16x2(dd[0], dd[1]);
+          reg_fence(pv[e]);
+          reg_fence(pv[e + 1]);
+          dk[e / 2] = pack_bf16x2(pkeep[cc][e] * (__uint_as_float(pv[e]) - dlt),
+                                  pkeep[cc][e + 1] * (__uint_as_float(pv[e + 1]) - dlt));
         }
-        tmem_st16(tl + 16u * c, dk);
+        // dS over this warp's own half of S (already read): keys 32c .. 32c + 31 at 16c + 32hc
+        tmem_st16(tl + static_cast<uint32_t>(16 * c + 32 * hc), dk);
       }
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(BAR_P);
+      if (lane == 0) mbar_arrive(BAR_DS);
     }
     if (ok && warp_wait(BAR_ACC, 0, ctl, WHERE_BWD_COMPUTE)) {
       tc_fence_after();
       __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(p.dq) +
                            ((static_cast<size_t>(b) * p.S + (valid ? qrow : 0)) * p.H + h) * D;
 #pragma unroll 1
-      for (int c = 0; c < D / 32; ++c) {
+      for (int c = hc * (D / 64); c < (hc + 1) * (D / 64); ++c) {   // this warp's half of dQ's columns
         uint32_t a[32];
         tmem_ld32(tl + 256u + 32u * c, a);
         tmem_wait_ld();
