@@ -17,8 +17,10 @@
 //              turn them into P^T and dS^T (bf16, written back over S^T and dP^T); then
 //              dV += P^T dO_j and dK += dS^T Q_j accumulate in
 //              Tensor Memory (A operand from Tensor Memory, B = dO_j / Q_j read N-major).
-//   3. dQ:     CTA = 128 queries; Q, dO resident, K_j, V_j stream; S = Q K_j^T and
-//              dP = dO V_j^T, dS by the compute warps (thread = query row), dQ += dS K_j.
+//   3. dQ:     CTA = 128 queries; Q, dO resident, K_j, V_j stream (rings of their own); S =
+//              Q K_j^T (double-buffered in Tensor Memory) and dP = dO V_j^T, dS by the compute
+//              warps (thread = query row), dQ += dS K_j; S(j+1) and dP(j+1) are issued before
+//              dQ(j), so the compute warps do not wait for the tensor core between tiles.
 //   Recomputing S and dP in both kernels costs two extra GEMMs per tile pair but needs no
 //   atomics and no fp32 dQ accumulator in device memory.
 //
@@ -30,7 +32,7 @@
 //
 // Tensor Memory (512 columns): S at 0 (P over columns 0-31 and 64-95: each half of the compute
 // warps over its own half of S), dP at 128 (dS likewise), then the accumulators (dV, dK at 256
-// and 256 + D; dQ at 256).  D = 64 or 128.
+// and 256 + D; dQ at 256, and the dQ kernel's second S buffer at 384).  D = 64 or 128.
 //
 // Every mbarrier wait is bounded (ptx.cuh); a wait that runs out records ATTN_ERR_TIMEOUT and
 // every role leaves through the common exit, which frees Tensor Memory.
@@ -403,30 +405,53 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
 }
 
 // ------------------------------------------------------------------ kernel 3: dQ --
+// CTA = 128 queries of one (b, h).  Q and dO stay in shared memory; K_j and V_j stream through
+// rings of their own (K is read by S_j and later by dQ += dS_j K_j, V only by dP_j, so V's slots
+// free early).  S is double-buffered in Tensor Memory (the columns beside dQ are free), so the
+// MMA warp issues S(j+1) and dP(j+1) while the compute warps still work on tile j, and
+// dQ += dS(j) K_j after their dS(j): the compute warps go from tile to tile without waiting
+// for the tensor core.  dS(j) is written over S(j)'s own buffer.
+template <int D>
+struct DqCfg {
+  using C = BwdCfg<D>;
+  static constexpr int NK = D == 64 ? 4 : 3;             // K slots
+  static constexpr int NV = D == 64 ? 4 : 2;             // V slots
+  // Q/dO ready, dP ready, dP read, accumulate done, drain; then S ready and dS written per
+  // S buffer; then full/empty per K slot and per V slot
+  static constexpr int NBAR = 5 + 4 + 2 * NK + 2 * NV;
+  static constexpr int SMEM_BYTES = 1024 + (2 + NK + NV) * C::TILE_BYTES + NBAR * 8 + 16;
+  static constexpr uint32_t S1 = 384;                    // second S buffer's first column
+  static_assert(256 + D <= S1 && S1 + 128 <= 512, "Tensor Memory: S, dP, dQ, second S");
+  static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
+};
+
 template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
                   const BwdParams p) {
   using C = BwdCfg<D>;
-  constexpr int NSTAGE = C::NSTAGE;
+  using Q = DqCfg<D>;
+  constexpr int NK = Q::NK, NV = Q::NV;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_u32 = smem_u32(smem_raw);
   const uint32_t base_u32 = (raw_u32 + 1023u) & ~1023u;
   uint8_t* base = smem_raw + (base_u32 - raw_u32);
   const uint32_t sQ = base_u32, sDO = base_u32 + C::TILE_BYTES;
-  const uint32_t ring = base_u32 + 2 * C::TILE_BYTES;
-  const uint32_t bar0 = ring + NSTAGE * C::STAGE_BYTES;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + (bar0 - base_u32) + C::NBAR * 8);
+  auto sK = [&](int s) { return base_u32 + (2 + s) * C::TILE_BYTES; };
+  auto sV = [&](int s) { return base_u32 + (2 + NK + s) * C::TILE_BYTES; };
+  const uint32_t bar0 = base_u32 + (2 + NK + NV) * C::TILE_BYTES;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + (bar0 - base_u32) + Q::NBAR * 8);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  auto sK = [&](int s) { return ring + s * C::STAGE_BYTES; };
-  auto sV = [&](int s) { return ring + s * C::STAGE_BYTES + C::TILE_BYTES; };
-  const uint32_t BAR_QD = bar0, BAR_S = bar0 + 8, BAR_P = bar0 + 16, BAR_ACC = bar0 + 24;
-  auto BAR_FULL = [&](int s) { return bar0 + 32 + 8u * s; };
-  auto BAR_EMPTY = [&](int s) { return bar0 + 32 + 8u * (NSTAGE + s); };
-  const uint32_t BAR_DONE = bar0 + 32 + 8u * (2 * NSTAGE);
-  // dP ready (its own commit, after S's), and dS written over S (BAR_P is not used here)
-  const uint32_t BAR_DP = BAR_DONE + 8, BAR_DS = BAR_DONE + 16;
+  const uint32_t BAR_QD = bar0, BAR_DP = bar0 + 8, BAR_DPR = bar0 + 16, BAR_ACC = bar0 + 24;
+  const uint32_t BAR_DONE = bar0 + 32;
+  auto BAR_S = [&](int b) { return bar0 + 40 + 8u * b; };          // S(j) of buffer b complete
+  auto BAR_DS = [&](int b) { return bar0 + 56 + 8u * b; };         // dS(j) of buffer b written
+  auto BAR_KF = [&](int s) { return bar0 + 72 + 8u * s; };
+  auto BAR_KE = [&](int s) { return bar0 + 72 + 8u * (NK + s); };
+  auto BAR_VF = [&](int s) { return bar0 + 72 + 8u * (2 * NK + s); };
+  auto BAR_VE = [&](int s) { return bar0 + 72 + 8u * (2 * NK + NV + s); };
+  auto s_col = [&](int j) { return (j & 1) ? Q::S1 : 0u; };        // tile j's S buffer
 
   const uint32_t warp = warp_id(), lane = lane_id();
   // CTA -> (query tile, b, h): causal query tiles with the most key tiles start first
@@ -441,16 +466,22 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(BAR_QD, 1);
-    mbar_init(BAR_S, 1);
-    mbar_init(BAR_P, C::COMPUTE_WARPS);
-    mbar_init(BAR_ACC, 1);
-    for (int s = 0; s < NSTAGE; ++s) {
-      mbar_init(BAR_FULL(s), 1);
-      mbar_init(BAR_EMPTY(s), 1);
-    }
-    mbar_init(BAR_DONE, 1);
     mbar_init(BAR_DP, 1);
-    mbar_init(BAR_DS, C::COMPUTE_WARPS);
+    mbar_init(BAR_DPR, C::COMPUTE_WARPS);
+    mbar_init(BAR_ACC, 1);
+    mbar_init(BAR_DONE, 1);
+    for (int bb = 0; bb < 2; ++bb) {
+      mbar_init(BAR_S(bb), 1);
+      mbar_init(BAR_DS(bb), C::COMPUTE_WARPS);
+    }
+    for (int s = 0; s < NK; ++s) {
+      mbar_init(BAR_KF(s), 1);
+      mbar_init(BAR_KE(s), 1);
+    }
+    for (int s = 0; s < NV; ++s) {
+      mbar_init(BAR_VF(s), 1);
+      mbar_init(BAR_VE(s), 1);
+    }
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -469,57 +500,75 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
         tma_load_4d(sQ + pn * C::PANEL_BYTES, &tmQ, BAR_QD, pn * C::PANEL_ELEMS, h, q0, b, pol_res);
         tma_load_4d(sDO + pn * C::PANEL_BYTES, &tmDO, BAR_QD, pn * C::PANEL_ELEMS, h, q0, b, pol_res);
       }
-      int i = 0;
-      for (; i < ntile && !*abort_flag; ++i) {
-        const int s = i % NSTAGE;
-        if (!wait_bounded(BAR_EMPTY(s), ((i / NSTAGE) & 1) ^ 1u, ctl, WHERE_BWD_LOAD)) break;
-        mbar_arrive_expect_tx(BAR_FULL(s), 2 * C::TILE_BYTES);
-        for (int pn = 0; pn < C::NPANEL; ++pn) {
-          tma_load_4d(sK(s) + pn * C::PANEL_BYTES, &tmK, BAR_FULL(s), pn * C::PANEL_ELEMS, hkv, 128 * i, b, pol_str);
-          tma_load_4d(sV(s) + pn * C::PANEL_BYTES, &tmV, BAR_FULL(s), pn * C::PANEL_ELEMS, hkv, 128 * i, b, pol_str);
-        }
+      int nk = 0, nv = 0;                                 // K and V tiles issued
+      for (int i = 0; i < ntile && !*abort_flag; ++i) {
+        const int ks = i % NK, vs = i % NV;
+        if (!wait_bounded(BAR_KE(ks), ((i / NK) & 1) ^ 1u, ctl, WHERE_BWD_LOAD)) break;
+        mbar_arrive_expect_tx(BAR_KF(ks), C::TILE_BYTES);
+        for (int pn = 0; pn < C::NPANEL; ++pn)
+          tma_load_4d(sK(ks) + pn * C::PANEL_BYTES, &tmK, BAR_KF(ks), pn * C::PANEL_ELEMS, hkv, 128 * i, b, pol_str);
+        ++nk;
+        if (!wait_bounded(BAR_VE(vs), ((i / NV) & 1) ^ 1u, ctl, WHERE_BWD_LOAD)) break;
+        mbar_arrive_expect_tx(BAR_VF(vs), C::TILE_BYTES);
+        for (int pn = 0; pn < C::NPANEL; ++pn)
+          tma_load_4d(sV(vs) + pn * C::PANEL_BYTES, &tmV, BAR_VF(vs), pn * C::PANEL_ELEMS, hkv, 128 * i, b, pol_str);
+        ++nv;
       }
       if (*abort_flag) {
+        // copies still in flight land before the CTA exits
         wait_drain(BAR_QD, 0, p.spin_limit);
-        for (int t = (i > NSTAGE ? i - NSTAGE : 0); t < i; ++t)
-          wait_drain(BAR_FULL(t % NSTAGE), (t / NSTAGE) & 1, p.spin_limit);
+        for (int t = (nk > NK ? nk - NK : 0); t < nk; ++t) wait_drain(BAR_KF(t % NK), (t / NK) & 1, p.spin_limit);
+        for (int t = (nv > NV ? nv - NV : 0); t < nv; ++t) wait_drain(BAR_VF(t % NV), (t / NV) & 1, p.spin_limit);
       }
     }
   } else if (warp == C::MMA_WARP) {
     if (lane == 0) {
       const uint64_t dQ = smem_desc(sQ, 16, C::SBO, C::LAYOUT), dDO = smem_desc(sDO, 16, C::SBO, C::LAYOUT);
-      bool ok = wait_bounded(BAR_QD, 0, ctl, WHERE_BWD_MMA);
-      for (int i = 0; ok && i < ntile; ++i) {
-        const int s = i % NSTAGE;
-        ok = wait_bounded(BAR_FULL(s), (i / NSTAGE) & 1, ctl, WHERE_BWD_MMA);
-        if (!ok) break;
+      auto issue_s = [&](int j) -> bool {                // S(j) = Q K_j^T into its buffer
+        if (!wait_bounded(BAR_KF(j % NK), (j / NK) & 1, ctl, WHERE_BWD_MMA)) return false;
         tc_fence_after();
-        const uint64_t dKk = smem_desc(sK(s), 16, C::SBO, C::LAYOUT);
-        const uint64_t dVk = smem_desc(sV(s), 16, C::SBO, C::LAYOUT);
+        const uint64_t dKk = smem_desc(sK(j % NK), 16, C::SBO, C::LAYOUT);
 #pragma unroll
-        for (int kk = 0; kk < C::KSTEPS_SS; ++kk) {      // S = Q K^T
+        for (int kk = 0; kk < C::KSTEPS_SS; ++kk) {
           const uint32_t off = ((kk / C::STEPS_PER_PANEL) * C::PANEL_BYTES + (kk % C::STEPS_PER_PANEL) * 32) >> 4;
-          mma_f16_ss(tmem, dQ + off, dKk + off, C::IDESC_SS, kk > 0);
+          mma_f16_ss(tmem + s_col(j), dQ + off, dKk + off, C::IDESC_SS, kk > 0);
         }
-        mma_commit(BAR_S);                                // the exponentials start on S ...
+        mma_commit(BAR_S(j & 1));
+        return true;
+      };
+      auto issue_dp = [&](int j) -> bool {               // dP(j) = dO V_j^T; V_j's slot then frees
+        if (!wait_bounded(BAR_VF(j % NV), (j / NV) & 1, ctl, WHERE_BWD_MMA)) return false;
+        tc_fence_after();
+        const uint64_t dVk = smem_desc(sV(j % NV), 16, C::SBO, C::LAYOUT);
 #pragma unroll
-        for (int kk = 0; kk < C::KSTEPS_SS; ++kk) {      // ... while dP = dO V^T forms
+        for (int kk = 0; kk < C::KSTEPS_SS; ++kk) {
           const uint32_t off = ((kk / C::STEPS_PER_PANEL) * C::PANEL_BYTES + (kk % C::STEPS_PER_PANEL) * 32) >> 4;
           mma_f16_ss(tmem + 128, dDO + off, dVk + off, C::IDESC_SS, kk > 0);
         }
         mma_commit(BAR_DP);
-        ok = wait_bounded(BAR_DS, i & 1, ctl, WHERE_BWD_MMA);
-        if (!ok) break;
+        mma_commit(BAR_VE(j % NV));
+        return true;
+      };
+      bool ok = wait_bounded(BAR_QD, 0, ctl, WHERE_BWD_MMA) && issue_s(0) && issue_dp(0);
+      for (int i = 0; ok && i < ntile; ++i) {
+        if (i + 1 < ntile) {
+          // S(i+1) into the other buffer: its last dS (tile i-1) was read by dQ(i-1), issued
+          // before; dP(i+1) over dP(i) once the compute warps have read dP(i)
+          if (!issue_s(i + 1)) { ok = false; break; }
+          if (!wait_bounded(BAR_DPR, i & 1, ctl, WHERE_BWD_MMA)) { ok = false; break; }
+          if (!issue_dp(i + 1)) { ok = false; break; }
+        }
+        if (!wait_bounded(BAR_DS(i & 1), (i >> 1) & 1, ctl, WHERE_BWD_MMA)) { ok = false; break; }
         tc_fence_after();
-        const uint64_t dKn = smem_desc(sK(s), C::PANEL_BYTES, C::SBO, C::LAYOUT);
+        const uint64_t dKn = smem_desc(sK(i % NK), C::PANEL_BYTES, C::SBO, C::LAYOUT);
 #pragma unroll
         for (int kk = 0; kk < C::KSTEPS_TS; ++kk) {      // dQ += dS K
           const uint32_t off = (kk * 16 * C::PANEL_ROW) >> 4;
-          // dS of keys 16kk .. 16kk + 15 at 8kk + 32 (kk / 4) (see the compute warps' stores)
-          mma_f16_ts(tmem + 256, tmem + 8u * kk + 32u * (kk / 4), dKn + off, C::IDESC_TS,
+          // dS of keys 16kk .. 16kk + 15 at 8kk + 32 (kk / 4) of tile i's buffer
+          mma_f16_ts(tmem + 256, tmem + s_col(i) + 8u * kk + 32u * (kk / 4), dKn + off, C::IDESC_TS,
                      (i > 0 || kk > 0) ? 1u : 0u);
         }
-        mma_commit(BAR_EMPTY(s));
+        mma_commit(BAR_KE(i % NK));
       }
       if (ok) mma_commit(BAR_ACC);
       mma_commit(BAR_DONE);
@@ -538,15 +587,16 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     for (int i = 0; ok && i < ntile; ++i) {
       const int kb = 128 * i;
       const bool masked = (CAUSAL && i == qt) || kb + 128 > p.S;
-      if (!warp_wait(BAR_S, i & 1, ctl, WHERE_BWD_COMPUTE)) { ok = false; break; }
+      const uint32_t ts = tl + s_col(i);
+      if (!warp_wait(BAR_S(i & 1), (i >> 1) & 1, ctl, WHERE_BWD_COMPUTE)) { ok = false; break; }
       tc_fence_after();
-      // P of this warp's 64 keys, while the tensor core forms dP
+      // P of this warp's 64 keys, while the tensor core may still be forming dP
       float pkeep[2][32];
 #pragma unroll
       for (int cc = 0; cc < 2; ++cc) {
         const int c = 2 * hc + cc;
         uint32_t sv[32];
-        tmem_ld32(tl + 32u * c, sv);
+        tmem_ld32(ts + 32u * c, sv);
         tmem_wait_ld();
 #pragma unroll
         for (int e = 0; e < 32; ++e) {
@@ -561,27 +611,32 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       }
       if (!warp_wait(BAR_DP, i & 1, ctl, WHERE_BWD_COMPUTE)) { ok = false; break; }
       tc_fence_after();
+      uint32_t pv[2][32];
+#pragma unroll
+      for (int cc = 0; cc < 2; ++cc) tmem_ld32(tl + 128u + 32u * (2 * hc + cc), pv[cc]);
+      tmem_wait_ld();
+      // dP(i) is in registers: the MMA warp may form dP(i+1) over it
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(BAR_DPR);
 #pragma unroll
       for (int cc = 0; cc < 2; ++cc) {
         const int c = 2 * hc + cc;
-        uint32_t pv[32];
-        tmem_ld32(tl + 128u + 32u * c, pv);
-        tmem_wait_ld();
         uint32_t dk[16];
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
-          reg_fence(pv[e]);
-          reg_fence(pv[e + 1]);
-          dk[e / 2] = pack_bf16x2(pkeep[cc][e] * (__uint_as_float(pv[e]) - dlt),
-                                  pkeep[cc][e + 1] * (__uint_as_float(pv[e + 1]) - dlt));
+          reg_fence(pv[cc][e]);
+          reg_fence(pv[cc][e + 1]);
+          dk[e / 2] = pack_bf16x2(pkeep[cc][e] * (__uint_as_float(pv[cc][e]) - dlt),
+                                  pkeep[cc][e + 1] * (__uint_as_float(pv[cc][e + 1]) - dlt));
         }
         // dS over this warp's own half of S (already read): keys 32c .. 32c + 31 at 16c + 32hc
-        tmem_st16(tl + static_cast<uint32_t>(16 * c + 32 * hc), dk);
+        tmem_st16(ts + static_cast<uint32_t>(16 * c + 32 * hc), dk);
       }
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(BAR_DS);
+      if (lane == 0) mbar_arrive(BAR_DS(i & 1));
     }
     if (ok && warp_wait(BAR_ACC, 0, ctl, WHERE_BWD_COMPUTE)) {
       tc_fence_after();
@@ -632,7 +687,8 @@ cudaError_t launch_bwd_d(const CUtensorMap* maps, const BwdParams& p, cudaStream
   if ((configured.load() & bit) == 0) {
     e = cudaFuncSetAttribute(bwd_dkdv_kernel<D, CAUSAL>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
     if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(bwd_dq_kernel<D, CAUSAL>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+      e = cudaFuncSetAttribute(bwd_dq_kernel<D, CAUSAL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               DqCfg<D>::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     configured.fetch_or(bit);
   }
@@ -652,7 +708,7 @@ cudaError_t launch_bwd_d(const CUtensorMap* maps, const BwdParams& p, cudaStream
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(static_cast<unsigned>(p.B * p.H) * nqt);
   cfg.blockDim = dim3(C::THREADS);
-  cfg.dynamicSmemBytes = C::SMEM_BYTES;
+  cfg.dynamicSmemBytes = DqCfg<D>::SMEM_BYTES;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
