@@ -267,6 +267,11 @@ __global__ void __launch_bounds__(QCfg<D, ROPE, ROTATE, VARLEN>::THREADS, 1)
   };
   const int my_blocks = (nblocks - static_cast<int>(blockIdx.x) + static_cast<int>(gridDim.x) - 1) /
                         static_cast<int>(gridDim.x);
+  // This grid may be launched while the previous grid on the stream is still running
+  // (programmatic dependent launch), and that grid may have produced x, the signs, the offsets
+  // or the rotary table: nothing is read from global memory before it has completed.  What
+  // comes before this point (barrier set-up, tensor-map prefetch) overlaps its tail.
+  grid_dependency_wait();
   // Fixed-length launches start their first loads at once, before the tables below (whose
   // global reads would otherwise delay them); packed batches check their offsets first.
   if (!VARLEN && threadIdx.x == 0)
@@ -301,15 +306,14 @@ __global__ void __launch_bounds__(QCfg<D, ROPE, ROTATE, VARLEN>::THREADS, 1)
     if (threadIdx.x == 0) bad |= p.cu_seqlens[0] != 0 || p.cu_seqlens[p.n_seq] != p.S;
     if (__syncthreads_or(bad)) {
       grid_launch_dependents();
-      grid_dependency_wait();
       if (threadIdx.x == 0 && atomicCAS(p.err_word, 0, 1 /* ATTN_ERR_INVALID_ARG */) == 0) atomicExch(p.err_info, 11);
       return;
     }
   }
   __syncthreads();
-  // Consecutive quantiser launches on a stream overlap: the next one's CTAs may start on the SMs
-  // this one's CTAs leave (one CTA per SM, so every CTA of this grid is running by now), read
-  // and transform their first blocks, and wait for this grid to complete before they write.
+  // The next grid on the stream may start its own set-up on the SMs this grid's CTAs leave
+  // (one CTA per SM, so every CTA of this grid is running by now); it reads nothing before
+  // this grid has completed.
   grid_launch_dependents();
   if (VARLEN && threadIdx.x == 0)
     for (int k = 0; k < NSTAGE && k < my_blocks; ++k) issue(k);
@@ -336,7 +340,6 @@ __global__ void __launch_bounds__(QCfg<D, ROPE, ROTATE, VARLEN>::THREADS, 1)
   };
 
   int n_stores = 0;                  // lane 0: tensor stores this warp has issued from its rows of the buffer
-  bool may_write = false;            // this thread has waited for the previous grid on the stream
   for (int k = g, it = 0; k < my_blocks; k += C::G, ++it) {
     // Blocks are numbered head-fastest: the groups running at one time read all heads of the
     // same tokens, i.e. contiguous memory.
@@ -459,10 +462,6 @@ __global__ void __launch_bounds__(QCfg<D, ROPE, ROTATE, VARLEN>::THREADS, 1)
     for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
     float* wm = warp_max + C::GWARPS * (it & 1);
     if (lane == 0) wm[gwarp] = amax;
-    if (!may_write) {                 // nothing is written to global memory before this
-      grid_dependency_wait();
-      may_write = true;
-    }
     // the block's one group-wide step: the maximum over its rows (and whether any wait failed)
     if (group_bar_or(gbar, C::GTHREADS, !ok)) break;
     amax = wm[0];

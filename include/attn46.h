@@ -326,13 +326,10 @@ int attn_bwd_noalloc(const void* q, const void* k, const void* v, const void* o,
  *            x' = (x * signs) H_D / sqrt(D), H_D the Sylvester Hadamard
  *            matrix; use the same signs for Q and K.
  *   out[e] = E4M3_round_nearest_even_saturating(x'[e] / scale).
- *   Overlap: consecutive quantiser launches on one stream (this function, its
- *   RoPE and packed forms) may run concurrently -- a launch reads its inputs
- *   and transforms its first blocks while the quantiser launch before it is
- *   finishing, and writes nothing until that launch has completed.  So the
- *   input (x, signs, the rotary table, cu_seqlens) of a quantiser call must
- *   not be an output of the quantiser call just before it on the stream.
- *   Any other kernel before it completes first, as usual.
+ *   Ordering: the launch may start while the kernel before it on the stream
+ *   is finishing (programmatic dependent launch), but only its set-up runs
+ *   then: it reads no input before that kernel has completed and its writes
+ *   are visible, so stream order holds for every argument.
  */
 int hadamard_rotate_quant_fp8(const void* x, void* out, float* scale, const float* signs,
                               int B, int H, int S, int D, void* stream);
@@ -353,8 +350,7 @@ int hadamard_rotate_quant_fp8(const void* x, void* out, float* scale, const floa
  *   its tensor (the same arithmetic); the three tensors' blocks are one
  *   grid's work list, so the launch has one start-up and one tail instead of
  *   three.  The six outputs must overlap neither each other nor the inputs.
- *   Overlap with neighbouring quantiser launches and errors as
- *   hadamard_rotate_quant_fp8.
+ *   Ordering and errors as hadamard_rotate_quant_fp8.
  */
 int hadamard_rotate_quant_fp8_qkv(const void* q, const void* k, const void* v, void* q8, void* k8,
                                   void* v8, float* q_scale, float* k_scale, float* v_scale,
