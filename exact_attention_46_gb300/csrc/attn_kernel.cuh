@@ -839,28 +839,52 @@ __global__ void __launch_bounds__(AttnCfg<D, FP8>::THREADS, 1)
 
       float m_run = -INFINITY;
       float l_run = 0.f;
-      // Per-tile FP8 scales are read one key tile ahead, so the loads' latency hides behind a
-      // whole step (S is often ready at once, with nothing else to wait for).
-      float sk_next = 1.f, sv_next = 1.f;
+      // FP8 per-key-tile factors, lane l holding those of tile 32 (j / 32) + l: the exponent
+      // multiplier c_log2 sq sk, the numerators' offset bias = log2(sv / sv_max) (V's block scale
+      // relative to the largest, folded into P) and 2^-bias, which takes it out of the row sum.
+      // A zero scale (a block of zeros) counts as 2^-30 of the largest: its numerators vanish in
+      // E4M3, the row sum still takes them at full weight.  The raw scales of the next 32 tiles
+      // are read 32 tiles ahead, so their latency hides behind the loop.
+      float cm_l = 1.f, bias_l = 0.f, ir_l = 1.f, skr_next = 1.f, svr_next = 1.f;
+      const float csq = p.c_log2 * sq, sv_floor = sv_max * 0x1p-30f, lg_svmax = __log2f(sv_max);
+      auto read_raw = [&](int jb, float& skr, float& svr) {
+        const int jj = jb + static_cast<int>(lane);
+        skr = 1.f;
+        svr = 1.f;
+        if (jj < nt) {
+          if (p.k_scale != nullptr) skr = p.k_scale[kv_tile0 + jj];
+          if (p.v_scale != nullptr) svr = p.v_scale[kv_tile0 + jj];
+        }
+      };
+      auto derive = [&](float skr, float svr) {
+        cm_l = csq * skr;
+        bias_l = __log2f(fmaxf(svr, sv_floor)) - lg_svmax;
+        ir_l = ex2(-bias_l);
+      };
+      float cm_n = p.c_log2, bias_n = 0.f, ir_n = 1.f;    // FP8: tile j's factors, fetched a tile ahead
       if (FP8) {
-        if (p.k_scale != nullptr) sk_next = p.k_scale[kv_tile0];
-        if (p.v_scale != nullptr) sv_next = p.v_scale[kv_tile0];
+        float skr, svr;
+        read_raw(0, skr, svr);
+        derive(skr, svr);
+        if (nt > 32) read_raw(32, skr_next, svr_next);
+        cm_n = __shfl_sync(0xffffffffu, cm_l, 0);
+        bias_n = __shfl_sync(0xffffffffu, bias_l, 0);
+        ir_n = __shfl_sync(0xffffffffu, ir_l, 0);
       }
       for (int j = 0; j < nt; ++j) {
         float cmul = p.c_log2, bias = 0.f, inv_r = 1.f;
         if (FP8) {
-          const float sk = sk_next;
-          const float sv_raw = sv_next;
-          if (j + 1 < nt) {
-            if (p.k_scale != nullptr) sk_next = p.k_scale[kv_tile0 + j + 1];
-            if (p.v_scale != nullptr) sv_next = p.v_scale[kv_tile0 + j + 1];
+          cmul = cm_n;
+          bias = bias_n;
+          inv_r = ir_n;
+          const int jn = j + 1;
+          if ((jn & 31) == 0 && jn < nt) {
+            derive(skr_next, svr_next);
+            if (jn + 32 < nt) read_raw(jn + 32, skr_next, svr_next);
           }
-          // a zero scale (a block of zeros) as 2^-30 of the largest: its numerators vanish in E4M3,
-          // the row sum still takes them at full weight
-          const float sv = fmaxf(sv_raw, sv_max * 0x1p-30f);
-          cmul *= sq * sk;
-          bias = __log2f(sv / sv_max);
-          inv_r = sv_max / sv;
+          cm_n = __shfl_sync(0xffffffffu, cm_l, jn & 31);
+          bias_n = __shfl_sync(0xffffffffu, bias_l, jn & 31);
+          ir_n = __shfl_sync(0xffffffffu, ir_l, jn & 31);
         }
         if (!warp_wait(BAR_S_FULL(t), sc & 1, ctl, WHERE_SOFTMAX)) { ok = false; break; }
         ++sc;

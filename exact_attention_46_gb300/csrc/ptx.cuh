@@ -151,12 +151,13 @@ __device__ __forceinline__ void bulk_wait_read_1() {
 // Wait until every committed bulk store has completed.
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
-// Order this thread's generic-proxy shared-memory writes before later async-proxy (TMA) reads.
+// One 16-byte shared-memory store.
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
                : "memory");
 }
 
+// Order this thread's generic-proxy shared-memory writes before later async-proxy (TMA) reads.
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
@@ -418,10 +419,13 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 
 // Four floats -> packed E4M3x4 (v0 in bits 0..7), round to nearest even, saturating.
 __device__ __forceinline__ uint32_t pack_e4m3x4(float v0, float v1, float v2, float v3) {
-  uint16_t lo, hi;
-  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(lo) : "f"(v1), "f"(v0));
-  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(hi) : "f"(v3), "f"(v2));
-  return static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+  uint32_t r;
+  asm("{\n\t.reg .b16 lo, hi;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 lo, %2, %1;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 hi, %4, %3;\n\t"
+      "mov.b32 %0, {lo, hi};\n\t}"
+      : "=r"(r) : "f"(v0), "f"(v1), "f"(v2), "f"(v3));
+  return r;
 }
 
 }  // namespace ea46
