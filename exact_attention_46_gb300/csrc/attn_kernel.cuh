@@ -159,16 +159,23 @@ __device__ __forceinline__ void wait_drain(uint32_t bar, uint32_t parity, long l
 }
 
 // Epilogue of one key range of a split tail block: the warp's 32 rows of partial O
-// (accumulator * inv_l, fp32) and their lse (log2 units) go to the scratch, kept in L2 by an
-// evict-last hint for split_merge_kernel, and O_t goes back to the MMA warp.  Rows past the
-// sequence (valid = false) store nothing.
+// (accumulator * inv_l, fp32) and their lse (log2 units) go to the scratch for
+// split_merge_kernel (stores that bypass L1), and O_t goes back to the MMA warp.  The rows go
+// through the warp's two 2 KB staging buffers, 16 columns at a time, so that each store
+// instruction writes 8 rows x 64 bytes rather than 32 rows x 16 bytes.  Rows past the sequence
+// (n_valid: the warp's rows that lie inside it) store nothing.  Inlined: as a call, the
+// registers live across it spilled in the E4M3 kernel and slowed its key loop.
 template <int D, int NT>
-__device__ __noinline__ void split_store(const SplitParams& sp, int slot, int part, int t, int row_local, bool valid,
-                                         uint32_t o_addr, float inv_l, float lse2, uint32_t bar_o_empty) {
+__device__ __forceinline__ void split_store(const SplitParams& sp, int slot, int part, int t, int row_local,
+                                            bool valid, uint32_t o_addr, float inv_l, float lse2,
+                                            uint32_t bar_o_empty, uint32_t ost, int n_valid) {
   constexpr int ROWS = 128 * NT;
   const uint32_t lane = lane_id();
   const size_t r = (static_cast<size_t>(slot) * sp.n_parts + part) * ROWS + 128 * t + row_local;
-  float* po = sp.part_o + r * D;
+  // this warp's first row in the scratch; its 32 rows are consecutive there
+  float* pw = sp.part_o + (r - lane) * D;
+  if (lane == 0) bulk_wait_read_all();      // the item before's tensor stores have read the buffers
+  __syncwarp();
 #pragma unroll 1
   for (int c = 0; c < D / 32; ++c) {
     uint32_t o[32];
@@ -176,13 +183,34 @@ __device__ __noinline__ void split_store(const SplitParams& sp, int slot, int pa
     tmem_wait_ld();
 #pragma unroll
     for (int i = 0; i < 32; ++i) reg_fence(o[i]);
-    if (valid) {
 #pragma unroll
-      for (int v4 = 0; v4 < 8; ++v4)
-        __stcg(reinterpret_cast<float4*>(po + 32 * c + 4 * v4),
-               make_float4(__uint_as_float(o[4 * v4]) * inv_l, __uint_as_float(o[4 * v4 + 1]) * inv_l,
-                           __uint_as_float(o[4 * v4 + 2]) * inv_l, __uint_as_float(o[4 * v4 + 3]) * inv_l));
+    for (int h = 0; h < 2; ++h) {
+      // 16 columns of the warp's 32 rows through buffer h (row = lane, 64 bytes, 64-byte swizzle),
+      // then out with each store instruction covering 8 rows x 64 bytes
+      const uint32_t buf = ost + h * (32 * 64);
+#pragma unroll
+      for (int v4 = 0; v4 < 4; ++v4) {
+        const uint32_t addr = buf + lane * 64 + ((v4 ^ ((lane >> 1) & 3)) << 4);
+        const int e = 16 * h + 4 * v4;
+        st_shared_v4(addr, __float_as_uint(__uint_as_float(o[e]) * inv_l), __float_as_uint(__uint_as_float(o[e + 1]) * inv_l),
+                     __float_as_uint(__uint_as_float(o[e + 2]) * inv_l), __float_as_uint(__uint_as_float(o[e + 3]) * inv_l));
+      }
     }
+    __syncwarp();
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const uint32_t buf = ost + h * (32 * 64);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int row = 8 * i + static_cast<int>(lane >> 2), piece = static_cast<int>(lane & 3);
+        float4 f;
+        asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                     : "=f"(f.x), "=f"(f.y), "=f"(f.z), "=f"(f.w)
+                     : "r"(buf + row * 64 + ((piece ^ ((row >> 1) & 3)) << 4)));
+        if (row < n_valid) __stcg(reinterpret_cast<float4*>(pw + static_cast<size_t>(row) * D + 32 * c + 16 * h + 4 * piece), f);
+      }
+    }
+    __syncwarp();
   }
   tc_fence_before();
   __syncwarp();
@@ -1064,8 +1092,11 @@ __global__ void __launch_bounds__(AttnCfg<D, FP8>::THREADS, 1)
         // a key range of a cut block (recomputed from n: nothing of it stays live in the loop)
         const int u = item_of(n) - sp.n_whole;
         if (u >= 0) {
+          const int wrow0 = it.q0 + 128 * t + 32 * wq;   // this warp's first row
           split_store<D, NT>(sp, u % sp.n_tail, u / sp.n_tail, t, row_local, valid, o_addr, inv_l,
-                             m_run + __log2f(l_run), BAR_O_EMPTY(t));
+                             m_run + __log2f(l_run), BAR_O_EMPTY(t),
+                             sOst + static_cast<uint32_t>(warp) * C::OST_WARP_BYTES,
+                             seq_len(it) - wrow0);
           continue;
         }
       }
