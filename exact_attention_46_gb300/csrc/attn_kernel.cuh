@@ -1116,8 +1116,12 @@ __global__ void __launch_bounds__(AttnCfg<D, FP8>::THREADS, 1)
           pk[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
         }
         if constexpr (STAGE_O) {
-          // buffer c & 1 is free once at most one store (chunk c - 1's) still reads its buffer
-          if (lane == 0 && c >= 2) bulk_wait_read_1();
+          // buffer c & 1 is free once at most one store (chunk c - 1's) still reads its buffer;
+          // at chunk 0 the item before's last stores (same buffers) must have read them all
+          if (lane == 0) {
+            if (c == 0) bulk_wait_read_all();
+            else if (c >= 2) bulk_wait_read_1();
+          }
           __syncwarp();
           const uint32_t buf = ost + (c & 1) * (32 * 64);
 #pragma unroll
