@@ -204,9 +204,11 @@ __device__ __forceinline__ void split_store(const SplitParams& sp, int slot, int
       for (int i = 0; i < 4; ++i) {
         const int row = 8 * i + static_cast<int>(lane >> 2), piece = static_cast<int>(lane & 3);
         float4 f;
+        // (a memory clobber: the read stays after the __syncwarp that publishes the other lanes' rows)
         asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
                      : "=f"(f.x), "=f"(f.y), "=f"(f.z), "=f"(f.w)
-                     : "r"(buf + row * 64 + ((piece ^ ((row >> 1) & 3)) << 4)));
+                     : "r"(buf + row * 64 + ((piece ^ ((row >> 1) & 3)) << 4))
+                     : "memory");
         if (row < n_valid) __stcg(reinterpret_cast<float4*>(pw + static_cast<size_t>(row) * D + 32 * c + 16 * h + 4 * piece), f);
       }
     }
